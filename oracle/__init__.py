@@ -1,0 +1,243 @@
+"""fp64 CPU oracle for causal grouped-query attention: forward (O, LSE) and the
+backward pass from a saved log-sum-exp, plus the interleaved RoPE backward.
+
+TEST INFRASTRUCTURE ONLY. Nothing in the product path imports this package:
+only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+legs of ``bench.py`` may use it. It shares no code with the CUDA path.
+
+What it computes, and where the pages define it
+-----------------------------------------------
+Notation: S = seq_len, H = n_heads, Hk = n_kv_heads, G = H / Hk, d = head_dim,
+sigma = scale. Query head h reads kv head g(h) = floor(h / G) ("blocked" GQA;
+10_backward_attention.wgsl, kernel ``attention_backward``, ``kv_h = h /
+q_per_group``; tang ``llm.rs``, ``causal_attention_fused``, ``kv_head = head /
+heads_per_group``). Key j is visible to query i iff seg[i] <= j <= i
+(10_backward_attention.wgsl, ``attention_backward``: the ``doc_start`` /
+``causal_len`` test).
+
+Forward (tang ``llm.rs``, ``causal_attention_fused``: row max, sum of exps,
+weighted V; document mask added as in the wgsl kernels):
+    s_ij = sigma * q_i . k_j             (allowed pairs)
+    LSE_i = m_i + ln sum_j exp(s_ij - m_i),   m_i = max_j s_ij
+    O_i = sum_j exp(s_ij - LSE_i) v_j
+
+Backward from a given LSE (10_backward_attention.wgsl header and kernel
+``attention_backward``; explicit-matrix form of tang ``llm.rs``,
+``GpuTrainModule for GpuCausalAttention::backward``):
+    P_ij  = exp(s_ij - LSE_i) if allowed else 0
+    dP_ij = dO_i . v_j
+    D_i   = sum_j P_ij dP_ij
+    dS_ij = sigma * P_ij (dP_ij - D_i)
+    dQ_i += sum_j dS_ij k_j
+    dK_j += sum_{h in group} sum_i dS_ij q_i
+    dV_j += sum_{h in group} sum_i P_ij dO_i
+Gradients accumulate (``+=``) into the arrays passed in.
+
+Interleaved RoPE backward (10_backward_attention.wgsl, ``rope_q_backward`` /
+``rope_k_backward``; tang ``llm.rs``, ``interleaved_rope_backward`` and the
+f64 angle tables of ``GpuInterleavedRoPE::new``): for pair p < d/2 at position
+t = pos_offset + s, theta = t * base^(-2p/d) computed in fp64,
+    (x0, x1) <- (x0 cos theta + x1 sin theta, -x0 sin theta + x1 cos theta).
+
+The explicit matrices P, dP, dS are materialised for one head and one block of
+query rows at a time (keys 0 .. last row of the block), which bounds memory;
+every row is computed from its own definition, so the block size changes
+nothing but rounding order inside the library matrix products.
+
+Pins: every function here is checked by ``tests/test_oracle_pins.py`` against
+central finite differences, closed forms (K = 0, S = 1, position 0), exact
+invariants (sum_j dS_ij = 0, no cross-document flow, GQA group sums) and an
+independent float64 autograd of the forward definition.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = ["fwd", "bwd", "bwd_rows", "bwd_dkdv_keys", "row_terms", "rope_bwd",
+           "allowed"]
+
+_ROW_BLOCK = 256
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def allowed(seg: np.ndarray, rows: np.ndarray, n_keys: int) -> np.ndarray:
+    """Boolean mask [len(rows), n_keys]: key j visible to query i iff seg[i] <= j <= i."""
+    rows = np.asarray(rows, dtype=np.int64)
+    j = np.arange(n_keys, dtype=np.int64)[None, :]
+    lo = np.asarray(seg, dtype=np.int64)[rows][:, None]
+    return (j >= lo) & (j <= rows[:, None])
+
+
+def _check_shapes(S, H, Hk, d):
+    if Hk <= 0 or H % Hk != 0:
+        raise ValueError("n_heads must be a positive multiple of n_kv_heads")
+    if d <= 0:
+        raise ValueError("head_dim must be positive")
+
+
+def _head_cols(h, d):
+    return slice(h * d, (h + 1) * d)
+
+
+def _blocks(rows: np.ndarray):
+    for b in range(0, len(rows), _ROW_BLOCK):
+        yield rows[b:b + _ROW_BLOCK]
+
+
+def fwd(Q, K, V, seg, n_heads, n_kv_heads, head_dim, scale, rows=None):
+    """Forward attention: returns (O [S, H*d], LSE [S, H]) in fp64.
+
+    With ``rows`` given, only those query rows are filled (others stay zero).
+    LSE is the natural log, scale included, over allowed keys only, so that
+    exp(sigma q.k - LSE) sums to one over a row.
+    """
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    S = Q.shape[0]
+    H, Hk, d = n_heads, n_kv_heads, head_dim
+    _check_shapes(S, H, Hk, d)
+    G = H // Hk
+    O = np.zeros((S, H * d))
+    LSE = np.zeros((S, H))
+    all_rows = np.arange(S, dtype=np.int64) if rows is None else np.sort(np.asarray(rows, np.int64))
+    for h in range(H):
+        g = h // G
+        Kg, Vg = K[:, _head_cols(g, d)], V[:, _head_cols(g, d)]
+        for r in _blocks(all_rows):
+            n_keys = int(r[-1]) + 1
+            s = scale * (Q[r, _head_cols(h, d)] @ Kg[:n_keys].T)
+            s = np.where(allowed(seg, r, n_keys), s, -np.inf)
+            m = s.max(axis=1)
+            lse = m + np.log(np.exp(s - m[:, None]).sum(axis=1))
+            p = np.exp(s - lse[:, None])
+            O[r, _head_cols(h, d)] = p @ Vg[:n_keys]
+            LSE[r, h] = lse
+    return O, LSE
+
+
+def row_terms(Q, K, V, dO, LSE, seg, h, n_heads, n_kv_heads, head_dim, scale, rows):
+    """Explicit P, dP, D, dS for query head ``h`` and query ``rows``.
+
+    Returns a dict of fp64 arrays; P, dP, dS are [len(rows), last_row + 1].
+    """
+    Q, K, V, dO, LSE = _f64(Q), _f64(K), _f64(V), _f64(dO), _f64(LSE)
+    H, Hk, d = n_heads, n_kv_heads, head_dim
+    _check_shapes(Q.shape[0], H, Hk, d)
+    g = h // (H // Hk)
+    r = np.asarray(rows, dtype=np.int64)
+    n_keys = int(r.max()) + 1
+    Kg, Vg = K[:n_keys, _head_cols(g, d)], V[:n_keys, _head_cols(g, d)]
+    s = scale * (Q[r, _head_cols(h, d)] @ Kg.T)
+    mask = allowed(seg, r, n_keys)
+    P = np.exp(np.where(mask, s - LSE[r, h][:, None], -np.inf))
+    dP = np.where(mask, dO[r, _head_cols(h, d)] @ Vg.T, 0.0)
+    D = (P * dP).sum(axis=1)
+    dS = scale * P * (dP - D[:, None])
+    return {"P": P, "dP": dP, "D": D, "dS": dS, "keys": n_keys, "g": g}
+
+
+def bwd(Q, K, V, dO, LSE, seg, n_heads, n_kv_heads, head_dim, scale,
+        dQ=None, dK=None, dV=None):
+    """Backward from the given LSE; accumulates into dQ, dK, dV (fp64, created
+    as zeros when not given) and returns them.
+
+    Follows the explicit-matrix backward of tang ``llm.rs``
+    (``GpuCausalAttention::backward``: recompute P, dP = dO V^T, dV += P^T dO,
+    D_i = sum_k dP P, dS = P (dP - D) scale, dQ += dS K, dK += dS^T Q, with the
+    kv group shared by ``+=``), using the saved LSE and the document mask of
+    10_backward_attention.wgsl (``attention_backward``: P = exp(scale q.k - lse)).
+    """
+    Q, K, V, dO, LSE = _f64(Q), _f64(K), _f64(V), _f64(dO), _f64(LSE)
+    S = Q.shape[0]
+    H, Hk, d = n_heads, n_kv_heads, head_dim
+    _check_shapes(S, H, Hk, d)
+    dQ = np.zeros((S, H * d)) if dQ is None else dQ
+    dK = np.zeros((S, Hk * d)) if dK is None else dK
+    dV = np.zeros((S, Hk * d)) if dV is None else dV
+    all_rows = np.arange(S, dtype=np.int64)
+    for h in range(H):
+        g = h // (H // Hk)
+        for r in _blocks(all_rows):
+            t = row_terms(Q, K, V, dO, LSE, seg, h, H, Hk, d, scale, r)
+            n = t["keys"]
+            Kg = K[:n, _head_cols(g, d)]
+            dQ[r, _head_cols(h, d)] += t["dS"] @ Kg
+            dK[:n, _head_cols(g, d)] += t["dS"].T @ Q[r, _head_cols(h, d)]
+            dV[:n, _head_cols(g, d)] += t["P"].T @ dO[r, _head_cols(h, d)]
+    return dQ, dK, dV
+
+
+def bwd_rows(Q, K, V, dO, LSE, seg, n_heads, n_kv_heads, head_dim, scale, rows, heads=None):
+    """dQ of the backward for the given query ``rows`` (all heads, or ``heads``).
+
+    Returns an fp64 array [len(rows), H*d]; columns of heads not asked for are
+    zero. Each row follows the same definition as ``bwd``; this only restricts
+    which outputs are formed, for spot checks at sizes where the whole backward
+    would take too long.
+    """
+    H, Hk, d = n_heads, n_kv_heads, head_dim
+    Q, K, V, dO, LSE = _f64(Q), _f64(K), _f64(V), _f64(dO), _f64(LSE)
+    r_all = np.asarray(rows, dtype=np.int64)
+    out = np.zeros((len(r_all), H * d))
+    heads = range(H) if heads is None else heads
+    for h in heads:
+        g = h // (H // Hk)
+        for b in range(0, len(r_all), _ROW_BLOCK):
+            r = r_all[b:b + _ROW_BLOCK]
+            t = row_terms(Q, K, V, dO, LSE, seg, h, H, Hk, d, scale, r)
+            out[b:b + len(r), _head_cols(h, d)] = t["dS"] @ K[:t["keys"], _head_cols(g, d)]
+    return out
+
+
+def bwd_dkdv_keys(Q, K, V, dO, LSE, seg, n_heads, n_kv_heads, head_dim, scale, keys, kv_heads=None):
+    """dK and dV of the backward for the given key positions ``keys``.
+
+    Returns two fp64 arrays [len(keys), Hk*d] (kv heads not asked for stay
+    zero). Every query row that can see one of the keys (rows >= min(keys)) is
+    formed in full, since its D needs the whole row; only the key columns asked
+    for are summed.
+    """
+    Q, K, V, dO, LSE = _f64(Q), _f64(K), _f64(V), _f64(dO), _f64(LSE)
+    S = Q.shape[0]
+    H, Hk, d = n_heads, n_kv_heads, head_dim
+    keys = np.asarray(keys, dtype=np.int64)
+    dK = np.zeros((len(keys), Hk * d))
+    dV = np.zeros((len(keys), Hk * d))
+    if len(keys) == 0:
+        return dK, dV
+    rows = np.arange(int(keys.min()), S, dtype=np.int64)
+    kv_heads = range(Hk) if kv_heads is None else kv_heads
+    G = H // Hk
+    for g in kv_heads:
+        for h in range(g * G, (g + 1) * G):
+            for r in _blocks(rows):
+                t = row_terms(Q, K, V, dO, LSE, seg, h, H, Hk, d, scale, r)
+                sel = keys < t["keys"]
+                kk = keys[sel]
+                dK[sel, _head_cols(g, d)] += t["dS"][:, kk].T @ Q[r, _head_cols(h, d)]
+                dV[sel, _head_cols(g, d)] += t["P"][:, kk].T @ dO[r, _head_cols(h, d)]
+    return dK, dV
+
+
+def rope_bwd(dX, n_heads, head_dim, pos_offset=0, base=10000.0):
+    """Interleaved RoPE backward (transposed rotation), returned as a new fp64 array.
+
+    dX is [S, n_heads*head_dim]; pair p of head h at row s is columns
+    (h*d + 2p, h*d + 2p + 1); the angle is (pos_offset + s) * base^(-2p/d) in fp64.
+    """
+    X = _f64(dX).copy()
+    S = X.shape[0]
+    d = head_dim
+    if d % 2:
+        raise ValueError("head_dim must be even for RoPE")
+    X = X.reshape(S, n_heads, d // 2, 2)
+    pos = (np.arange(S, dtype=np.float64) + pos_offset)[:, None]
+    inv_freq = np.array([base ** (-(2.0 * p) / d) for p in range(d // 2)], dtype=np.float64)
+    theta = pos * inv_freq[None, :]                     # [S, d/2]
+    c, s = np.cos(theta)[:, None, :], np.sin(theta)[:, None, :]
+    x0, x1 = X[..., 0].copy(), X[..., 1].copy()
+    X[..., 0] = x0 * c + x1 * s
+    X[..., 1] = -x0 * s + x1 * c
+    return X.reshape(S, n_heads * d)
