@@ -1,0 +1,429 @@
+"""Benchmark: causal GQA attention backward from a saved LSE on GB300.
+
+One step = the whole hot path over one batch of synthetic input: zero the
+gradient buffers, attention backward (D pre-pass, key-tile and query-tile
+work), then the interleaved RoPE backward on dQ and dK (the 16k-token
+workload's recipe). Metric: attention-backward TFLOP/s counted over unmasked
+(query, key) pairs, 10 * head_dim * n_heads * N_pairs per step (five d-deep
+contractions per pair and head), and the fraction of the dense TF32 tensor
+peak.
+
+Prints ONE JSON line (rank 0). ``--impl reference`` times the fp64 CPU
+oracle instead, on a bounded sample of the same workload.
+
+Multi-GPU (torchrun): every rank runs its own copy of the workload (the kv-head
+groups, batches or documents of a training step are independent problems), so
+per-GPU work is fixed and scaling is weak; the only collectives are the
+barrier and the max-over-ranks of the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")   # the oracle's thread pool is the parallelism
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "attn-backward TFLOP/s (unmasked pairs) and % of GB300 dense TF32 peak"
+UNIT = "TFLOP/s"
+
+
+# ---------------------------------------------------------------------------
+# host-side helpers (covered by CPU tests)
+# ---------------------------------------------------------------------------
+def counted_flops(head_dim: int, n_heads: int, pairs: int) -> float:
+    """Five d-deep contractions (QK^T, dO V^T, P^T dO, dS^T Q, dS K) per pair and head."""
+    return 10.0 * head_dim * n_heads * pairs
+
+
+def dist_env() -> tuple[int, int, int]:
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Max of a host float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        p["source"] = "measured"
+        return p
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# Nominal dense rates (TFLOP/s): bf16 2250, tf32 1100. A TF32 contraction is
+# measured against the measured bf16 peak times this ratio.
+TF32_PER_BF16 = 1100.0 / 2250.0
+
+
+def tf32_peak(peaks: dict, sustained: bool) -> float:
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    return peaks[key] * TF32_PER_BF16
+
+
+def fp32_simt_peak_tflops(n_sm: int, max_mhz: float) -> float:
+    """CUDA-core fp32 peak: 128 FMA lanes per SM, 2 flops per FMA, at the max SM clock."""
+    return n_sm * 128 * 2 * max_mhz * 1e6 / 1e12
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id, self.proc, self.lines = gpu_id, None, []
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self) -> dict:
+        return summarize_clocks(self.lines)
+
+
+def summarize_clocks(lines: list[str]) -> dict:
+    sm, mx, reasons = [], [], set()
+    names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    for ln in lines:
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 8:
+            continue
+        try:
+            sm.append(float(parts[0]))
+            mx.append(float(parts[1]))
+        except ValueError:
+            continue
+        for name, val in zip(names, parts[4:8]):
+            if val.lower() in ("active", "1", "yes"):
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+    # median over samples under load (clock above half of max)
+    top = max(mx) if mx else max(sm)
+    loaded = [s for s in sm if s >= 0.5 * top] or sm
+    return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": top, "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+def _source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "causal_gqa_attention_attn_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(stage: str, workload: str):
+    """DRAM bytes per launch of the dominant stage from the committed ncu
+    summary, when it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(f"{workload}:{stage}")
+    if not rec or rec.get("source_hash") != _source_hash():
+        return None
+    return rec.get("bytes_per_launch")
+
+
+def _gpu_uuid(torch, dev) -> str | None:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+def run_gpu(args) -> dict | None:
+    import torch
+    import causal_gqa_attention_attn_gb300 as ga
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.make_inputs(w, seed=w.seed + rank)      # each rank: its own problem
+    S, H, Hk, d, sc = w.seq_len, w.n_heads, w.n_kv_heads, w.head_dim, w.scale
+    pairs = workloads.n_pairs(x["seg"])
+    flops = counted_flops(d, H, pairs)
+    impl_fn = ga.attn_bwd if args.path == "auto" else ga.attn_bwd_simt
+
+    host = {k: torch.from_numpy(np.ascontiguousarray(x[k])).pin_memory()
+            for k in ("Q", "K", "V", "dO")}
+    host["seg"] = torch.from_numpy(x["seg"].astype(np.int32)).pin_memory()
+    t = {k: v.to(dev) for k, v in host.items()}
+    _, LSE = ga.attn_fwd_lse(t["Q"], t["K"], t["V"], t["seg"], H, Hk, d, sc)   # setup, untimed
+    host["LSE"] = LSE.cpu().pin_memory()
+    t["LSE"] = LSE
+    dQ = torch.zeros(S, H * d, device=dev)
+    dK = torch.zeros(S, Hk * d, device=dev)
+    dV = torch.zeros(S, Hk * d, device=dev)
+    ws = torch.empty(ga.workspace_bytes(S, H, Hk, d), dtype=torch.uint8, device=dev)
+
+    def step():
+        dQ.zero_()
+        dK.zero_()
+        dV.zero_()
+        impl_fn(t["Q"], t["K"], t["V"], t["dO"], t["LSE"], t["seg"], dQ, dK, dV, H, Hk, d, sc,
+                workspace=ws)
+        if w.rope:
+            ga.rope_bwd_inplace(dQ, H, d, 0, 10000.0)
+            ga.rope_bwd_inplace(dK, Hk, d, 0, 10000.0)
+
+    for _ in range(args.warmup):
+        step()
+    ga.read_device_status(ws)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in ev_a + ev_b:            # create the underlying cudaEvent_t now
+        e.record()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    launches0 = ga.launch_count()
+    with ClockSampler(_gpu_uuid(torch, dev)) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        start.record()
+        for k in range(K):
+            ga.profile_events(ev_a[k], ev_b[k])
+            step()
+        end.record()
+        torch.cuda.synchronize()
+        barrier()
+    launches = ga.launch_count() - launches0
+    stage = ga.profile_stage_name()
+    ga.read_device_status(ws)
+    ms = start.elapsed_time(end)
+    ms_max = max_over_ranks(ms, dev)
+    stage_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / K
+    value = world * flops / (ms_max / K / 1e3) / 1e12
+
+    # end to end through the public API with host buffers (pinned) every step
+    outs = {"dQ": torch.empty(dQ.shape, pin_memory=True), "dK": torch.empty(dK.shape, pin_memory=True),
+            "dV": torch.empty(dV.shape, pin_memory=True)}
+    h2d = sum(host[k].numel() * host[k].element_size() for k in ("Q", "K", "V", "dO", "LSE", "seg"))
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+
+    def e2e_step():
+        for k in ("Q", "K", "V", "dO", "LSE", "seg"):
+            t[k].copy_(host[k], non_blocking=True)
+        step()
+        outs["dQ"].copy_(dQ, non_blocking=True)
+        outs["dK"].copy_(dK, non_blocking=True)
+        outs["dV"].copy_(dV, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record()
+    for _ in range(K):
+        e2e_step()
+    e2.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2), dev)
+    e2e_value = world * flops / (e2e_ms / K / 1e3) / 1e12
+
+    peaks = load_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    tensor_path = "tc" in stage
+    clocks = clk.summary()
+    if tensor_path:
+        peak = tf32_peak(peaks, sustained=False)
+        roof = {"bound": "tensor", "unit": UNIT, "peak_source":
+                f"{peaks['source']} bf16 burst x nominal tf32/bf16 ratio {TF32_PER_BF16:.4f}"}
+    else:
+        peak = fp32_simt_peak_tflops(props.multi_processor_count, peaks.get("sm_max_mhz", 2070.0))
+        roof = {"bound": "alu", "unit": UNIT, "peak_source":
+                f"{props.multi_processor_count} SMs x 128 fp32 FMA/clk x 2 x max SM clock"}
+    achieved = flops / (stage_ms / 1e3) / 1e12
+    roof.update({"kernel": stage, "achieved": achieved, "peak": peak, "frac": achieved / peak,
+                 "traffic": _traffic(stage, w.name), "stage_ms": stage_ms,
+                 "flops_per_launch": flops})
+    tf32 = tf32_peak(peaks, sustained=False)
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_max / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "tf32" if tensor_path else "f32",
+        "data": "synthetic (seeded N(0,sigma^2) Q,K,V,dO; LSE from this library's forward)",
+        "pct_of_tf32_peak": 100.0 * value / tf32,
+        "config": {"workload": w.name, "shape": w.describe, "seq_len": S, "n_heads": H,
+                   "n_kv_heads": Hk, "head_dim": d, "n_pairs": pairs,
+                   "counted_flop_per_step": flops,
+                   "step": "zero grads + attn_bwd" + (" + rope_bwd(dQ) + rope_bwd(dK)" if w.rope else ""),
+                   "l2": "inputs larger than L2 (129 MB)" if 4 * S * H * d > 129e6 else
+                         "inputs smaller than L2: steps run back to back (warm L2)",
+                   "path": stage},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "roofline": roof,
+        "clocks": clocks,
+    }
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+# ---------------------------------------------------------------------------
+# the fp64 oracle on the host cores: CPU baseline and the reference arm
+# ---------------------------------------------------------------------------
+def oracle_sample(w, x, lse32, n_rows: int) -> tuple[float, float, str, int]:
+    """Time the oracle's backward over the last ``n_rows`` query rows of every
+    head (each row against all of its visible keys). Returns (seconds,
+    counted flops of the sample, description, threads)."""
+    import oracle
+    S = w.seq_len
+    rows = np.arange(max(0, S - n_rows), S)
+    seg = x["seg"]
+    pairs = int(np.sum(rows - seg[rows].astype(np.int64) + 1))
+    t0 = time.perf_counter()
+    oracle.bwd(x["Q"], x["K"], x["V"], x["dO"], lse32, seg, w.n_heads, w.n_kv_heads,
+               w.head_dim, w.scale, rows=rows)
+    dt = time.perf_counter() - t0
+    desc = (f"oracle.bwd (fp64, numpy) on query rows [{rows[0]}, {S}) of all {w.n_heads} heads "
+            f"({pairs} unmasked pairs per head) of workload {w.name}")
+    return dt, counted_flops(w.head_dim, w.n_heads, pairs), desc, oracle._workers()
+
+
+def sample_lse(w, x, n_rows: int) -> np.ndarray:
+    """LSE for the sampled rows from the oracle forward (other rows unused)."""
+    import oracle
+    rows = np.arange(max(0, w.seq_len - n_rows), w.seq_len)
+    _, lse = oracle.fwd(x["Q"], x["K"], x["V"], x["seg"], w.n_heads, w.n_kv_heads, w.head_dim,
+                        w.scale, rows=rows)
+    return lse.astype(np.float32)
+
+
+CPU_SAMPLE_ROWS = {"tiny": 64, "causal512": 512, "docs2k": 2048, "docs4k": 1024, "causal16k": 512}
+REF_SAMPLE_ROWS = {"tiny": 64, "causal512": 512, "docs2k": 1024, "docs4k": 512, "causal16k": 256}
+
+
+def cpu_baseline(w) -> dict:
+    x = workloads.make_inputs(w)
+    n = CPU_SAMPLE_ROWS.get(w.name, 256)
+    lse32 = sample_lse(w, x, n)
+    dt, fl, desc, cores = oracle_sample(w, x, lse32, n)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": desc, "seconds": dt}
+
+
+def run_reference(args) -> dict | None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.make_inputs(w)
+    n = REF_SAMPLE_ROWS.get(w.name, 256)
+    lse32 = sample_lse(w, x, n)
+    for _ in range(args.warmup):
+        oracle_sample(w, x, lse32, n)
+    times, fl, desc, cores = [], 0.0, "", 1
+    for _ in range(args.steps):
+        dt, fl, desc, cores = oracle_sample(w, x, lse32, n)
+        times.append(dt)
+    mean = sum(times) / len(times)
+    value = fl / mean / 1e12
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * mean,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "shape": w.describe, "sample_rows": n},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default="causal16k")
+    ap.add_argument("--path", choices=["auto", "simt"], default="auto",
+                    help="auto: attn_bwd (tensor cores where built); simt: attn_bwd_simt")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        res = run_reference(args)
+    else:
+        res = run_gpu(args)
+        rank, world, _ = dist_env()
+        if res is not None and world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(workloads.WORKLOADS[args.workload])
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

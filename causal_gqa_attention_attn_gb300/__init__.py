@@ -1,0 +1,191 @@
+"""Causal grouped-query attention backward from a saved log-sum-exp on GB300.
+
+Thin ctypes binding over ``libgqa_attn.so`` (C ABI in ``include/gqa_attn.h``).
+The functions here only check tensor metadata and pass device pointers and the
+current CUDA stream through; every step of the computation runs in the
+library's CUDA kernels. PyTorch provides device memory and streams.
+
+If the shared library has not been built, importing works but the first call
+raises :class:`GqaError`; build it with ``__graft_entry__.build()`` (or
+``python -m causal_gqa_attention_attn_gb300.build``). There is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = ["GqaError", "lib", "lib_path", "attn_fwd_lse", "attn_bwd", "attn_bwd_simt",
+           "rope_bwd_inplace", "workspace_bytes", "read_device_status", "n_pairs_from_seg",
+           "profile_events", "profile_stage_name", "launch_count"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libgqa_attn.so")
+_lib = None
+
+GQA_OK = 0
+_STATUS = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_UNSUPPORTED", 3: "GQA_ERR_CUDA",
+           4: "GQA_ERR_DEVICE_TIMEOUT"}
+
+
+class GqaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (declares the argument types of every entry point)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise GqaError(3, f"{_LIB_PATH} is missing: build it first (__graft_entry__.build())")
+    L = ctypes.CDLL(_LIB_PATH)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.attn_fwd_lse.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P]
+    bwd_args = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
+    L.attn_bwd.argtypes = bwd_args
+    L.attn_bwd_simt.argtypes = bwd_args
+    L.rope_bwd_inplace.argtypes = [P, I, I, I, I, F, P]
+    L.attn_bwd_workspace_bytes.argtypes = [I, I, I, I]
+    L.attn_bwd_workspace_bytes.restype = Z
+    L.attn_read_device_status.argtypes = [P, P]
+    L.gqa_status_str.argtypes = [I]
+    L.gqa_status_str.restype = ctypes.c_char_p
+    L.gqa_profile_events.argtypes = [P, P]
+    L.gqa_profile_events.restype = None
+    L.gqa_profile_stage_name.argtypes = []
+    L.gqa_profile_stage_name.restype = ctypes.c_char_p
+    L.gqa_launch_count.argtypes = []
+    L.gqa_launch_count.restype = ctypes.c_ulonglong
+    L.gqa_last_error.argtypes = []
+    L.gqa_last_error.restype = ctypes.c_char_p
+    for name in ("attn_fwd_lse", "attn_bwd", "attn_bwd_simt", "rope_bwd_inplace",
+                 "attn_read_device_status"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(status: int):
+    if status != GQA_OK:
+        raise GqaError(status, lib().gqa_last_error().decode())
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t, name, dtypes):
+    if t is None:
+        return None
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _f32(t, name):
+    return _ptr(t, name, (_torch().float32,))
+
+
+def _seg(t):
+    torch = _torch()
+    return _ptr(t, "seg", tuple(x for x in (torch.int32, getattr(torch, "uint32", None)) if x))
+
+
+def workspace_bytes(seq_len, n_heads, n_kv_heads, head_dim) -> int:
+    return int(lib().attn_bwd_workspace_bytes(seq_len, n_heads, n_kv_heads, head_dim))
+
+
+def attn_fwd_lse(Q, K, V, seg, n_heads, n_kv_heads, head_dim, scale, O=None, LSE=None,
+                 stream=None):
+    """Forward attention: returns (O, LSE); O [S, H*d], LSE [S, H] fp32."""
+    torch = _torch()
+    S = Q.shape[0]
+    O = torch.empty((S, n_heads * head_dim), device=Q.device, dtype=torch.float32) if O is None else O
+    LSE = torch.empty((S, n_heads), device=Q.device, dtype=torch.float32) if LSE is None else LSE
+    _check(lib().attn_fwd_lse(_f32(Q, "Q"), _f32(K, "K"), _f32(V, "V"), _seg(seg), _f32(O, "O"),
+                              _f32(LSE, "LSE"), S, n_heads, n_kv_heads, head_dim, float(scale),
+                              _stream(stream)))
+    return O, LSE
+
+
+def _bwd(fn, Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_dim, scale,
+         workspace, stream):
+    torch = _torch()
+    S = Q.shape[0]
+    need = workspace_bytes(S, n_heads, n_kv_heads, head_dim)
+    if workspace is None:
+        workspace = torch.empty(need, device=Q.device, dtype=torch.uint8)
+    _check(fn(_f32(Q, "Q"), _f32(K, "K"), _f32(V, "V"), _f32(dO, "dO"), _f32(LSE, "LSE"),
+              _seg(seg), _f32(dQ, "dQ"), _f32(dK, "dK"), _f32(dV, "dV"), S, n_heads, n_kv_heads,
+              head_dim, float(scale), _ptr(workspace, "workspace", (torch.uint8,)),
+              workspace.numel(), _stream(stream)))
+    return workspace
+
+
+def attn_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_dim, scale,
+             workspace=None, stream=None):
+    """Backward from a saved LSE; accumulates into dQ, dK, dV (+=). Returns the
+    workspace used (a uint8 device tensor; pass it back in to reuse it)."""
+    return _bwd(lib().attn_bwd, Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads,
+                head_dim, scale, workspace, stream)
+
+
+def attn_bwd_simt(Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_dim, scale,
+                  workspace=None, stream=None):
+    """Same as :func:`attn_bwd`, on CUDA cores only (exact fp32 products)."""
+    return _bwd(lib().attn_bwd_simt, Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads,
+                head_dim, scale, workspace, stream)
+
+
+def rope_bwd_inplace(dX, n_heads, head_dim, pos_offset=0, base=10000.0, stream=None):
+    """Interleaved RoPE backward in place on dX [S, n_heads*head_dim]."""
+    _check(lib().rope_bwd_inplace(_f32(dX, "dX"), dX.shape[0], n_heads, head_dim, pos_offset,
+                                  float(base), _stream(stream)))
+    return dX
+
+
+def profile_events(before, after):
+    """Arm the one-shot measurement hook with two torch.cuda.Event objects: the
+    next backward call records them around its dominant kernel stage."""
+    lib().gqa_profile_events(before.cuda_event, after.cuda_event)
+
+
+def profile_stage_name() -> str:
+    return lib().gqa_profile_stage_name().decode()
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib().gqa_launch_count())
+
+
+def read_device_status(workspace, stream=None):
+    """Synchronise and raise if a bounded device wait gave up during the last call."""
+    _check(lib().attn_read_device_status(workspace.data_ptr(), _stream(stream)))
+
+
+def n_pairs_from_seg(seg_host) -> int:
+    """Unmasked (query, key) pairs: sum over i of i - seg[i] + 1 (host-side count)."""
+    import numpy as np
+    s = np.arange(len(seg_host), dtype=np.int64)
+    return int(np.sum(s - np.asarray(seg_host, dtype=np.int64) + 1))

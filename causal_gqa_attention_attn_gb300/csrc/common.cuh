@@ -1,0 +1,92 @@
+// Internal definitions shared by the translation units of libgqa_attn.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/gqa_attn.h"
+
+namespace gqa {
+
+// ---------------------------------------------------------------------------
+// Workspace layout (caller-allocated, 256-byte aligned pieces)
+//   [0, 256)                       header: status word (uint32) at byte 0
+//   [kWsD, kWsD + S*H*4)           D[i, h] = sum_j P_ij dP_ij   (fp32, [S, H])
+//   [kWsD + align256(S*H*4), ...)  per query tile: smallest seg in the tile
+//                                  (uint32, one per 64-row tile and one per
+//                                  128-row tile)
+// ---------------------------------------------------------------------------
+constexpr size_t kWsHeader = 256;
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t d_off;       // D
+  size_t minseg64;    // min seg per 64-row query tile
+  size_t minseg128;   // min seg per 128-row query tile
+  size_t total;
+};
+
+inline WsLayout ws_layout(int S, int H) {
+  WsLayout w;
+  w.d_off = kWsHeader;
+  size_t off = w.d_off + align256(size_t(S) * size_t(H) * sizeof(float));
+  w.minseg64 = off;
+  off += align256(size_t((S + 63) / 64) * sizeof(uint32_t));
+  w.minseg128 = off;
+  off += align256(size_t((S + 127) / 128) * sizeof(uint32_t));
+  w.total = off;
+  return w;
+}
+
+// Problem description passed by value to kernels.
+struct Shape {
+  int S, H, Hk, d, G;   // seq_len, n_heads, n_kv_heads, head_dim, H / Hk
+  float scale;
+};
+
+// Measurement hook (gqa_profile_events): one-shot events around the dominant
+// stage of the next backward call on this host thread.
+struct ProfileHook {
+  cudaEvent_t before = nullptr, after = nullptr;
+  const char* stage = "";
+};
+ProfileHook& profile_hook();
+inline void profile_before(cudaStream_t st, const char* stage) {
+  ProfileHook& h = profile_hook();
+  h.stage = stage;
+  if (h.before) cudaEventRecord(h.before, st);
+}
+inline void profile_after(cudaStream_t st) {
+  ProfileHook& h = profile_hook();
+  if (h.after) cudaEventRecord(h.after, st);
+  h.before = h.after = nullptr;
+}
+
+// Count of kernels this library has launched (gqa_launch_count).
+void note_launch(int n = 1);
+
+// Host-side error reporting (thread-local one-line reason).
+gqa_status set_error(gqa_status st, const char* fmt, ...);
+gqa_status check_launch(const char* what);
+
+// Argument checks shared by the attention entry points; returns GQA_OK or an
+// error with gqa_last_error() set.
+gqa_status check_attn_args(int S, int H, int Hk, int d, float scale, int max_d);
+bool aligned16(const void* p);
+
+// SIMT (CUDA-core) kernels, simt_attn.cu
+gqa_status simt_fwd_lse(const float* Q, const float* K, const float* V, const uint32_t* seg,
+                        float* O, float* LSE, const Shape& sh, cudaStream_t st);
+gqa_status simt_bwd(const float* Q, const float* K, const float* V, const float* dO,
+                    const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
+                    const Shape& sh, char* ws, cudaStream_t st);
+
+// RoPE backward, rope_bwd.cu
+gqa_status rope_bwd_launch(float* X, int S, int H, int d, int pos_offset, float base,
+                           cudaStream_t st);
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+}  // namespace gqa

@@ -1,0 +1,148 @@
+/*
+ * gqa_attn.h — C ABI of libgqa_attn.so: causal grouped-query attention on one
+ * GB300 (sm_103a). Forward producing O and the log-sum-exp, the backward pass
+ * from a saved log-sum-exp, and the interleaved RoPE backward.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *    never allocates, frees or keeps them, and never synchronises the stream
+ *    (attn_read_device_status is the one exception, and says so).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Every launch is asynchronous on it.
+ *  - Layouts are row-major fp32 (backward_attention.wgsl, bindings of kernel
+ *    attention_backward): Q, dO, dQ, O are [seq_len, n_heads * head_dim], head
+ *    h in columns [h*head_dim, (h+1)*head_dim); K, V, dK, dV are
+ *    [seq_len, n_kv_heads * head_dim]; LSE is [seq_len, n_heads]; seg is
+ *    [seq_len] uint32.
+ *  - GQA grouping is blocked: query head h reads kv head h / (n_heads /
+ *    n_kv_heads) (backward_attention.wgsl, attention_backward: kv_h =
+ *    h / q_per_group; tang llm.rs, causal_attention_fused).
+ *  - Masking: key j is visible to query i iff seg[i] <= j <= i, where seg[i]
+ *    is the first position of the document holding i (backward_attention.wgsl,
+ *    attention_backward: doc_start / causal_len). seg[i] <= i is a
+ *    precondition; seg need not be monotone. seg all zero = pure causal.
+ *  - Arguments are checked on the host before any launch. A bad argument
+ *    returns GQA_ERR_INVALID_ARG (or GQA_ERR_UNSUPPORTED for a valid shape the
+ *    library has no kernel for) and launches nothing; gqa_last_error() then
+ *    holds a one-line reason. seq_len == 0 is a no-op that returns GQA_OK.
+ *  - Pointers must be 16-byte aligned and n_heads*head_dim, n_kv_heads*head_dim
+ *    multiples of 4 (row starts on 16-byte boundaries, as TMA requires).
+ *  - Sizes: seq_len * max(n_heads, n_kv_heads) * head_dim must stay below 2^31.
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GQA_OK = 0,
+  GQA_ERR_INVALID_ARG = 1,    /* bad pointer, size, alignment or workspace        */
+  GQA_ERR_UNSUPPORTED = 2,    /* valid shape with no kernel (e.g. head_dim > 128) */
+  GQA_ERR_CUDA = 3,           /* a CUDA launch or copy failed                     */
+  GQA_ERR_DEVICE_TIMEOUT = 4  /* a bounded device-side wait gave up (see below)   */
+} gqa_status;
+
+/*
+ * attn_fwd_lse — forward attention with the log-sum-exp.
+ * tang llm.rs, causal_attention_fused (row max, sum of exponentials, weighted
+ * V) with the document mask of backward_attention.wgsl; the LSE is the one the
+ * backward consumes (backward_attention.wgsl header: P = exp(scale*Q.K - LSE)).
+ *   O[i, h]   = sum_j exp(scale*q_i.k_j - LSE[i,h]) v_j   over visible j
+ *   LSE[i, h] = ln sum_j exp(scale*q_i.k_j)               (natural log, scale in)
+ * In:  Q, K, V, seg. Out (overwritten): O, LSE. head_dim: 4..128, multiple of 4.
+ */
+gqa_status attn_fwd_lse(const float* Q, const float* K, const float* V, const uint32_t* seg,
+                        float* O, float* LSE, int seq_len, int n_heads, int n_kv_heads,
+                        int head_dim, float scale, void* stream);
+
+/*
+ * attn_bwd_workspace_bytes — bytes of device workspace attn_bwd needs for this
+ * shape (a multiple of 256). The caller allocates it (any contents) and may
+ * reuse it across calls that do not overlap on the GPU.
+ */
+size_t attn_bwd_workspace_bytes(int seq_len, int n_heads, int n_kv_heads, int head_dim);
+
+/*
+ * attn_bwd — backward pass of causal GQA attention from a saved LSE.
+ * backward_attention.wgsl, header and kernel attention_backward (P recomputed
+ * from the saved LSE, dP = dO.V, D = sum_j P*dP, dS = scale*P*(dP - D)); the
+ * explicit-matrix form is tang llm.rs, GpuCausalAttention::backward.
+ *   dQ[i,h] += sum_j dS_ij k_j,  dK[j,g] += sum_{h in g, i} dS_ij q_i,
+ *   dV[j,g] += sum_{h in g, i} P_ij dO_i
+ * In:  Q, K, V, dO, LSE, seg, scale. In/out: dQ, dK, dV are ACCUMULATED (+=),
+ * as in the streaming kernel: zero them before the first call of a step.
+ * workspace: >= attn_bwd_workspace_bytes(...) device bytes, caller-owned.
+ * head_dim 32, 64 or 128 runs the tensor-core path where it is built; other
+ * multiples of 4 up to 128 run the CUDA-core path (attn_bwd_simt).
+ * The result is not bitwise deterministic (dQ partial sums may be reduced in
+ * any order); it stays within fp32/TF32 rounding of the exact value.
+ */
+gqa_status attn_bwd(const float* Q, const float* K, const float* V, const float* dO,
+                    const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
+                    int seq_len, int n_heads, int n_kv_heads, int head_dim, float scale,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_bwd_simt — the same operation and contract as attn_bwd, computed with
+ * fp32 FFMA on CUDA cores only (no tensor cores): exact fp32 products, any
+ * head_dim that is a multiple of 4 up to 128. Deterministic.
+ */
+gqa_status attn_bwd_simt(const float* Q, const float* K, const float* V, const float* dO,
+                         const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
+                         int seq_len, int n_heads, int n_kv_heads, int head_dim, float scale,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * rope_bwd_inplace — interleaved RoPE backward, in place on dX
+ * [seq_len, n_heads * head_dim] (backward_attention.wgsl, rope_q_backward /
+ * rope_k_backward; tang llm.rs, interleaved_rope_backward). For pair p <
+ * head_dim/2 of every head at row s, with t = pos_offset + s and
+ * theta = t * base^(-2p/head_dim):
+ *   (x0, x1) <- (x0*cos theta + x1*sin theta, -x0*sin theta + x1*cos theta)
+ * on columns (2p, 2p+1). The angle is reduced in fp64 on the device, so large
+ * positions keep full fp32 accuracy. head_dim a multiple of 4 (at most 128),
+ * base > 0, pos_offset >= 0.
+ */
+gqa_status rope_bwd_inplace(float* dX, int seq_len, int n_heads, int head_dim,
+                            int pos_offset, float base, void* stream);
+
+/*
+ * attn_read_device_status — test/debug helper: SYNCHRONISES `stream`, then
+ * reads the device-side status word that the last attn_bwd on this workspace
+ * left (GQA_OK, or GQA_ERR_DEVICE_TIMEOUT if a bounded wait inside a kernel
+ * gave up and the kernel returned early instead of hanging).
+ */
+gqa_status attn_read_device_status(const void* workspace, void* stream);
+
+/*
+ * gqa_profile_events — measurement hook (no counterpart on the pages). When
+ * both are non-NULL cudaEvent_t handles, the next attn_bwd / attn_bwd_simt
+ * call on this host thread records `before` on its stream immediately before
+ * its dominant kernel stage and `after` immediately after it, then clears the
+ * hook. The events are owned by the caller. Stage: the whole two-kernel
+ * backward on the CUDA-core path; the main key-tile kernel on the
+ * tensor-core path. gqa_profile_stage_name() names it.
+ */
+void gqa_profile_events(void* before, void* after);
+const char* gqa_profile_stage_name(void);
+
+/* Number of kernels this library has launched in this process (all threads). */
+unsigned long long gqa_launch_count(void);
+
+/* Static string naming a status code. */
+const char* gqa_status_str(gqa_status status);
+
+/* One-line reason for the last non-OK status returned on this host thread. */
+const char* gqa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

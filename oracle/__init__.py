@@ -51,7 +51,13 @@ independent float64 autograd of the forward definition.
 """
 from __future__ import annotations
 
-import numpy as np
+import concurrent.futures as _cf
+import os
+import sys
+
+if "numpy" not in sys.modules:      # the pool below supplies the parallelism
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+import numpy as np  # noqa: E402
 
 __all__ = ["fwd", "bwd", "bwd_rows", "bwd_dkdv_keys", "row_terms", "rope_bwd",
            "allowed"]
@@ -82,6 +88,27 @@ def _head_cols(h, d):
     return slice(h * d, (h + 1) * d)
 
 
+def _workers() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def _for_each(fn, items):
+    """Run fn(item) for independent items (distinct output columns) on a thread
+    pool; numpy releases the GIL inside its kernels. Each item is computed by
+    one thread in a fixed order, so results do not depend on scheduling."""
+    items = list(items)
+    if len(items) <= 1 or _workers() == 1:
+        for it in items:
+            fn(it)
+        return
+    with _cf.ThreadPoolExecutor(max_workers=min(len(items), _workers())) as ex:
+        for f in [ex.submit(fn, it) for it in items]:
+            f.result()
+
+
 def _blocks(rows: np.ndarray):
     for b in range(0, len(rows), _ROW_BLOCK):
         yield rows[b:b + _ROW_BLOCK]
@@ -102,10 +129,12 @@ def fwd(Q, K, V, seg, n_heads, n_kv_heads, head_dim, scale, rows=None):
     O = np.zeros((S, H * d))
     LSE = np.zeros((S, H))
     all_rows = np.arange(S, dtype=np.int64) if rows is None else np.sort(np.asarray(rows, np.int64))
-    for h in range(H):
+
+    def one_item(item):
+        h, r = item
         g = h // G
         Kg, Vg = K[:, _head_cols(g, d)], V[:, _head_cols(g, d)]
-        for r in _blocks(all_rows):
+        if True:
             n_keys = int(r[-1]) + 1
             s = scale * (Q[r, _head_cols(h, d)] @ Kg[:n_keys].T)
             s = np.where(allowed(seg, r, n_keys), s, -np.inf)
@@ -114,6 +143,8 @@ def fwd(Q, K, V, seg, n_heads, n_kv_heads, head_dim, scale, rows=None):
             p = np.exp(s - lse[:, None])
             O[r, _head_cols(h, d)] = p @ Vg[:n_keys]
             LSE[r, h] = lse
+
+    _for_each(one_item, [(h, r) for h in range(H) for r in _blocks(all_rows)])
     return O, LSE
 
 
@@ -139,9 +170,11 @@ def row_terms(Q, K, V, dO, LSE, seg, h, n_heads, n_kv_heads, head_dim, scale, ro
 
 
 def bwd(Q, K, V, dO, LSE, seg, n_heads, n_kv_heads, head_dim, scale,
-        dQ=None, dK=None, dV=None):
+        dQ=None, dK=None, dV=None, rows=None):
     """Backward from the given LSE; accumulates into dQ, dK, dV (fp64, created
-    as zeros when not given) and returns them.
+    as zeros when not given) and returns them. ``rows`` (sorted query
+    positions) restricts the sum to those query rows: the contributions of
+    every other row are left out (used to time bounded samples).
 
     Follows the explicit-matrix backward of tang ``llm.rs``
     (``GpuCausalAttention::backward``: recompute P, dP = dO V^T, dV += P^T dO,
@@ -156,16 +189,26 @@ def bwd(Q, K, V, dO, LSE, seg, n_heads, n_kv_heads, head_dim, scale,
     dQ = np.zeros((S, H * d)) if dQ is None else dQ
     dK = np.zeros((S, Hk * d)) if dK is None else dK
     dV = np.zeros((S, Hk * d)) if dV is None else dV
-    all_rows = np.arange(S, dtype=np.int64)
-    for h in range(H):
-        g = h // (H // Hk)
+    all_rows = np.arange(S, dtype=np.int64) if rows is None else np.asarray(rows, np.int64)
+    G = H // Hk
+    # per query head: its dK / dV contribution, summed over its kv group below
+    part_k = np.zeros((H, S, d))
+    part_v = np.zeros((H, S, d))
+
+    def one_head(h):
+        g = h // G
         for r in _blocks(all_rows):
             t = row_terms(Q, K, V, dO, LSE, seg, h, H, Hk, d, scale, r)
             n = t["keys"]
-            Kg = K[:n, _head_cols(g, d)]
-            dQ[r, _head_cols(h, d)] += t["dS"] @ Kg
-            dK[:n, _head_cols(g, d)] += t["dS"].T @ Q[r, _head_cols(h, d)]
-            dV[:n, _head_cols(g, d)] += t["P"].T @ dO[r, _head_cols(h, d)]
+            dQ[r, _head_cols(h, d)] += t["dS"] @ K[:n, _head_cols(g, d)]
+            part_k[h, :n] += t["dS"].T @ Q[r, _head_cols(h, d)]
+            part_v[h, :n] += t["P"].T @ dO[r, _head_cols(h, d)]
+
+    _for_each(one_head, range(H))
+    for h in range(H):
+        g = h // G
+        dK[:, _head_cols(g, d)] += part_k[h]
+        dV[:, _head_cols(g, d)] += part_v[h]
     return dQ, dK, dV
 
 
@@ -182,12 +225,15 @@ def bwd_rows(Q, K, V, dO, LSE, seg, n_heads, n_kv_heads, head_dim, scale, rows, 
     r_all = np.asarray(rows, dtype=np.int64)
     out = np.zeros((len(r_all), H * d))
     heads = range(H) if heads is None else heads
-    for h in heads:
+
+    def one_item(item):
+        h, b = item
         g = h // (H // Hk)
-        for b in range(0, len(r_all), _ROW_BLOCK):
-            r = r_all[b:b + _ROW_BLOCK]
-            t = row_terms(Q, K, V, dO, LSE, seg, h, H, Hk, d, scale, r)
-            out[b:b + len(r), _head_cols(h, d)] = t["dS"] @ K[:t["keys"], _head_cols(g, d)]
+        r = r_all[b:b + _ROW_BLOCK]
+        t = row_terms(Q, K, V, dO, LSE, seg, h, H, Hk, d, scale, r)
+        out[b:b + len(r), _head_cols(h, d)] = t["dS"] @ K[:t["keys"], _head_cols(g, d)]
+
+    _for_each(one_item, [(h, b) for h in heads for b in range(0, len(r_all), _ROW_BLOCK)])
     return out
 
 
@@ -210,14 +256,26 @@ def bwd_dkdv_keys(Q, K, V, dO, LSE, seg, n_heads, n_kv_heads, head_dim, scale, k
     rows = np.arange(int(keys.min()), S, dtype=np.int64)
     kv_heads = range(Hk) if kv_heads is None else kv_heads
     G = H // Hk
-    for g in kv_heads:
-        for h in range(g * G, (g + 1) * G):
-            for r in _blocks(rows):
-                t = row_terms(Q, K, V, dO, LSE, seg, h, H, Hk, d, scale, r)
-                sel = keys < t["keys"]
-                kk = keys[sel]
-                dK[sel, _head_cols(g, d)] += t["dS"][:, kk].T @ Q[r, _head_cols(h, d)]
-                dV[sel, _head_cols(g, d)] += t["P"][:, kk].T @ dO[r, _head_cols(h, d)]
+
+    items = [(h, b) for g in kv_heads for h in range(g * G, (g + 1) * G)
+             for b in range(0, len(rows), _ROW_BLOCK)]
+    part_k = {it: np.zeros((len(keys), d)) for it in items}
+    part_v = {it: np.zeros((len(keys), d)) for it in items}
+
+    def one_item(item):
+        h, b = item
+        r = rows[b:b + _ROW_BLOCK]
+        t = row_terms(Q, K, V, dO, LSE, seg, h, H, Hk, d, scale, r)
+        sel = keys < t["keys"]
+        kk = keys[sel]
+        part_k[item][sel] = t["dS"][:, kk].T @ Q[r, _head_cols(h, d)]
+        part_v[item][sel] = t["P"][:, kk].T @ dO[r, _head_cols(h, d)]
+
+    _for_each(one_item, items)
+    for it in items:                      # fixed summation order
+        g = it[0] // G
+        dK[:, _head_cols(g, d)] += part_k[it]
+        dV[:, _head_cols(g, d)] += part_v[it]
     return dK, dV
 
 

@@ -1,7 +1,11 @@
 import os
 import sys
 
-import pytest
+# The oracle parallelises over independent heads / row blocks itself; one BLAS
+# thread per worker avoids oversubscription. Must precede the first numpy import.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+
+import pytest  # noqa: E402
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:

@@ -1,0 +1,90 @@
+"""Full-size parity on the 16k-token workload (S=16384, H=32, Hk=8, d=128,
+N(0, 0.5^2), pure causal) in the launch configuration the benchmark times:
+attention backward followed by the RoPE backward on dQ and dK.
+
+The fp64 oracle cannot form the whole backward at this size in a test's time,
+so it forms sampled outputs one by one: dQ rows (every head) spread over the
+sequence including the first and last tiles, and dK / dV at key positions of
+one kv group that include the first key tile (whose owner visits every query
+tile), plus the last keys of every kv group. The LSE both sides consume is the
+oracle forward's, rounded to fp32.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+TOL = 5e-3
+
+
+@pytest.fixture(scope="module")
+def ga():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from causal_gqa_attention_attn_gb300 import build
+    build.build()
+    import causal_gqa_attention_attn_gb300 as mod
+    return mod
+
+
+def _check(name, got, ref):
+    ref = np.asarray(ref, np.float64)
+    got = np.asarray(got, np.float64)
+    assert np.all(np.isfinite(got))
+    err = float(np.max(np.abs(got - ref)))
+    mag = float(np.max(np.abs(ref)))
+    assert err <= TOL * mag, f"{name}: {err:.3e} > {TOL} * {mag:.3e}"
+
+
+def test_causal16k_sampled_with_rope(ga):
+    w = workloads.WORKLOADS["causal16k"]
+    x = workloads.make_inputs(w)
+    S, H, Hk, d, sc = w.seq_len, w.n_heads, w.n_kv_heads, w.head_dim, w.scale
+    _, lse = oracle.fwd(x["Q"], x["K"], x["V"], x["seg"], H, Hk, d, sc)
+    lse32 = lse.astype(np.float32)
+    del lse
+
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    Q, K, V, dO = dev(x["Q"]), dev(x["K"]), dev(x["V"]), dev(x["dO"])
+    seg, LSE = dev(x["seg"].astype(np.int32)), dev(lse32)
+    dQ = torch.zeros(S, H * d, device="cuda")
+    dK = torch.zeros(S, Hk * d, device="cuda")
+    dV = torch.zeros(S, Hk * d, device="cuda")
+    ws = ga.attn_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, H, Hk, d, sc)
+    ga.rope_bwd_inplace(dQ, H, d, 0, 10000.0)
+    ga.rope_bwd_inplace(dK, Hk, d, 0, 10000.0)
+    ga.read_device_status(ws)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(dQ).all()) and bool(torch.isfinite(dK).all())
+    assert bool(torch.isfinite(dV).all())
+
+    rows = np.unique(np.concatenate([[0, 1, 2, 63, 64, 127, 128, 129], np.arange(1000, S, 997),
+                                     [S - 129, S - 128, S - 65, S - 2, S - 1]]))
+    rq = oracle.bwd_rows(x["Q"], x["K"], x["V"], x["dO"], lse32, x["seg"], H, Hk, d, sc, rows)
+    rq = np.concatenate([oracle.rope_bwd(rq[i:i + 1], H, d, pos_offset=int(r))
+                         for i, r in enumerate(rows)])
+    _check("dQ (sampled rows, after RoPE)", dQ[torch.from_numpy(rows).cuda()].cpu().numpy(), rq)
+
+    g0 = 5
+    keys0 = np.array([0, 1, 31, 63, 64, 100, 127, 128, 4095, 8191, 8192, 12345, S - 1])
+    rk, rv = oracle.bwd_dkdv_keys(x["Q"], x["K"], x["V"], x["dO"], lse32, x["seg"], H, Hk, d, sc,
+                                  keys0, kv_heads=[g0])
+    cols = slice(g0 * d, (g0 + 1) * d)
+    rk = np.concatenate([oracle.rope_bwd(rk[i:i + 1], Hk, d, pos_offset=int(k))
+                         for i, k in enumerate(keys0)])
+    kidx = torch.from_numpy(keys0).cuda()
+    _check("dK (one group, after RoPE)", dK[kidx].cpu().numpy()[:, cols], rk[:, cols])
+    _check("dV (one group)", dV[kidx].cpu().numpy()[:, cols], rv[:, cols])
+
+    keys1 = np.arange(S - 200, S, 9)
+    rk, rv = oracle.bwd_dkdv_keys(x["Q"], x["K"], x["V"], x["dO"], lse32, x["seg"], H, Hk, d, sc,
+                                  keys1)
+    rk = np.concatenate([oracle.rope_bwd(rk[i:i + 1], Hk, d, pos_offset=int(k))
+                         for i, k in enumerate(keys1)])
+    kidx = torch.from_numpy(keys1).cuda()
+    _check("dK (last keys, all groups, after RoPE)", dK[kidx].cpu().numpy(), rk)
+    _check("dV (last keys, all groups)", dV[kidx].cpu().numpy(), rv)

@@ -1,0 +1,176 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the
+same seeded inputs.
+
+Acceptance (per output tensor): max|gpu - oracle| <= 5e-3 * max|oracle|.
+Where the exact reference of a tensor is zero (seq_len 1: dQ = dK = 0), the
+bound uses the magnitude of dV instead, since the GPU only reaches zero up to
+fp32 rounding of P = exp(s - LSE) ~ 1.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL = 5e-3
+
+
+@pytest.fixture(scope="module")
+def ga():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from causal_gqa_attention_attn_gb300 import build
+    build.build()
+    import causal_gqa_attention_attn_gb300 as mod
+    return mod
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _seg_dev(seg):
+    return _dev(np.asarray(seg, dtype=np.int32))
+
+
+def assert_parity(name, got, ref, scale_ref=None):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    mag = float(np.max(np.abs(ref))) if ref.size else 0.0
+    if scale_ref is not None:
+        mag = max(mag, float(np.max(np.abs(scale_ref))))
+    err = float(np.max(np.abs(got - ref))) if ref.size else 0.0
+    assert err <= TOL * mag, f"{name}: max|gpu-oracle| = {err:.3e} > {TOL} * {mag:.3e}"
+    return err / mag if mag else 0.0
+
+
+def gpu_bwd(ga, fn, x, lse32, init=None, calls=1):
+    S, H, Hk, d = x["seq_len"], x["n_heads"], x["n_kv_heads"], x["head_dim"]
+    t = {k: _dev(x[k]) for k in ("Q", "K", "V", "dO")}
+    if init is None:
+        dQ = torch.zeros(S, H * d, device="cuda")
+        dK = torch.zeros(S, Hk * d, device="cuda")
+        dV = torch.zeros(S, Hk * d, device="cuda")
+    else:
+        dQ, dK, dV = (_dev(a.astype(np.float32)) for a in init)
+    seg, LSE = _seg_dev(x["seg"]), _dev(lse32)
+    ws = None
+    for _ in range(calls):
+        ws = getattr(ga, fn)(t["Q"], t["K"], t["V"], t["dO"], LSE, seg, dQ, dK, dV, H, Hk, d,
+                             x["scale"], workspace=ws)
+    ga.read_device_status(ws)
+    torch.cuda.synchronize()
+    return dQ.cpu().numpy(), dK.cpu().numpy(), dV.cpu().numpy()
+
+
+_REF = {}
+
+
+def reference(name):
+    """Inputs, fp32 LSE from the oracle forward, and the oracle backward."""
+    if name not in _REF:
+        w = workloads.WORKLOADS[name]
+        x = workloads.make_inputs(w)
+        O, lse = oracle.fwd(x["Q"], x["K"], x["V"], x["seg"], w.n_heads, w.n_kv_heads,
+                            w.head_dim, w.scale)
+        lse32 = lse.astype(np.float32)
+        g = oracle.bwd(x["Q"], x["K"], x["V"], x["dO"], lse32, x["seg"], w.n_heads,
+                       w.n_kv_heads, w.head_dim, w.scale)
+        _REF[name] = (x, O, lse, lse32, g)
+    return _REF[name]
+
+
+@pytest.mark.parametrize("fn", ["attn_bwd", "attn_bwd_simt"])
+@pytest.mark.parametrize("name", ["tiny", "causal512", "docs2k", "docs4k"])
+def test_backward_matches_oracle(ga, name, fn):
+    x, _, _, lse32, (rq, rk, rv) = reference(name)
+    dQ, dK, dV = gpu_bwd(ga, fn, x, lse32)
+    assert_parity("dQ", dQ, rq)
+    assert_parity("dK", dK, rk)
+    assert_parity("dV", dV, rv)
+
+
+@pytest.mark.parametrize("name", ["tiny", "causal512", "docs2k", "docs4k"])
+def test_forward_matches_oracle(ga, name):
+    x, O_ref, lse_ref, _, _ = reference(name)
+    H, Hk, d = x["n_heads"], x["n_kv_heads"], x["head_dim"]
+    O, LSE = ga.attn_fwd_lse(_dev(x["Q"]), _dev(x["K"]), _dev(x["V"]), _seg_dev(x["seg"]),
+                             H, Hk, d, x["scale"])
+    torch.cuda.synchronize()
+    assert_parity("O", O.cpu().numpy(), O_ref)
+    assert_parity("LSE", LSE.cpu().numpy(), lse_ref)
+
+
+def _edge_inputs(S, H, Hk, d, seg_kind, seed):
+    rng = np.random.default_rng(seed)
+    if seg_kind == "causal":
+        seg = np.zeros(S, np.uint32)
+    else:
+        seg = workloads.random_seg(S, rng, monotone=(seg_kind == "docs"))
+    f = lambda c: rng.standard_normal((S, c), dtype=np.float32)  # noqa: E731
+    return {"Q": f(H * d), "K": f(Hk * d), "V": f(Hk * d), "dO": f(H * d), "seg": seg,
+            "scale": 1.0 / math.sqrt(d), "seq_len": S, "n_heads": H, "n_kv_heads": Hk,
+            "head_dim": d}
+
+
+EDGE = [
+    (1, 4, 2, 32, "causal"), (2, 4, 4, 64, "causal"), (65, 8, 2, 128, "docs"),
+    (127, 4, 1, 32, "nonmonotone"), (129, 6, 3, 64, "docs"), (200, 8, 8, 128, "causal"),
+    (333, 16, 2, 64, "nonmonotone"), (97, 4, 2, 100, "docs"), (64, 2, 1, 16, "causal"),
+    (300, 8, 1, 128, "docs"), (513, 4, 2, 32, "docs"), (256, 16, 2, 128, "causal"),
+]
+
+
+@pytest.mark.parametrize("fn", ["attn_bwd", "attn_bwd_simt"])
+@pytest.mark.parametrize("S,H,Hk,d,seg_kind", EDGE)
+def test_edge_shapes(ga, S, H, Hk, d, seg_kind, fn):
+    x = _edge_inputs(S, H, Hk, d, seg_kind, seed=S * 31 + d)
+    _, lse = oracle.fwd(x["Q"], x["K"], x["V"], x["seg"], H, Hk, d, x["scale"])
+    lse32 = lse.astype(np.float32)
+    rq, rk, rv = oracle.bwd(x["Q"], x["K"], x["V"], x["dO"], lse32, x["seg"], H, Hk, d, x["scale"])
+    dQ, dK, dV = gpu_bwd(ga, fn, x, lse32)
+    assert_parity("dQ", dQ, rq, scale_ref=rv)
+    assert_parity("dK", dK, rk, scale_ref=rv)
+    assert_parity("dV", dV, rv)
+
+
+@pytest.mark.parametrize("fn", ["attn_bwd", "attn_bwd_simt"])
+def test_gradients_accumulate(ga, fn):
+    """+= semantics: two calls on non-zero initial gradients give init + 2 * grad."""
+    x, _, _, lse32, (rq, rk, rv) = reference("causal512")
+    rng = np.random.default_rng(5)
+    init = [rng.standard_normal(a.shape) for a in (rq, rk, rv)]
+    dQ, dK, dV = gpu_bwd(ga, fn, x, lse32, init=init, calls=2)
+    assert_parity("dQ", dQ, init[0].astype(np.float32) + 2 * rq)
+    assert_parity("dK", dK, init[1].astype(np.float32) + 2 * rk)
+    assert_parity("dV", dV, init[2].astype(np.float32) + 2 * rv)
+
+
+def test_seq_len_one(ga):
+    x = _edge_inputs(1, 8, 2, 64, "causal", seed=1)
+    _, lse = oracle.fwd(x["Q"], x["K"], x["V"], x["seg"], 8, 2, 64, x["scale"])
+    dQ, dK, dV = gpu_bwd(ga, "attn_bwd", x, lse.astype(np.float32))
+    want_v = np.stack([x["dO"][0].reshape(8, 64)[4 * g:4 * g + 4].sum(0) for g in range(2)]).reshape(1, -1)
+    assert_parity("dV", dV, want_v)
+    assert_parity("dQ", dQ, np.zeros_like(dQ), scale_ref=want_v)
+    assert_parity("dK", dK, np.zeros_like(dK), scale_ref=want_v)
+
+
+@pytest.mark.parametrize("pos_offset", [0, 100000])
+def test_rope_backward_matches_oracle(ga, pos_offset):
+    rng = np.random.default_rng(pos_offset + 3)
+    S, H, d = 300, 5, 64
+    X = rng.standard_normal((S, H * d), dtype=np.float32)
+    t = _dev(X)
+    ga.rope_bwd_inplace(t, H, d, pos_offset=pos_offset, base=10000.0)
+    torch.cuda.synchronize()
+    ref = oracle.rope_bwd(X, H, d, pos_offset=pos_offset, base=10000.0)
+    got = t.cpu().numpy()
+    assert np.max(np.abs(got - ref)) <= 2e-6 * np.max(np.abs(ref))

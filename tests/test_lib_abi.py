@@ -1,0 +1,101 @@
+"""The C-ABI library: it loads, exports every function include/*.h declares, and
+rejects bad arguments on the host before touching the GPU (runs without one)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import causal_gqa_attention_attn_gb300 as ga
+from causal_gqa_attention_attn_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    gbuild.build()
+    return ga.lib()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\(", text, flags=re.M):
+            if m.group(1) not in ("if", "defined"):
+                names.add(m.group(1))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared_functions()
+    assert "attn_bwd" in names and "attn_fwd_lse" in names and "rope_bwd_inplace" in names
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings(L):
+    for code, name in ((0, "GQA_OK"), (1, "GQA_ERR_INVALID_ARG"), (2, "GQA_ERR_UNSUPPORTED"),
+                       (3, "GQA_ERR_CUDA"), (4, "GQA_ERR_DEVICE_TIMEOUT")):
+        assert L.gqa_status_str(code).decode() == name
+
+
+def test_workspace_size(L):
+    a = L.attn_bwd_workspace_bytes(4096, 32, 8, 128)
+    b = L.attn_bwd_workspace_bytes(16384, 32, 8, 128)
+    assert a % 256 == 0 and b % 256 == 0
+    assert b >= 16384 * 32 * 4 > a >= 4096 * 32 * 4
+    assert L.attn_bwd_workspace_bytes(0, 4, 2, 32) >= 0
+
+
+FAKE = 0x10000  # a 16-byte-aligned non-null address; never dereferenced (checks fail first)
+
+
+def _bwd(L, S=128, H=4, Hk=2, d=32, scale=0.17, ws_bytes=None, ptrs=None, fn="attn_bwd"):
+    p = [FAKE] * 10 if ptrs is None else ptrs
+    if ws_bytes is None:
+        ws_bytes = L.attn_bwd_workspace_bytes(S, H, Hk, d)
+    return getattr(L, fn)(*p[:9], S, H, Hk, d, scale, p[9], ws_bytes, None)
+
+
+@pytest.mark.parametrize("fn", ["attn_bwd", "attn_bwd_simt"])
+def test_bwd_rejects_bad_arguments(L, fn):
+    assert _bwd(L, H=6, Hk=4, fn=fn) == 1                       # heads not a multiple
+    assert _bwd(L, Hk=0, fn=fn) == 1
+    assert _bwd(L, S=-1, fn=fn) == 1
+    assert _bwd(L, d=30, fn=fn) == 1                            # not a multiple of 4
+    assert _bwd(L, d=132, fn=fn) == 2                           # no kernel above 128
+    assert _bwd(L, scale=float("nan"), fn=fn) == 1
+    assert _bwd(L, ws_bytes=16, fn=fn) == 1                     # workspace too small
+    assert "workspace" in L.gqa_last_error().decode()
+    for k in range(10):
+        p = [FAKE] * 10
+        p[k] = None
+        assert _bwd(L, ptrs=p, fn=fn) == 1
+        p[k] = FAKE + 4                                         # misaligned
+        assert _bwd(L, ptrs=p, fn=fn) == 1
+    assert _bwd(L, S=1 << 20, H=64, Hk=8, d=128, fn=fn) == 2   # 2^33 elements
+    assert _bwd(L, S=0, fn=fn) == 0                             # empty: no-op
+
+
+def test_fwd_and_rope_reject_bad_arguments(L):
+    fwd = lambda S=64, H=4, Hk=2, d=32, s=0.2: L.attn_fwd_lse(  # noqa: E731
+        FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, S, H, Hk, d, s, None)
+    assert fwd(H=5) == 1 and fwd(d=136) == 2 and fwd(S=-3) == 1 and fwd(S=0) == 0
+    assert L.attn_fwd_lse(FAKE, None, FAKE, FAKE, FAKE, FAKE, 64, 4, 2, 32, 0.2, None) == 1
+    rope = L.rope_bwd_inplace
+    assert rope(FAKE, 16, 4, 6, 0, 10000.0, None) == 1          # head_dim not a multiple of 4
+    assert rope(FAKE, 16, 4, 8, -1, 10000.0, None) == 1
+    assert rope(FAKE, 16, 4, 8, 0, 0.0, None) == 1
+    assert rope(None, 16, 4, 8, 0, 10000.0, None) == 1
+    assert rope(FAKE + 8, 16, 4, 8, 0, 10000.0, None) == 1
+    assert rope(FAKE, 0, 4, 8, 0, 10000.0, None) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(ga, "_lib", None)
+    monkeypatch.setattr(ga, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ga.GqaError):
+        ga.lib()
