@@ -360,8 +360,8 @@ def sample_lse(w, x, n_rows: int) -> np.ndarray:
     return lse.astype(np.float32)
 
 
-CPU_SAMPLE_ROWS = {"tiny": 64, "causal512": 512, "docs2k": 2048, "docs4k": 1024, "causal16k": 512}
-REF_SAMPLE_ROWS = {"tiny": 64, "causal512": 512, "docs2k": 1024, "docs4k": 512, "causal16k": 256}
+CPU_SAMPLE_ROWS = {"tiny": 64, "causal512": 512, "docs2k": 2048, "docs4k": 4096, "causal16k": 4096}
+REF_SAMPLE_ROWS = {"tiny": 64, "causal512": 512, "docs2k": 2048, "docs4k": 2048, "causal16k": 2048}
 
 
 def cpu_baseline(w) -> dict:
