@@ -16,7 +16,7 @@ import os
 
 __all__ = ["GqaError", "lib", "lib_path", "attn_fwd_lse", "attn_bwd", "attn_bwd_simt",
            "rope_bwd_inplace", "workspace_bytes", "read_device_status", "n_pairs_from_seg",
-           "profile_events", "profile_stage_name", "launch_count"]
+           "profile_events", "profile_stage_name", "launch_count", "attn_bwd_noalloc"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libgqa_attn.so")
@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
     bwd_args = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
     L.attn_bwd.argtypes = bwd_args
     L.attn_bwd_simt.argtypes = bwd_args
+    L.attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P]
+    L.attn_bwd_noalloc.restype = ctypes.c_int
     L.rope_bwd_inplace.argtypes = [P, I, I, I, I, F, P]
     L.attn_bwd_workspace_bytes.argtypes = [I, I, I, I]
     L.attn_bwd_workspace_bytes.restype = Z
@@ -155,6 +157,17 @@ def attn_bwd_simt(Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_d
     """Same as :func:`attn_bwd`, on CUDA cores only (exact fp32 products)."""
     return _bwd(lib().attn_bwd_simt, Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads,
                 head_dim, scale, workspace, stream)
+
+
+def attn_bwd_noalloc(Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_dim, scale,
+                     stream=None):
+    """Same as :func:`attn_bwd_simt`, for callers that cannot allocate device
+    memory: no workspace argument; the library's fixed 4 MiB scratch array is
+    used instead (seq_len * n_heads up to about 1M; overlapping calls race)."""
+    _check(lib().attn_bwd_noalloc(_f32(Q, "Q"), _f32(K, "K"), _f32(V, "V"), _f32(dO, "dO"),
+                                  _f32(LSE, "LSE"), _seg(seg), _f32(dQ, "dQ"), _f32(dK, "dK"),
+                                  _f32(dV, "dV"), Q.shape[0], n_heads, n_kv_heads, head_dim,
+                                  float(scale), _stream(stream)))
 
 
 def rope_bwd_inplace(dX, n_heads, head_dim, pos_offset=0, base=10000.0, stream=None):

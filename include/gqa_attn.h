@@ -99,6 +99,29 @@ gqa_status attn_bwd_simt(const float* Q, const float* K, const float* V, const f
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_bwd_noalloc — attn_bwd for callers that cannot allocate device memory
+ * (no counterpart on the pages: an addition of this library). Some callers
+ * are handed only their input and output buffers — a plugin inside a host
+ * engine, code where the process's memory manager forbids raw cudaMalloc after
+ * start-up, a binding with no device allocator — and so cannot provide the
+ * workspace attn_bwd needs. This entry point takes the same arguments minus
+ * the workspace and uses a fixed 4 MiB device array inside the library
+ * instead; it calls no allocator. Limits: seq_len * n_heads must fit that
+ * array (about 1M, e.g. 16384 x 32); larger shapes return
+ * GQA_ERR_UNSUPPORTED before any launch. Every GPU that loads the library
+ * holds the array until exit. All calls share it: calls whose GPU work
+ * overlaps (other streams or host threads) race and give wrong results. The
+ * first call on a device looks up the array's address with that device
+ * current; make that first call before any stream capture. It runs the
+ * CUDA-core kernels (same results as attn_bwd_simt); dQ, dK, dV are
+ * accumulated (+=) as in attn_bwd.
+ */
+gqa_status attn_bwd_noalloc(const float* Q, const float* K, const float* V, const float* dO,
+                            const float* LSE, const uint32_t* seg, float* dQ, float* dK,
+                            float* dV, int seq_len, int n_heads, int n_kv_heads, int head_dim,
+                            float scale, void* stream);
+
+/*
  * rope_bwd_inplace — interleaved RoPE backward, in place on dX
  * [seq_len, n_heads * head_dim] (backward_attention.wgsl, rope_q_backward /
  * rope_k_backward; tang llm.rs, interleaved_rope_backward). For pair p <
