@@ -23,8 +23,11 @@ struct RopeFreqs {
 };
 
 __device__ __forceinline__ void rot(float& x0, float& x1, double theta) {
+  // theta - 2 pi n with n = rint(theta / 2 pi); a multiply by the reciprocal
+  // constant instead of a division (fp64 is a slow pipe on this part).
   const double two_pi = 6.283185307179586476925286766559;
-  const double r = theta - two_pi * rint(theta / two_pi);
+  const double inv_two_pi = 0.15915494309189533576888376337251;
+  const double r = fma(-two_pi, rint(theta * inv_two_pi), theta);
   float s, c;
   sincosf((float)r, &s, &c);
   const float a = x0, b = x1;
