@@ -111,9 +111,9 @@ const char* gqa_profile_stage_name(void) { return g_hook.stage; }
 unsigned long long gqa_launch_count(void) { return g_launches.load(); }
 
 size_t attn_bwd_workspace_bytes(int seq_len, int n_heads, int n_kv_heads, int head_dim) {
-  (void)n_kv_heads;
-  (void)head_dim;
-  if (seq_len <= 0 || n_heads <= 0) return kWsHeader;
+  if (seq_len <= 0 || n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads) return kWsHeader;
+  const Shape sh{seq_len, n_heads, n_kv_heads, head_dim, n_heads / n_kv_heads, 1.f};
+  if (tc_supported(sh)) return tc_ws_layout(seq_len, n_heads, n_kv_heads, head_dim).total;
   return ws_layout(seq_len, n_heads).total;
 }
 
@@ -147,8 +147,20 @@ gqa_status attn_bwd(const float* Q, const float* K, const float* V, const float*
                     const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
                     int seq_len, int n_heads, int n_kv_heads, int head_dim, float scale,
                     void* workspace, size_t workspace_bytes, void* stream) {
-  return attn_bwd_simt(Q, K, V, dO, LSE, seg, dQ, dK, dV, seq_len, n_heads, n_kv_heads,
-                       head_dim, scale, workspace, workspace_bytes, stream);
+  gqa_status r = check_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, seq_len, n_heads, n_kv_heads,
+                           head_dim, scale, workspace, workspace_bytes);
+  if (r != GQA_OK || seq_len == 0) return r;
+  const Shape sh{seq_len, n_heads, n_kv_heads, head_dim, n_heads / n_kv_heads, scale};
+  if (!tc_supported(sh))
+    return attn_bwd_simt(Q, K, V, dO, LSE, seg, dQ, dK, dV, seq_len, n_heads, n_kv_heads,
+                         head_dim, scale, workspace, workspace_bytes, stream);
+  const size_t need = tc_ws_layout(seq_len, n_heads, n_kv_heads, head_dim).total;
+  if (workspace_bytes < need)
+    return set_error(GQA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
+    return check_launch("workspace header reset");
+  return tc_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st);
 }
 
 gqa_status rope_bwd_inplace(float* dX, int seq_len, int n_heads, int head_dim, int pos_offset,

@@ -40,6 +40,15 @@ inline WsLayout ws_layout(int S, int H) {
   return w;
 }
 
+// The tensor-core path needs more: K^T per kv head, [Hk*d rows][ld_kt],
+// ld_kt = S rounded up to 32 (so TMA row strides stay 128-byte multiples).
+struct TcWsLayout {
+  long long ld_kt;
+  size_t kt_off;
+  size_t total;
+};
+TcWsLayout tc_ws_layout(int S, int H, int Hk, int d);
+
 // Problem description passed by value to kernels.
 struct Shape {
   int S, H, Hk, d, G;   // seq_len, n_heads, n_kv_heads, head_dim, H / Hk
@@ -82,6 +91,17 @@ gqa_status simt_fwd_lse(const float* Q, const float* K, const float* V, const ui
 gqa_status simt_bwd(const float* Q, const float* K, const float* V, const float* dO,
                     const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
                     const Shape& sh, char* ws, cudaStream_t st);
+
+gqa_status simt_bwd_key_major(const float* Q, const float* K, const float* V, const float* dO,
+                              const float* LSE, const uint32_t* seg, float* dK, float* dV,
+                              const Shape& sh, char* ws, cudaStream_t st);
+gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cudaStream_t st);
+
+// Tensor-core backward, tc_bwd.cu: true if this shape has a tensor-core path.
+bool tc_supported(const Shape& sh);
+gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* dO,
+                  const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
+                  const Shape& sh, char* ws, cudaStream_t st);
 
 // RoPE backward, rope_bwd.cu
 gqa_status rope_bwd_launch(float* X, int S, int H, int d, int pos_offset, float base,

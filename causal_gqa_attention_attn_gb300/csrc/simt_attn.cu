@@ -449,7 +449,53 @@ gqa_status bwd_launch(const float* Q, const float* K, const float* V, const floa
   return check_launch("simt backward (key-major)");
 }
 
+// Smallest seg over each `tile`-row query tile (one warp per tile).
+__global__ void tile_minseg_kernel(const uint32_t* __restrict__ seg, int S, int tile,
+                                   uint32_t* __restrict__ out, int n_tiles) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
+  if (w >= n_tiles) return;
+  unsigned v = 0xffffffffu;
+  for (int i = lane; i < tile; i += 32) {
+    const int q = w * tile + i;
+    if (q < S) v = min(v, __ldg(seg + q));
+  }
+  for (int o = 16; o >= 1; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (lane == 0) out[w] = v;
+}
+
+template <int DP>
+gqa_status key_major_launch(const float* Q, const float* K, const float* V, const float* dO,
+                            const float* LSE, const uint32_t* seg, float* dK, float* dV,
+                            const Shape& sh, char* ws, cudaStream_t st) {
+  const WsLayout L = ws_layout(sh.S, sh.H);
+  const float* Dws = reinterpret_cast<const float*>(ws + L.d_off);
+  const uint32_t* minseg = reinterpret_cast<const uint32_t*>(ws + L.minseg64);
+  const size_t s2 = sizeof(KmSmem<DP>);
+  if (allow_smem(bwd_key_major<DP>, s2) != cudaSuccess) return check_launch("bwd smem attribute");
+  const int nt = (sh.S + BT - 1) / BT;
+  bwd_key_major<DP><<<dim3(nt, sh.Hk), NT, s2, st>>>(Q, K, V, dO, LSE, seg, Dws, minseg, dK, dV, sh);
+  note_launch();
+  return check_launch("simt backward (key-major)");
+}
+
 }  // namespace
+
+gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cudaStream_t st) {
+  const int n_tiles = (S + tile - 1) / tile;
+  const int warps_per_block = 8;
+  tile_minseg_kernel<<<(n_tiles + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0,
+                       st>>>(seg, S, tile, out, n_tiles);
+  note_launch();
+  return check_launch("tile min seg");
+}
+
+gqa_status simt_bwd_key_major(const float* Q, const float* K, const float* V, const float* dO,
+                              const float* LSE, const uint32_t* seg, float* dK, float* dV,
+                              const Shape& sh, char* ws, cudaStream_t st) {
+  if (sh.d <= 32) return key_major_launch<32>(Q, K, V, dO, LSE, seg, dK, dV, sh, ws, st);
+  if (sh.d <= 64) return key_major_launch<64>(Q, K, V, dO, LSE, seg, dK, dV, sh, ws, st);
+  return key_major_launch<128>(Q, K, V, dO, LSE, seg, dK, dV, sh, ws, st);
+}
 
 gqa_status simt_fwd_lse(const float* Q, const float* K, const float* V, const uint32_t* seg,
                         float* O, float* LSE, const Shape& sh, cudaStream_t st) {

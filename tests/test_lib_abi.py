@@ -46,7 +46,9 @@ def test_workspace_size(L):
     a = L.attn_bwd_workspace_bytes(4096, 32, 8, 128)
     b = L.attn_bwd_workspace_bytes(16384, 32, 8, 128)
     assert a % 256 == 0 and b % 256 == 0
-    assert b >= 16384 * 32 * 4 > a >= 4096 * 32 * 4
+    assert b > a >= 4096 * 32 * 4 + 4096 * 8 * 128 * 4     # D + K^T of the tensor-core path
+    odd = L.attn_bwd_workspace_bytes(4096, 32, 8, 100)      # CUDA-core only: D and tile minima
+    assert 4096 * 32 * 4 <= odd < a
     assert L.attn_bwd_workspace_bytes(0, 4, 2, 32) >= 0
 
 
