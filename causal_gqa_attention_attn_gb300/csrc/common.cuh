@@ -42,9 +42,12 @@ inline WsLayout ws_layout(int S, int H) {
 
 // The tensor-core path needs more: K^T per kv head, [Hk*d rows][ld_kt],
 // ld_kt = S rounded up to 32 (so TMA row strides stay 128-byte multiples).
+// Q^T and dO^T per kv group, [Hk*d rows][ld_qt] with column q*G + h'
+// (ld_qt = S*G rounded up to 32), and the minimum seg per key-major block of
+// (128 or 64)/G queries.
 struct TcWsLayout {
-  long long ld_kt;
-  size_t kt_off;
+  long long ld_kt, ld_qt;
+  size_t kt_off, qt_off, dot_off, blk_off;
   size_t total;
 };
 TcWsLayout tc_ws_layout(int S, int H, int Hk, int d);

@@ -638,6 +638,46 @@ gqa_status map_2d(CUtensorMap* m, const float* base, long long cols, long long r
   return GQA_OK;
 }
 
+// 3-D fp32 map over X [S][Hx][d]: box = 32 dims x `bh` heads x `bq` queries.
+gqa_status map_3d(CUtensorMap* m, const float* base, int d, int Hx, int S, int bh, int bq) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return set_error(GQA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hx, (cuuint64_t)S};
+  cuuint64_t strides[2] = {(cuuint64_t)d * sizeof(float), (cuuint64_t)Hx * d * sizeof(float)};
+  cuuint32_t box[3] = {32, (cuuint32_t)bh, (cuuint32_t)bq};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(GQA_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d)", (int)r);
+  return GQA_OK;
+}
+
+template <int D>
+gqa_status km_launch(const float* Q, const float* K, const float* V, const float* dO,
+                     const float* LSE, const uint32_t* seg, float* dK, float* dV, const float* Qt,
+                     const float* dOt, long long ld_qt, const float* Dws, const uint32_t* blk_minseg,
+                     uint32_t* status, const Shape& sh, cudaStream_t st) {
+  using C = KmCfg<D>;
+  const int QB = C::NQ / sh.G;
+  CUtensorMap mv, mq, mdo, mqt, mdot;
+  gqa_status r;
+  if ((r = map_2d(&mv, V, (long long)sh.Hk * D, sh.S, (long long)sh.Hk * D, 128)) != GQA_OK) return r;
+  if ((r = map_3d(&mq, Q, D, sh.H, sh.S, sh.G, QB)) != GQA_OK) return r;
+  if ((r = map_3d(&mdo, dO, D, sh.H, sh.S, sh.G, QB)) != GQA_OK) return r;
+  const long long cols = (long long)sh.S * sh.G;
+  if ((r = map_2d(&mqt, Qt, cols, (long long)sh.Hk * D, ld_qt, D)) != GQA_OK) return r;
+  if ((r = map_2d(&mdot, dOt, cols, (long long)sh.Hk * D, ld_qt, D)) != GQA_OK) return r;
+  if (cudaFuncSetAttribute(tc_key_major<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::SMEM_BYTES) != cudaSuccess)
+    return check_launch("key-major smem attribute");
+  dim3 grid((sh.S + 127) / 128, sh.Hk);
+  tc_key_major<D><<<grid, kThreads, C::SMEM_BYTES, st>>>(mv, mq, mdo, mqt, mdot, K, LSE, Dws, seg,
+                                                         blk_minseg, dK, dV, status, sh);
+  note_launch();
+  return check_launch("tensor-core key-major");
+}
+
 gqa_status transpose_launch(const float* X, float* Xt, int S, int Hk, int Gx, int d, long long ld,
                             cudaStream_t st) {
   const long long nrows = (long long)S * Gx;
@@ -674,15 +714,22 @@ gqa_status qm_launch(const float* Q, const float* K, const float* V, const float
 TcWsLayout tc_ws_layout(int S, int H, int Hk, int d) {
   TcWsLayout t;
   const WsLayout base = ws_layout(S, H);
+  const long long G = H / Hk;
   t.ld_kt = ((long long)S + 31) / 32 * 32;
+  t.ld_qt = ((long long)S * G + 31) / 32 * 32;
   t.kt_off = base.total;
-  t.total = t.kt_off + align256((size_t)Hk * d * t.ld_kt * sizeof(float));
+  t.qt_off = t.kt_off + align256((size_t)Hk * d * t.ld_kt * sizeof(float));
+  t.dot_off = t.qt_off + align256((size_t)Hk * d * t.ld_qt * sizeof(float));
+  t.blk_off = t.dot_off + align256((size_t)Hk * d * t.ld_qt * sizeof(float));
+  t.total = t.blk_off + align256((size_t)S * sizeof(uint32_t));
   return t;
 }
 
 bool tc_supported(const Shape& sh) {
-  return (sh.d == 32 || sh.d == 64 || sh.d == 128) && sh.G >= 1 && sh.G <= 128 &&
-         (128 % sh.G) == 0;
+  // G must divide the 128-row slab and the key-major (query, head) block
+  const int nq = (sh.d == 128) ? 64 : 128;
+  return (sh.d == 32 || sh.d == 64 || sh.d == 128) && sh.G >= 1 && sh.G <= nq &&
+         (nq % sh.G) == 0;
 }
 
 gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* dO,
@@ -693,18 +740,33 @@ gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* d
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   float* Dws = reinterpret_cast<float*>(ws + L.d_off);
   float* Kt = reinterpret_cast<float*>(ws + T.kt_off);
+  float* Qt = reinterpret_cast<float*>(ws + T.qt_off);
+  float* dOt = reinterpret_cast<float*>(ws + T.dot_off);
+  uint32_t* blk = reinterpret_cast<uint32_t*>(ws + T.blk_off);
+  const int QB = ((sh.d == 128) ? 64 : 128) / sh.G;
   gqa_status r;
-  if ((r = tile_minseg(seg, sh.S, 64, reinterpret_cast<uint32_t*>(ws + L.minseg64), st)) != GQA_OK)
-    return r;
+  if ((r = tile_minseg(seg, sh.S, QB, blk, st)) != GQA_OK) return r;
   if ((r = transpose_launch(K, Kt, sh.S, sh.Hk, 1, sh.d, T.ld_kt, st)) != GQA_OK) return r;
-  profile_before(st, "tc_query_major+simt_key_major");
+  if ((r = transpose_launch(Q, Qt, sh.S, sh.Hk, sh.G, sh.d, T.ld_qt, st)) != GQA_OK) return r;
+  if ((r = transpose_launch(dO, dOt, sh.S, sh.Hk, sh.G, sh.d, T.ld_qt, st)) != GQA_OK) return r;
+  profile_before(st, "tc_query_major+tc_key_major");
   switch (sh.d) {
-    case 32: r = qm_launch<32>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, status, sh, st); break;
-    case 64: r = qm_launch<64>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, status, sh, st); break;
-    default: r = qm_launch<128>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, status, sh, st); break;
+    case 32:
+      r = qm_launch<32>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, status, sh, st);
+      if (r == GQA_OK)
+        r = km_launch<32>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, status, sh, st);
+      break;
+    case 64:
+      r = qm_launch<64>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, status, sh, st);
+      if (r == GQA_OK)
+        r = km_launch<64>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, status, sh, st);
+      break;
+    default:
+      r = qm_launch<128>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, status, sh, st);
+      if (r == GQA_OK)
+        r = km_launch<128>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, status, sh, st);
+      break;
   }
-  if (r != GQA_OK) return r;
-  r = simt_bwd_key_major(Q, K, V, dO, LSE, seg, dK, dV, sh, ws, st);
   profile_after(st);
   return r;
 }
