@@ -5,7 +5,7 @@
 #include <stdint.h>
 #include <stddef.h>
 
-#include "../../include/gqa_attn.h"
+#include "gqa_attn.h"   // include/ is on the include path (build.py)
 
 namespace gqa {
 
@@ -47,7 +47,7 @@ inline WsLayout ws_layout(int S, int H) {
 // (128 or 64)/G queries.
 struct TcWsLayout {
   long long ld_kt, ld_qt;
-  size_t kt_off, qt_off, dot_off, blk_off;
+  size_t kt_off, qt_off, dot_off, blk_off, blkmax_off;
   size_t total;
 };
 TcWsLayout tc_ws_layout(int S, int H, int Hk, int d);
@@ -98,7 +98,8 @@ gqa_status simt_bwd(const float* Q, const float* K, const float* V, const float*
 gqa_status simt_bwd_key_major(const float* Q, const float* K, const float* V, const float* dO,
                               const float* LSE, const uint32_t* seg, float* dK, float* dV,
                               const Shape& sh, char* ws, cudaStream_t st);
-gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cudaStream_t st);
+gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cudaStream_t st,
+                       uint32_t* out_max = nullptr);
 
 // Tensor-core backward, tc_bwd.cu: true if this shape has a tensor-core path.
 bool tc_supported(const Shape& sh);

@@ -449,18 +449,29 @@ gqa_status bwd_launch(const float* Q, const float* K, const float* V, const floa
   return check_launch("simt backward (key-major)");
 }
 
-// Smallest seg over each `tile`-row query tile (one warp per tile).
+// Smallest (and optionally largest) seg over each `tile`-row query tile (one warp per tile).
 __global__ void tile_minseg_kernel(const uint32_t* __restrict__ seg, int S, int tile,
-                                   uint32_t* __restrict__ out, int n_tiles) {
+                                   uint32_t* __restrict__ out, uint32_t* __restrict__ out_max,
+                                   int n_tiles) {
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
   if (w >= n_tiles) return;
-  unsigned v = 0xffffffffu;
+  unsigned v = 0xffffffffu, m = 0u;
   for (int i = lane; i < tile; i += 32) {
     const int q = w * tile + i;
-    if (q < S) v = min(v, __ldg(seg + q));
+    if (q < S) {
+      const unsigned x = __ldg(seg + q);
+      v = min(v, x);
+      m = max(m, x);
+    }
   }
-  for (int o = 16; o >= 1; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if (lane == 0) out[w] = v;
+  for (int o = 16; o >= 1; o >>= 1) {
+    v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  }
+  if (lane == 0) {
+    out[w] = v;
+    if (out_max) out_max[w] = m;
+  }
 }
 
 template <int DP>
@@ -480,11 +491,12 @@ gqa_status key_major_launch(const float* Q, const float* K, const float* V, cons
 
 }  // namespace
 
-gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cudaStream_t st) {
+gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cudaStream_t st,
+                       uint32_t* out_max) {
   const int n_tiles = (S + tile - 1) / tile;
   const int warps_per_block = 8;
   tile_minseg_kernel<<<(n_tiles + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0,
-                       st>>>(seg, S, tile, out, n_tiles);
+                       st>>>(seg, S, tile, out, out_max, n_tiles);
   note_launch();
   return check_launch("tile min seg");
 }

@@ -8,13 +8,12 @@
 //   16-byte chunk index of each row XOR-ed with (row % 8). That is exactly
 //   what a TMA load with CU_TENSOR_MAP_SWIZZLE_128B and a 32-float box
 //   writes, and it is an 8-row x 128-byte swizzle atom stack that the MMA
-//   reads either
-//     K-major   (K along the 128-byte rows):  SBO = 1024 B between 8-row
-//               groups; a K step of 8 floats advances the start by 32 B;
-//               the next panel is the next 32 K values;
-//     MN-major  (M or N along the 128-byte rows, K along rows): LBO = panel
-//               size between 32-wide M/N groups, SBO = 1024 B between
-//               8-row K groups; a K step of 8 rows advances the start by 1 KB.
+//   reads K-major (K along the 128-byte rows): SBO = 1024 B between 8-row
+//   groups; a K step of 8 floats advances the start by 32 B; the next panel
+//   holds the next 32 K values.
+// Every TF32 operand here is K-major: on this part the kind::tf32 MMA gave
+// all-zero results with the transpose (MN-major) bits set, so where a
+// contraction needs the other orientation the code stages a transposed copy.
 #pragma once
 
 #include <cuda.h>
@@ -105,6 +104,60 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            int w, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Multicast forms: the tile lands at the same shared-memory offset in every
+// CTA of the cluster named in `mask`, and signals each one's mbarrier at the
+// barrier's offset. Used only for tiles in this GPU's own memory.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y,
+                                               uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, int x, int y,
+                                               int z, uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_mc(void* dst, const CUtensorMap* map, int x, int y,
+                                               int z, int w, uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA in the cluster: release this CTA's prior shared
+// memory writes (e.g. mbarrier inits) and wait for all CTAs to arrive.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05: TMEM allocation, fences, MMA, commit
 // ---------------------------------------------------------------------------
@@ -153,6 +206,14 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
           smem_u32(bar))
       : "memory");
 }
+// The same, arriving on the barrier at `bar`'s offset in every CTA of `mask`.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
 
 // Shared-memory matrix descriptor, 128-byte swizzle, sm_100 descriptor version.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -163,6 +224,14 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
   d |= (uint64_t)1 << 46;   // descriptor version
   d |= (uint64_t)2 << 61;   // 128-byte swizzle
   return d;
+}
+
+// Descriptor increment for K step `ks` (8 fp32 = 32 bytes) of a K-major
+// operand stored as 128-byte panels of `panel_bytes` each: the start address
+// field is (address >> 4) in the low 14 bits, and shared-memory addresses stay
+// below 256 KB, so adding to the descriptor never carries out of the field.
+__host__ __device__ constexpr uint64_t desc_off(int ks, int panel_bytes) {
+  return (uint64_t)(((ks / 4) * panel_bytes + (ks % 4) * 32) >> 4);
 }
 
 // Instruction descriptor: kind::tf32, fp32 D, M x N, operand majorness.
