@@ -149,21 +149,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = 2 * nk;
   volatile int* abort = &bars.abort;
 
+  // The producer and MMA warps run their loops with all 32 lanes (waits
+  // included) so that addresses and descriptors are warp-uniform; one elected
+  // lane issues each TMA / MMA / commit. Issuing from a single thread inside a
+  // divergent branch cost 3-10x more cycles per MMA on this part.
   if (warp == 0) {
     // ---------------- TMA producer ----------------
-    if (lane == 0) {
+    if (elect_one()) {
       tma_prefetch_desc(&mapK);
       tma_prefetch_desc(&mapV);
       tma_prefetch_desc(&mapKt);
-      for (int c = 0; c < total; ++c) {
-        const int slot = c % Cfg::NSLOT;
-        if (c >= Cfg::NSLOT &&
-            !mbar_wait(&bars.kv_empty[slot], ((c / Cfg::NSLOT) - 1) & 1, abort, status, kSiteQmProducer))
-          break;
-        const int key0 = (kc0 + c % nk) * Cfg::BK;
-        unsigned char* sk = smem + slot * Cfg::SLOT_BYTES;
-        unsigned char* sv = sk + Cfg::TILE_BYTES;
-        const bool pass2 = c >= nk;
+    }
+    __syncwarp();
+    for (int c = 0; c < total; ++c) {
+      const int slot = c % Cfg::NSLOT;
+      if (c >= Cfg::NSLOT &&
+          !warp_wait(&bars.kv_empty[slot], ((c / Cfg::NSLOT) - 1) & 1, abort, status, kSiteQmProducer))
+        break;
+      const int key0 = (kc0 + c % nk) * Cfg::BK;
+      unsigned char* sk = smem + slot * Cfg::SLOT_BYTES;
+      unsigned char* sv = sk + Cfg::TILE_BYTES;
+      const bool pass2 = c >= nk;
+      if (elect_one()) {
         mbar_arrive_expect_tx(&bars.kv_full[slot], (pass2 ? 3 : 2) * Cfg::TILE_BYTES);
         // one box per tile (all its 128-byte panels); tile i of the chunk is
         // loaded by cluster rank i % C into every CTA
@@ -175,63 +182,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         load(1, sv, &mapV, key0, g * Cfg::PANELS);
         if (pass2) load(2, sv + Cfg::TILE_BYTES, &mapKt, g * D, key0 / 32);
       }
-      // leave only once every load this CTA issued has landed
-      for (int c = max(0, total - Cfg::NSLOT); c < total; ++c)
-        mbar_wait(&bars.kv_full[c % Cfg::NSLOT], (c / Cfg::NSLOT) & 1, abort, status, kSiteQmProducer);
+      __syncwarp();
     }
+    // leave only once every load this CTA issued has landed
+    for (int c = max(0, total - Cfg::NSLOT); c < total; ++c)
+      warp_wait(&bars.kv_full[c % Cfg::NSLOT], (c / Cfg::NSLOT) & 1, abort, status, kSiteQmProducer);
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_tf32(128, Cfg::BK, false, false);   // S, dP: N = BK keys
-      constexpr uint32_t id_q = idesc_tf32(128, D, false, false);       // dQ: N = d, B = K^T chunk
-      bool ok = mbar_wait(&bars.qdo_ready, 0, abort, status, kSiteQmMma);
-      bool first_dq = true;
-      // a slot is free once this CTA's MMAs that read it are done, in every CTA
-      auto release = [&](int slot) {
-        if (C == 1) mma_commit(&bars.kv_empty[slot]);
-        else mma_commit_mc(&bars.kv_empty[slot], all_ctas);
-      };
-      auto issue_dq = [&](int cc) -> bool {
-        const int st = cc & 1, slot = cc % Cfg::NSLOT;
-        if (!mbar_wait(&bars.s_free[st], (cc / 2) & 1, abort, status, kSiteQmMma)) return false;
+    constexpr uint32_t id_s = idesc_tf32(128, Cfg::BK, false, false);   // S, dP: N = BK keys
+    constexpr uint32_t id_q = idesc_tf32(128, D, false, false);         // dQ: N = d, B = K^T chunk
+    bool ok = warp_wait(&bars.qdo_ready, 0, abort, status, kSiteQmMma);
+    bool first_dq = true;
+    const uint64_t desc0 = sdesc(smem_u32(smem), 16, 1024);
+    // a slot is free once this CTA's MMAs that read it are done, in every CTA
+    auto release = [&](int slot) {
+      if (C == 1) mma_commit(&bars.kv_empty[slot]);
+      else mma_commit_mc(&bars.kv_empty[slot], all_ctas);
+    };
+    auto issue_dq = [&](int cc) -> bool {
+      const int st = cc & 1, slot = cc % Cfg::NSLOT;
+      if (!warp_wait(&bars.s_free[st], (cc / 2) & 1, abort, status, kSiteQmMma)) return false;
+      const uint64_t bkt = desc0 + (uint64_t)((slot * Cfg::SLOT_BYTES + 2 * Cfg::TILE_BYTES) >> 4);
+      const uint32_t a_ds = tmem + Cfg::t_s(st), d_q = tmem + Cfg::T_DQ;
+      const uint32_t acc0 = first_dq ? 0u : 1u;
+      if (elect_one()) {
         tc_fence_after();
-        const uint64_t bkt = sdesc(smem_u32(smem + slot * Cfg::SLOT_BYTES + 2 * Cfg::TILE_BYTES), 16, 1024);
-        const uint32_t a_ds = tmem + Cfg::t_s(st), d_q = tmem + Cfg::T_DQ;
-        mma_ts(d_q, a_ds, bkt, id_q, first_dq ? 0u : 1u);
+        mma_ts(d_q, a_ds, bkt, id_q, acc0);
 #pragma unroll
         for (int kk = 1; kk < Cfg::BK / 8; ++kk)
-          mma_ts(d_q, a_ds + 8 * kk, bkt + desc_off(kk, Cfg::KT_PANEL_BYTES), id_q, 1u);
-        first_dq = false;
+          mma_ts_acc(d_q, a_ds + 8 * kk, bkt + desc_off(kk, Cfg::KT_PANEL_BYTES), id_q);
         release(slot);
-        return true;
-      };
-      tc_fence_after();
-      for (int c = 0; ok && c < total; ++c) {
-        const int slot = c % Cfg::NSLOT, st = c & 1;
-        const bool pass2 = c >= nk;
-        if (!mbar_wait(&bars.kv_full[slot], (c / Cfg::NSLOT) & 1, abort, status, kSiteQmMma)) break;
-        if (c >= 2 && !mbar_wait(&bars.s_free[st], ((c - 2) / 2) & 1, abort, status, kSiteQmMma))
-          break;
+      }
+      __syncwarp();
+      first_dq = false;
+      return true;
+    };
+    for (int c = 0; ok && c < total; ++c) {
+      const int slot = c % Cfg::NSLOT, st = c & 1;
+      const bool pass2 = c >= nk;
+      if (!warp_wait(&bars.kv_full[slot], (c / Cfg::NSLOT) & 1, abort, status, kSiteQmMma)) break;
+      if (c >= 2 && !warp_wait(&bars.s_free[st], ((c - 2) / 2) & 1, abort, status, kSiteQmMma))
+        break;
+      const uint64_t bk = desc0 + (uint64_t)((slot * Cfg::SLOT_BYTES) >> 4);
+      const uint64_t bv = bk + ((uint64_t)Cfg::TILE_BYTES >> 4);
+      const uint32_t d_s = tmem + Cfg::t_s(st), d_dp = tmem + Cfg::t_dp(st);
+      const uint32_t a_q = tmem + Cfg::T_Q, a_do = tmem + Cfg::T_DO;
+      if (elect_one()) {
         tc_fence_after();
-        const uint64_t bk = sdesc(smem_u32(smem + slot * Cfg::SLOT_BYTES), 16, 1024);
-        const uint64_t bv = bk + ((uint64_t)Cfg::TILE_BYTES >> 4);
-        const uint32_t d_s = tmem + Cfg::t_s(st), d_dp = tmem + Cfg::t_dp(st);
-        const uint32_t a_q = tmem + Cfg::T_Q, a_do = tmem + Cfg::T_DO;
         mma_ts(d_s, a_q, bk, id_s, 0u);
         mma_ts(d_dp, a_do, bv, id_s, 0u);
 #pragma unroll
         for (int ks = 1; ks < D / 8; ++ks) {
           const uint64_t off = desc_off(ks, Cfg::PANEL_BYTES);
-          mma_ts(d_s, a_q + 8 * ks, bk + off, id_s, 1u);
-          mma_ts(d_dp, a_do + 8 * ks, bv + off, id_s, 1u);
+          mma_ts_acc(d_s, a_q + 8 * ks, bk + off, id_s);
+          mma_ts_acc(d_dp, a_do + 8 * ks, bv + off, id_s);
         }
         mma_commit(&bars.s_full[st]);
         if (!pass2) release(slot);
-        if (pass2 && c > nk && !issue_dq(c - 1)) { ok = false; break; }
       }
-      if (ok) ok = issue_dq(total - 1);
-      mma_commit(&bars.dq_done);     // also drains every MMA issued above
+      __syncwarp();
+      if (pass2 && c > nk && !issue_dq(c - 1)) { ok = false; break; }
     }
+    if (ok) ok = issue_dq(total - 1);
+    if (elect_one()) mma_commit(&bars.dq_done);     // also drains every MMA issued above
+    __syncwarp();
   } else {
     // ---------------- compute: two warpgroups, one TMEM lane (= one row) per thread ----------------
     // Warpgroup wg handles the chunks that use TMEM stage wg (c % 2 == wg), so
@@ -453,97 +467,106 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto visible = [&](int qb) { return __ldg(blk_minseg + qb) <= (unsigned)k_hi; };
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      const CUtensorMap* maps[4] = {&mapQ, &mapDO, &mapQt, &mapDOt};
+    // ---------------- TMA producer (warp-converged, elected issue) ----------------
+    const CUtensorMap* maps[4] = {&mapQ, &mapDO, &mapQt, &mapDOt};
+    if (elect_one()) {
       for (int i = 0; i < 4; ++i) tma_prefetch_desc(maps[i]);
       tma_prefetch_desc(&mapV);
       mbar_arrive_expect_tx(&bars.v_full, Cfg::V_BYTES);
       tma_load_3d(smem + Cfg::OFF_V, &mapV, 0, k0, g * (D / 32), &bars.v_full);
-      const int offs[4] = {Cfg::OFF_Q, Cfg::OFF_DO, Cfg::OFF_QT, Cfg::OFF_DOT};
-      int n = 0;
-      bool ok = true;
-      for (int qb = nqb - 1; ok && qb >= qb0; --qb) {
-        if (!visible(qb)) continue;
-        const int q0 = qb * QB;
-        // one box per tile; tile t is loaded by cluster rank t % C into every CTA
-        for (int t = 0; t < 4; ++t) {
-          if (n > 0 && !mbar_wait(&bars.empty[t], (n - 1) & 1, abort, status, kSiteKmProducer)) {
-            ok = false;
-            break;
-          }
+    }
+    __syncwarp();
+    const int offs[4] = {Cfg::OFF_Q, Cfg::OFF_DO, Cfg::OFF_QT, Cfg::OFF_DOT};
+    int n = 0;
+    bool ok = true;
+    for (int qb = nqb - 1; ok && qb >= qb0; --qb) {
+      if (!visible(qb)) continue;
+      const int q0 = qb * QB;
+      // one box per tile; tile t is loaded by cluster rank t % C into every CTA
+      for (int t = 0; t < 4; ++t) {
+        if (n > 0 && !warp_wait(&bars.empty[t], (n - 1) & 1, abort, status, kSiteKmProducer)) {
+          ok = false;
+          break;
+        }
+        if (elect_one()) {
           mbar_arrive_expect_tx(&bars.full[t], Cfg::BLK_BYTES);
-          if (C > 1 && t % C != (int)rank) continue;
-          unsigned char* dst = smem + offs[t];
-          if (t < 2) {          // Q / dO block: 4-D box (32 dims, G heads, QB queries, d/32 panels)
-            if (C == 1) tma_load_4d(dst, maps[t], 0, g * G, q0, 0, &bars.full[t]);
-            else tma_load_4d_mc(dst, maps[t], 0, g * G, q0, 0, &bars.full[t], all_ctas);
-          } else {              // Q^T / dO^T block: d rows x NQ (query, head) columns, in panels
-            if (C == 1) tma_load_3d(dst, maps[t], 0, g * D, (q0 * G) / 32, &bars.full[t]);
-            else tma_load_3d_mc(dst, maps[t], 0, g * D, (q0 * G) / 32, &bars.full[t], all_ctas);
+          if (C == 1 || t % C == (int)rank) {
+            unsigned char* dst = smem + offs[t];
+            if (t < 2) {          // Q / dO block: 4-D box (32 dims, G heads, QB queries, d/32 panels)
+              if (C == 1) tma_load_4d(dst, maps[t], 0, g * G, q0, 0, &bars.full[t]);
+              else tma_load_4d_mc(dst, maps[t], 0, g * G, q0, 0, &bars.full[t], all_ctas);
+            } else {              // Q^T / dO^T block: d rows x NQ (query, head) columns, in panels
+              if (C == 1) tma_load_3d(dst, maps[t], 0, g * D, (q0 * G) / 32, &bars.full[t]);
+              else tma_load_3d_mc(dst, maps[t], 0, g * D, (q0 * G) / 32, &bars.full[t], all_ctas);
+            }
           }
         }
-        ++n;
+        __syncwarp();
       }
-      // leave only once every load this CTA issued has landed
-      mbar_wait(&bars.v_full, 0, abort, status, kSiteKmProducer);
-      if (n > 0)
-        for (int t = 0; t < 4; ++t) mbar_wait(&bars.full[t], (n - 1) & 1, abort, status, kSiteKmProducer);
+      ++n;
     }
+    // leave only once every load this CTA issued has landed
+    warp_wait(&bars.v_full, 0, abort, status, kSiteKmProducer);
+    if (n > 0)
+      for (int t = 0; t < 4; ++t) warp_wait(&bars.full[t], (n - 1) & 1, abort, status, kSiteKmProducer);
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_tf32(128, Cfg::NQ, false, false);
-      constexpr uint32_t id_g = idesc_tf32(128, D, false, false);
-      bool ok = mbar_wait(&bars.v_full, 0, abort, status, kSiteKmMma) &&
-                mbar_wait(&bars.k_ready, 0, abort, status, kSiteKmMma);
-      auto release = [&](int t) {     // tile t is free once every CTA's MMAs read it
-        if (C == 1) mma_commit(&bars.empty[t]);
-        else mma_commit_mc(&bars.empty[t], all_ctas);
-      };
-      tc_fence_after();
-      const uint64_t av = sdesc(smem_u32(smem + Cfg::OFF_V), 16, 1024),
-                     bq = sdesc(smem_u32(smem + Cfg::OFF_Q), 16, 1024),
-                     bdo = sdesc(smem_u32(smem + Cfg::OFF_DO), 16, 1024),
-                     bqt = sdesc(smem_u32(smem + Cfg::OFF_QT), 16, 1024),
-                     bdot = sdesc(smem_u32(smem + Cfg::OFF_DOT), 16, 1024);
-      int n = 0;
-      for (int qb = nqb - 1; ok && qb >= qb0; --qb) {
-        if (!visible(qb)) continue;
-        const uint32_t par = n & 1;
-        if (!mbar_wait(&bars.full[0], par, abort, status, kSiteKmMma) ||
-            !mbar_wait(&bars.full[1], par, abort, status, kSiteKmMma)) { ok = false; break; }
+    // ---------------- MMA issuer (warp-converged, elected issue) ----------------
+    constexpr uint32_t id_s = idesc_tf32(128, Cfg::NQ, false, false);
+    constexpr uint32_t id_g = idesc_tf32(128, D, false, false);
+    bool ok = warp_wait(&bars.v_full, 0, abort, status, kSiteKmMma) &&
+              warp_wait(&bars.k_ready, 0, abort, status, kSiteKmMma);
+    auto release = [&](int t) {     // tile t is free once every CTA's MMAs read it
+      if (C == 1) mma_commit(&bars.empty[t]);
+      else mma_commit_mc(&bars.empty[t], all_ctas);
+    };
+    const uint64_t desc0 = sdesc(smem_u32(smem), 16, 1024);
+    const uint64_t av = desc0 + (uint64_t)(Cfg::OFF_V >> 4), bq = desc0 + (uint64_t)(Cfg::OFF_Q >> 4),
+                   bdo = desc0 + (uint64_t)(Cfg::OFF_DO >> 4),
+                   bqt = desc0 + (uint64_t)(Cfg::OFF_QT >> 4),
+                   bdot = desc0 + (uint64_t)(Cfg::OFF_DOT >> 4);
+    int n = 0;
+    for (int qb = nqb - 1; ok && qb >= qb0; --qb) {
+      if (!visible(qb)) continue;
+      const uint32_t par = n & 1;
+      if (!warp_wait(&bars.full[0], par, abort, status, kSiteKmMma) ||
+          !warp_wait(&bars.full[1], par, abort, status, kSiteKmMma)) { ok = false; break; }
+      if (elect_one()) {
         tc_fence_after();
         mma_ts(tmem + Cfg::T_S, tmem + Cfg::T_K, bq, id_s, 0u);
         mma_ss(tmem + Cfg::T_DP, av, bdo, id_s, 0u);
 #pragma unroll
         for (int ks = 1; ks < D / 8; ++ks) {
           const uint64_t ob = desc_off(ks, Cfg::BLK_PANEL_BYTES);
-          mma_ts(tmem + Cfg::T_S, tmem + Cfg::T_K + 8 * ks, bq + ob, id_s, 1u);
-          mma_ss(tmem + Cfg::T_DP, av + desc_off(ks, Cfg::V_PANEL_BYTES), bdo + ob, id_s, 1u);
+          mma_ts_acc(tmem + Cfg::T_S, tmem + Cfg::T_K + 8 * ks, bq + ob, id_s);
+          mma_ss_acc(tmem + Cfg::T_DP, av + desc_off(ks, Cfg::V_PANEL_BYTES), bdo + ob, id_s);
         }
         mma_commit(&bars.s_full);
         release(0);
         release(1);
-        if (!mbar_wait(&bars.p_ready, par, abort, status, kSiteKmMma) ||
-            !mbar_wait(&bars.full[2], par, abort, status, kSiteKmMma) ||
-            !mbar_wait(&bars.full[3], par, abort, status, kSiteKmMma)) { ok = false; break; }
+      }
+      __syncwarp();
+      if (!warp_wait(&bars.p_ready, par, abort, status, kSiteKmMma) ||
+          !warp_wait(&bars.full[2], par, abort, status, kSiteKmMma) ||
+          !warp_wait(&bars.full[3], par, abort, status, kSiteKmMma)) { ok = false; break; }
+      const uint32_t acc0 = (n > 0) ? 1u : 0u;
+      if (elect_one()) {
         tc_fence_after();
-        const uint32_t acc0 = (n > 0) ? 1u : 0u;
         mma_ts(tmem + Cfg::T_DV, tmem + Cfg::T_S, bdot, id_g, acc0);
         mma_ts(tmem + Cfg::T_DK, tmem + Cfg::T_DP, bqt, id_g, acc0);
 #pragma unroll
         for (int kk = 1; kk < Cfg::NQ / 8; ++kk) {
           const uint64_t ot = desc_off(kk, Cfg::T_PANEL_BYTES);
-          mma_ts(tmem + Cfg::T_DV, tmem + Cfg::T_S + 8 * kk, bdot + ot, id_g, 1u);
-          mma_ts(tmem + Cfg::T_DK, tmem + Cfg::T_DP + 8 * kk, bqt + ot, id_g, 1u);
+          mma_ts_acc(tmem + Cfg::T_DV, tmem + Cfg::T_S + 8 * kk, bdot + ot, id_g);
+          mma_ts_acc(tmem + Cfg::T_DK, tmem + Cfg::T_DP + 8 * kk, bqt + ot, id_g);
         }
         release(2);
         release(3);
-        ++n;
       }
-      mma_commit(&bars.acc_done);
+      __syncwarp();
+      ++n;
     }
+    if (elect_one()) mma_commit(&bars.acc_done);
+    __syncwarp();
   } else {
     // ---------------- compute: thread = key (TMEM lane); warpgroup wg owns half the columns ----------------
     const int wg = (warp - 2) >> 2;

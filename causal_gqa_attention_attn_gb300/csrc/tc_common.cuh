@@ -81,6 +81,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// The same wait by every lane of a warp; the result is made warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* status, uint32_t site) {
+  const bool ok = mbar_wait(bar, parity, abort, status, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// One lane of a converged warp (the same one each time): issue point for
+// TMA, MMA and commit instructions whose operands the warp computed.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\t@p mov.u32 %0, 1;\n\t}"
+      : "+r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------------------
 // TMA tile loads (no multicast)
 // ---------------------------------------------------------------------------
@@ -199,6 +216,20 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Accumulating form with a constant predicate (K steps after the first).
+__device__ __forceinline__ void mma_ts_acc(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
+               "r"(a_tmem), "l"(b_desc), "r"(idesc)
+               : "memory");
+}
+__device__ __forceinline__ void mma_ss_acc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, 1;" ::"r"(d_tmem),
+               "l"(a_desc), "l"(b_desc), "r"(idesc)
+               : "memory");
+}
+
 // Arrive on `bar` once every MMA this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
