@@ -32,8 +32,13 @@ namespace {
 
 using namespace tc;
 
-constexpr int kComputeWarps = 8;                      // two warpgroups
-constexpr int kThreads = 32 * (2 + kComputeWarps);   // producer, MMA, 8 compute warps
+// Warp roles: two TMA producer warps (one issuing stream reached ~43 B/clk
+// per SM on this part, two ~71), one MMA warp, two compute warpgroups.
+constexpr int kProducerWarps = 2;
+constexpr int kMmaWarp = kProducerWarps;
+constexpr int kFirstCompute = kProducerWarps + 1;
+constexpr int kComputeWarps = 8;
+constexpr int kThreads = 32 * (kFirstCompute + kComputeWarps);
 constexpr uint32_t kTmemCols = 512;
 
 // Status-word sites of bounded waits (ORed into the workspace status word).
@@ -107,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Cfg::NSLOT; ++i) {
-      mbar_init(&bars.kv_full[i], 1);
+      mbar_init(&bars.kv_full[i], kProducerWarps);   // each producer arms its own bytes
       mbar_init(&bars.kv_empty[i], C);      // every CTA of the cluster releases a slot
     }
     for (int i = 0; i < 2; ++i) {
@@ -120,14 +125,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars.kmin = 0xffffffffu;
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&bars.tmem_base, kTmemCols);
     tmem_relinquish();
   }
   __syncthreads();
   // smallest document start over the cluster's queries -> first chunk; all
   // CTAs of a cluster walk the same chunk range (the union of their slabs')
-  if (warp >= 2) {
+  if (warp >= kFirstCompute) {
     const int r = 32 * (warp & 3) + lane;
     unsigned v = 0xffffffffu;
     for (int i = 0; i < C; ++i) {
@@ -153,12 +158,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // included) so that addresses and descriptors are warp-uniform; one elected
   // lane issues each TMA / MMA / commit. Issuing from a single thread inside a
   // divergent branch cost 3-10x more cycles per MMA on this part.
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
+  if (warp < kProducerWarps) {
+    // ---------------- TMA producers: warp 0 loads K (and K^T in pass 2), warp 1 loads V ----------------
+    const int pw = warp;
     if (elect_one()) {
-      tma_prefetch_desc(&mapK);
-      tma_prefetch_desc(&mapV);
-      tma_prefetch_desc(&mapKt);
+      if (pw == 0) { tma_prefetch_desc(&mapK); tma_prefetch_desc(&mapKt); }
+      else tma_prefetch_desc(&mapV);
     }
     __syncwarp();
     for (int c = 0; c < total; ++c) {
@@ -171,23 +176,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       unsigned char* sv = sk + Cfg::TILE_BYTES;
       const bool pass2 = c >= nk;
       if (elect_one()) {
-        mbar_arrive_expect_tx(&bars.kv_full[slot], (pass2 ? 3 : 2) * Cfg::TILE_BYTES);
+        const uint32_t bytes = (pw == 0) ? (pass2 ? 2 : 1) * Cfg::TILE_BYTES : Cfg::TILE_BYTES;
+        mbar_arrive_expect_tx(&bars.kv_full[slot], bytes);
         // one box per tile (all its 128-byte panels); tile i of the chunk is
         // loaded by cluster rank i % C into every CTA
         auto load = [&](int i, void* dst, const CUtensorMap* m, int y, int z) {
           if (C == 1) tma_load_3d(dst, m, 0, y, z, &bars.kv_full[slot]);
           else if (i % C == (int)rank) tma_load_3d_mc(dst, m, 0, y, z, &bars.kv_full[slot], all_ctas);
         };
-        load(0, sk, &mapK, key0, g * Cfg::PANELS);
-        load(1, sv, &mapV, key0, g * Cfg::PANELS);
-        if (pass2) load(2, sv + Cfg::TILE_BYTES, &mapKt, g * D, key0 / 32);
+        if (pw == 0) {
+          load(0, sk, &mapK, key0, g * Cfg::PANELS);
+          if (pass2) load(2, sv + Cfg::TILE_BYTES, &mapKt, g * D, key0 / 32);
+        } else {
+          load(1, sv, &mapV, key0, g * Cfg::PANELS);
+        }
       }
       __syncwarp();
     }
     // leave only once every load this CTA issued has landed
     for (int c = max(0, total - Cfg::NSLOT); c < total; ++c)
       warp_wait(&bars.kv_full[c % Cfg::NSLOT], (c / Cfg::NSLOT) & 1, abort, status, kSiteQmProducer);
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t id_s = idesc_tf32(128, Cfg::BK, false, false);   // S, dP: N = BK keys
     constexpr uint32_t id_q = idesc_tf32(128, D, false, false);         // dQ: N = d, B = K^T chunk
@@ -252,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // two chunks are in flight at once; each keeps a partial row sum of P dP
     // over its pass-1 chunks, and the two partials are added through shared
     // memory before the first dS is formed.
-    const int wg = (warp - 2) >> 2;
+    const int wg = (warp - kFirstCompute) >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int qi = r / G, q = q0 + qi;
     const int h = g * G + r % G;
@@ -365,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
   if (C > 1) cluster_sync();   // no CTA leaves while a peer may still signal it
 }
 
@@ -454,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars.abort = 0;
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&bars.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -466,14 +475,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &bars.abort;
   auto visible = [&](int qb) { return __ldg(blk_minseg + qb) <= (unsigned)k_hi; };
 
-  if (warp == 0) {
-    // ---------------- TMA producer (warp-converged, elected issue) ----------------
+  if (warp < kProducerWarps) {
+    // ---------------- TMA producers: warp 0 loads Q and Q^T, warp 1 dO, dO^T and V ----------------
+    const int pw = warp;
     const CUtensorMap* maps[4] = {&mapQ, &mapDO, &mapQt, &mapDOt};
     if (elect_one()) {
-      for (int i = 0; i < 4; ++i) tma_prefetch_desc(maps[i]);
-      tma_prefetch_desc(&mapV);
-      mbar_arrive_expect_tx(&bars.v_full, Cfg::V_BYTES);
-      tma_load_3d(smem + Cfg::OFF_V, &mapV, 0, k0, g * (D / 32), &bars.v_full);
+      tma_prefetch_desc(maps[pw]);
+      tma_prefetch_desc(maps[pw + 2]);
+      if (pw == 1) {
+        tma_prefetch_desc(&mapV);
+        mbar_arrive_expect_tx(&bars.v_full, Cfg::V_BYTES);
+        tma_load_3d(smem + Cfg::OFF_V, &mapV, 0, k0, g * (D / 32), &bars.v_full);
+      }
     }
     __syncwarp();
     const int offs[4] = {Cfg::OFF_Q, Cfg::OFF_DO, Cfg::OFF_QT, Cfg::OFF_DOT};
@@ -483,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!visible(qb)) continue;
       const int q0 = qb * QB;
       // one box per tile; tile t is loaded by cluster rank t % C into every CTA
-      for (int t = 0; t < 4; ++t) {
+      for (int t = pw; t < 4; t += 2) {
         if (n > 0 && !warp_wait(&bars.empty[t], (n - 1) & 1, abort, status, kSiteKmProducer)) {
           ok = false;
           break;
@@ -505,11 +518,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++n;
     }
-    // leave only once every load this CTA issued has landed
-    warp_wait(&bars.v_full, 0, abort, status, kSiteKmProducer);
+    // leave only once every load this warp issued has landed
+    if (pw == 1) warp_wait(&bars.v_full, 0, abort, status, kSiteKmProducer);
     if (n > 0)
-      for (int t = 0; t < 4; ++t) warp_wait(&bars.full[t], (n - 1) & 1, abort, status, kSiteKmProducer);
-  } else if (warp == 1) {
+      for (int t = pw; t < 4; t += 2) warp_wait(&bars.full[t], (n - 1) & 1, abort, status, kSiteKmProducer);
+  } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer (warp-converged, elected issue) ----------------
     constexpr uint32_t id_s = idesc_tf32(128, Cfg::NQ, false, false);
     constexpr uint32_t id_g = idesc_tf32(128, D, false, false);
@@ -569,11 +582,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------- compute: thread = key (TMEM lane); warpgroup wg owns half the columns ----------------
-    const int wg = (warp - 2) >> 2;
+    const int wg = (warp - kFirstCompute) >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int key = k0 + r;
     const uint32_t tl = lane_base(tmem, warp);
-    const int ct = threadIdx.x - 64;                       // 0..255 among compute threads
+    const int ct = threadIdx.x - 32 * kFirstCompute;       // 0..255 among compute threads
     {
       float v[16];
       const float* krow = K + (long long)key * sh.Hk * D + (long long)g * D;
@@ -675,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
   if (C > 1) cluster_sync();   // no CTA leaves while a peer may still signal it
 }
 
