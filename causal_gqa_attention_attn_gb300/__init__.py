@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
     L.gqa_profile_events.restype = None
     L.gqa_profile_stage_name.argtypes = []
     L.gqa_profile_stage_name.restype = ctypes.c_char_p
+    L.gqa_wait_selftest.argtypes = [P, Z, ctypes.c_longlong, P]
+    L.gqa_wait_selftest.restype = ctypes.c_int
     L.gqa_launch_count.argtypes = []
     L.gqa_launch_count.restype = ctypes.c_ulonglong
     L.gqa_last_error.argtypes = []

@@ -180,6 +180,18 @@ gqa_status rope_bwd_inplace(float* dX, int seq_len, int n_heads, int head_dim, i
   return rope_bwd_launch(dX, seq_len, n_heads, head_dim, pos_offset, base, (cudaStream_t)stream);
 }
 
+gqa_status gqa_wait_selftest(void* workspace, size_t workspace_bytes, long long limit_cycles,
+                             void* stream) {
+  if (workspace == nullptr || !aligned16(workspace))
+    return set_error(GQA_ERR_INVALID_ARG, "workspace is NULL or not 16-byte aligned");
+  if (workspace_bytes < kWsHeader)
+    return set_error(GQA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes,
+                     kWsHeader);
+  if (limit_cycles <= 0 || limit_cycles > 100000000LL)
+    return set_error(GQA_ERR_INVALID_ARG, "limit_cycles must be in (0, 1e8]");
+  return wait_selftest(workspace, limit_cycles, (cudaStream_t)stream);
+}
+
 gqa_status attn_read_device_status(const void* workspace, void* stream) {
   if (workspace == nullptr) return set_error(GQA_ERR_INVALID_ARG, "workspace is NULL");
   uint32_t word = 0;

@@ -107,6 +107,8 @@ gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* d
                   const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
                   const Shape& sh, char* ws, cudaStream_t st);
 
+gqa_status wait_selftest(void* workspace, long long limit_cycles, cudaStream_t st);
+
 // RoPE backward, rope_bwd.cu
 gqa_status rope_bwd_launch(float* X, int S, int H, int d, int pos_offset, float base,
                            cudaStream_t st);

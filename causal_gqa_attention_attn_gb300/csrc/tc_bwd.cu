@@ -724,6 +724,19 @@ __global__ void __launch_bounds__(256) group_transpose(const float* __restrict__
   }
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// arrives on, with a short limit, and must give up and record the site.
+__global__ void wait_selftest_kernel(uint32_t* status, long long limit) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    mbar_wait(&bar, 0, &abort_flag, status, 1u << 12, limit);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -895,6 +908,14 @@ gqa_status qm_launch(const float* Q, const float* K, const float* V, const float
 }
 
 }  // namespace
+
+gqa_status wait_selftest(void* workspace, long long limit_cycles, cudaStream_t st) {
+  if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
+    return check_launch("self-test status reset");
+  wait_selftest_kernel<<<1, 32, 0, st>>>(reinterpret_cast<uint32_t*>(workspace), limit_cycles);
+  note_launch();
+  return check_launch("wait self-test");
+}
 
 TcWsLayout tc_ws_layout(int S, int H, int Hk, int d) {
   TcWsLayout t;

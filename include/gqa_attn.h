@@ -158,6 +158,19 @@ const char* gqa_profile_stage_name(void);
 /* Number of kernels this library has launched in this process (all threads). */
 unsigned long long gqa_launch_count(void);
 
+/*
+ * gqa_wait_selftest — test helper for the device-side failure path (no
+ * counterpart on the pages). Launches one thread that waits, through the same
+ * bounded mbarrier wait the tensor-core kernels use, on a barrier that nothing
+ * arrives on, with a limit of limit_cycles SM cycles (at most 1e8, i.e. well
+ * under a second). The wait gives up, sets the status word in `workspace`
+ * (>= 256 bytes, its header is cleared first) and the kernel returns; a
+ * following attn_read_device_status() then reports GQA_ERR_DEVICE_TIMEOUT and
+ * the CUDA context stays usable. Nothing hangs and nothing faults.
+ */
+gqa_status gqa_wait_selftest(void* workspace, size_t workspace_bytes, long long limit_cycles,
+                             void* stream);
+
 /* Static string naming a status code. */
 const char* gqa_status_str(gqa_status status);
 
