@@ -45,37 +45,71 @@ constexpr uint32_t kTmemCols = 512;
 enum : uint32_t {
   kSiteQmProducer = 1u << 0, kSiteQmMma = 1u << 1, kSiteQmCompute = 1u << 2,
   kSiteKmProducer = 1u << 4, kSiteKmMma = 1u << 5, kSiteKmCompute = 1u << 6,
+  kSiteKmLayout = 1u << 7,   // dynamic shared memory not 1 KB aligned (nothing ran)
 };
 
 // ---------------------------------------------------------------------------
-// Query-major configuration
+// Query-major configuration. Both passes stream K / V (and K^T in pass 2) in
+// chunks of BK1 keys, one TMA box per tensor, chunk and CTA (on this part a
+// box costs about the same TMA time from 8 KB up to 32 KB, so few large boxes
+// keep the copies ahead). The boxes go through a ring of NUNIT equal units
+// with a full / empty barrier each: a pass-1 chunk takes two units (K, V), a
+// pass-2 chunk three (K, V, K^T). Pass 1 runs N = BK1 MMAs; pass 2 splits a
+// chunk into sub-chunks of BK2 keys so that the softmax of one sub-chunk
+// overlaps the MMAs of the next.
+//
+// C = CTA group. With C = 2 an SM pair runs M = 256 rows (two slabs) with
+// cta_group::2 MMAs: each CTA stages half of every B operand (its BK1/2 keys
+// of a K / V chunk, its d/2 rows of a K^T chunk), so each SM's shared memory
+// takes half the TMA writes and half the tensor-core reads per flop (the two
+// together are what limits the one-SM kernel). An MMA with N columns takes
+// rows [0, N/2) of B from the even CTA and [N/2, N) from the odd one, so a
+// pass-2 sub-chunk h is made of keys h*BK2/2 + [0, BK2/2) of each CTA's half
+// (a fixed permutation of the chunk's keys, undone by key_of()).
 // ---------------------------------------------------------------------------
-template <int D_>
+template <int D_, int C_>
 struct QmCfg {
-  static constexpr int D = D_;
-  static constexpr int BK = (D == 128) ? 32 : 64;          // keys per chunk
+  static constexpr int D = D_, C = C_;
+  static constexpr int BK1 = 64;                            // keys per chunk
+  static constexpr int BK2 = (D == 128) ? 32 : 64;          // keys per pass-2 sub-chunk
+  static constexpr int NSUB = BK1 / BK2;
+  static constexpr int HALF1 = BK1 / C, HALF2 = BK2 / C;    // this CTA's keys of a chunk / sub-chunk
   static constexpr int PANELS = D / 32;
-  static constexpr int PANEL_BYTES = BK * 128;             // BK rows x 32 floats
-  static constexpr int TILE_BYTES = PANELS * PANEL_BYTES;  // one K or V chunk
-  static constexpr int KT_PANELS = BK / 32;                // K^T chunk: d rows x BK keys
-  static constexpr int KT_PANEL_BYTES = D * 128;
-  static_assert(KT_PANELS * KT_PANEL_BYTES == TILE_BYTES, "K^T chunk size");
-  static constexpr int SLOT_BYTES = 3 * TILE_BYTES;        // K, V, K^T
-  static constexpr int NSLOT = (4 * SLOT_BYTES <= 200 * 1024) ? 4 : 3;
+  static constexpr int KV_PANEL_BYTES = HALF1 * 128;        // K / V unit: HALF1 rows x 32 floats per panel
+  static constexpr int UNIT_BYTES = PANELS * KV_PANEL_BYTES;
+  static constexpr int KT_ROWS = D / C;                     // K^T unit: d/C rows x 32 keys per panel
+  static constexpr int KT_PANELS = BK1 / 32;
+  static constexpr int KT_PANEL_BYTES = KT_ROWS * 128;
+  static_assert(KT_PANELS * KT_PANEL_BYTES == UNIT_BYTES, "K^T unit size");
+  static constexpr int NUNIT = (192 * 1024 / UNIT_BYTES < 12) ? 192 * 1024 / UNIT_BYTES : 12;
+  static_assert(NUNIT >= 6, "ring depth");
   // + alignment slack; at least 120 KB so that one CTA (holding all 512 TMEM
   // columns) runs per SM and a second never waits in tcgen05.alloc
   static constexpr int SMEM_BYTES =
-      (NSLOT * SLOT_BYTES + 1024 > 120 * 1024) ? NSLOT * SLOT_BYTES + 1024 : 120 * 1024;
-  // TMEM columns
+      (NUNIT * UNIT_BYTES + 1024 > 120 * 1024) ? NUNIT * UNIT_BYTES + 1024 : 120 * 1024;
+  // TMEM columns: Q | dO | dQ | stages. A pass-1 stage holds S and dP of a
+  // chunk (2 BK1 columns); when two do not fit beside dQ, stage 1 of pass 1
+  // uses the dQ columns, which pass 1 does not touch. The two pass-2 stages
+  // (2 BK2 columns each) lie inside the pass-1 stage columns.
   static constexpr uint32_t T_Q = 0, T_DO = D, T_DQ = 2 * D, T_ST = 3 * D;
-  static constexpr uint32_t t_s(int st) { return T_ST + st * 2 * BK; }
-  static constexpr uint32_t t_dp(int st) { return T_ST + st * 2 * BK + BK; }
-  static_assert(3 * D + 4 * BK <= 512, "TMEM budget");
-  static_assert(PANEL_BYTES % 1024 == 0, "panels must keep 1 KB swizzle alignment");
+  static constexpr uint32_t W1 = 2 * BK1, W2 = 2 * BK2;
+  static constexpr bool P1_IN_DQ = T_ST + 2 * W1 > 512;
+  static constexpr uint32_t p1_stage(int st) { return st == 0 ? T_ST : (P1_IN_DQ ? T_DQ : T_ST + W1); }
+  static constexpr uint32_t p2_stage(int st) { return T_ST + st * W2; }
+  static_assert(T_ST + W1 <= 512 && T_ST + 2 * W2 <= 512, "TMEM budget");
+  static_assert(!P1_IN_DQ || (W1 <= D && 2 * W2 <= W1), "pass-1 stage 1 must fit the dQ columns");
+  static_assert(P1_IN_DQ || W2 == W1, "pass-2 stages coincide with pass-1 stages");
+  static_assert(KV_PANEL_BYTES % 1024 == 0 && KT_PANEL_BYTES % 1024 == 0 &&
+                    (HALF2 * 128) % 1024 == 0 && HALF2 % 8 == 0,
+                "panels must keep 1 KB swizzle alignment");
+  // key offset (in the chunk) of column n of pass-2 sub-chunk h
+  static __device__ __forceinline__ int key_of(int h, int n) {
+    return (n / HALF2) * HALF1 + h * HALF2 + (n % HALF2);
+  }
 };
 
 struct QmBarriers {
-  uint64_t kv_full[4], kv_empty[4], s_full[2], s_free[2], qdo_ready, dq_done;
+  uint64_t full[12], empty[12], peer_full[12], s_full[2], s_free[2], qdo_ready, dq_done;
   uint32_t tmem_base;
   int abort;
   unsigned kmin;
@@ -86,6 +120,14 @@ __device__ __forceinline__ uint32_t lane_base(uint32_t tmem, int warp) {
   return tmem + ((uint32_t)(32 * (warp & 3)) << 16);
 }
 
+// Arrive on a barrier of the MMA-issuing CTA: this CTA's own (C = 1) or the
+// even CTA's of the pair (C = 2, a remote arrive at cluster scope).
+template <int C>
+__device__ __forceinline__ void arrive_issuer(uint64_t* bar) {
+  if constexpr (C == 1) mbar_arrive(bar);
+  else mbar_arrive_cl(mapa_u32(bar, 0));
+}
+
 template <int D, int C>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_query_major(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
@@ -94,7 +136,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const float* __restrict__ LSE, const uint32_t* __restrict__ seg,
                    float* __restrict__ dQ, float* __restrict__ Dws, uint32_t* __restrict__ status,
                    Shape sh) {
-  using Cfg = QmCfg<D>;
+  using Cfg = QmCfg<D, C>;
+  constexpr int NU = Cfg::NUNIT;
+  constexpr bool kCl = C > 1;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -104,34 +148,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_pad = gridDim.x;                           // slabs, padded to a multiple of C
   const int slab = n_pad - 1 - (int)blockIdx.x;          // longest rows first
   const uint32_t rank = (C > 1) ? cluster_ctarank() : 0u;
-  const int top_slab = n_pad - 1 - ((int)blockIdx.x - (int)rank);   // cluster's last slab
-  const uint16_t all_ctas = (uint16_t)((1u << C) - 1u);
+  const bool issuer = rank == 0;                         // issues the group's MMAs
+  const int top_slab = n_pad - 1 - ((int)blockIdx.x - (int)rank);   // the group's last slab
   const int g = blockIdx.y;
   const int q0 = slab * QR;
   const int S = sh.S, H = sh.H;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Cfg::NSLOT; ++i) {
-      mbar_init(&bars.kv_full[i], kProducerWarps);   // each producer arms its own bytes
-      mbar_init(&bars.kv_empty[i], C);      // every CTA of the cluster releases a slot
+    for (int i = 0; i < NU; ++i) {
+      mbar_init(&bars.full[i], 1);        // the producer warp of the unit arms its bytes
+      mbar_init(&bars.empty[i], 1);       // released by the issuer's MMA commit
+      mbar_init(&bars.peer_full[i], 1);   // C = 2: the odd CTA's unit landed (forwarded)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.s_free[i], kComputeWarps / 2);   // one warpgroup per stage
+      mbar_init(&bars.s_free[i], C * kComputeWarps / 2);   // the stage's warpgroup in each CTA
     }
-    mbar_init(&bars.qdo_ready, kComputeWarps);
+    mbar_init(&bars.qdo_ready, C * kComputeWarps);
     mbar_init(&bars.dq_done, 1);
     bars.abort = 0;
     bars.kmin = 0xffffffffu;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(&bars.tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_g<C>(&bars.tmem_base, kTmemCols);
+    tmem_relinquish_g<C>();
   }
   __syncthreads();
-  // smallest document start over the cluster's queries -> first chunk; all
-  // CTAs of a cluster walk the same chunk range (the union of their slabs')
+  // smallest document start over the group's queries -> first chunk; both
+  // CTAs of a pair walk the same chunk range (the union of their slabs')
   if (warp >= kFirstCompute) {
     const int r = 32 * (warp & 3) + lane;
     unsigned v = 0xffffffffu;
@@ -144,14 +189,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (C > 1) cluster_sync();   // the issuer's barriers are initialised before any remote arrive
   tc_fence_after();
-  if (C > 1) cluster_sync();   // peers' barriers are initialised before any multicast
   const uint32_t tmem = bars.tmem_base;
   const int q_last = min(top_slab * QR + QR, S) - 1;
-  const int kc0 = (int)(min(bars.kmin, (unsigned)q_last) / Cfg::BK);
-  const int kc1 = q_last / Cfg::BK;
-  const int nk = kc1 - kc0 + 1;
-  const int total = 2 * nk;
+  const int kc0 = (int)(min(bars.kmin, (unsigned)q_last) / Cfg::BK1);
+  const int nk = q_last / Cfg::BK1 - kc0 + 1;          // chunks per pass
+  const int n_units = 5 * nk;                          // 2 per pass-1 chunk, 3 per pass-2 chunk
+  const int n_sub = Cfg::NSUB * nk;                    // pass-2 sub-chunks
   volatile int* abort = &bars.abort;
 
   // The producer and MMA warps run their loops with all 32 lanes (waits
@@ -159,108 +204,145 @@ __global__ void __launch_bounds__(kThreads, 1)
   // lane issues each TMA / MMA / commit. Issuing from a single thread inside a
   // divergent branch cost 3-10x more cycles per MMA on this part.
   if (warp < kProducerWarps) {
-    // ---------------- TMA producers: warp 0 loads K (and K^T in pass 2), warp 1 loads V ----------------
+    // ---------------- TMA producers: warp pw loads this CTA's part of the units i with i % 2 == pw ----------------
     const int pw = warp;
     if (elect_one()) {
-      if (pw == 0) { tma_prefetch_desc(&mapK); tma_prefetch_desc(&mapKt); }
-      else tma_prefetch_desc(&mapV);
+      tma_prefetch_desc(&mapK);
+      tma_prefetch_desc(&mapV);
+      tma_prefetch_desc(&mapKt);
     }
     __syncwarp();
-    for (int c = 0; c < total; ++c) {
-      const int slot = c % Cfg::NSLOT;
-      if (c >= Cfg::NSLOT &&
-          !warp_wait(&bars.kv_empty[slot], ((c / Cfg::NSLOT) - 1) & 1, abort, status, kSiteQmProducer))
+    for (int i = pw; i < n_units; i += 2) {
+      const int u = i % NU;
+      if (i >= NU &&
+          !warp_wait<kCl>(&bars.empty[u], ((i / NU) - 1) & 1, abort, status, kSiteQmProducer))
         break;
-      const int key0 = (kc0 + c % nk) * Cfg::BK;
-      unsigned char* sk = smem + slot * Cfg::SLOT_BYTES;
-      unsigned char* sv = sk + Cfg::TILE_BYTES;
-      const bool pass2 = c >= nk;
+      // unit i: pass-1 chunk i/2 (K, V) or pass-2 chunk (i - 2nk)/3 (K, V, K^T)
+      const bool p1 = i < 2 * nk;
+      const int chunk = p1 ? i / 2 : (i - 2 * nk) / 3;
+      const int kind = p1 ? i % 2 : (i - 2 * nk) % 3;
+      const int key0 = (kc0 + chunk) * Cfg::BK1;
+      unsigned char* dst = smem + u * Cfg::UNIT_BYTES;
       if (elect_one()) {
-        const uint32_t bytes = (pw == 0) ? (pass2 ? 2 : 1) * Cfg::TILE_BYTES : Cfg::TILE_BYTES;
-        mbar_arrive_expect_tx(&bars.kv_full[slot], bytes);
-        // one box per tile (all its 128-byte panels); tile i of the chunk is
-        // loaded by cluster rank i % C into every CTA
-        auto load = [&](int i, void* dst, const CUtensorMap* m, int y, int z) {
-          if (C == 1) tma_load_3d(dst, m, 0, y, z, &bars.kv_full[slot]);
-          else if (i % C == (int)rank) tma_load_3d_mc(dst, m, 0, y, z, &bars.kv_full[slot], all_ctas);
-        };
-        if (pw == 0) {
-          load(0, sk, &mapK, key0, g * Cfg::PANELS);
-          if (pass2) load(2, sv + Cfg::TILE_BYTES, &mapKt, g * D, key0 / 32);
-        } else {
-          load(1, sv, &mapV, key0, g * Cfg::PANELS);
-        }
+        mbar_arrive_expect_tx(&bars.full[u], Cfg::UNIT_BYTES);
+        if (kind == 2)
+          tma_load_3d(dst, &mapKt, 0, g * D + (int)rank * Cfg::KT_ROWS, key0 / 32, &bars.full[u]);
+        else
+          tma_load_3d(dst, kind == 0 ? &mapK : &mapV, 0, key0 + (int)rank * Cfg::HALF1,
+                      g * Cfg::PANELS, &bars.full[u]);
       }
       __syncwarp();
     }
-    // leave only once every load this CTA issued has landed
-    for (int c = max(0, total - Cfg::NSLOT); c < total; ++c)
-      warp_wait(&bars.kv_full[c % Cfg::NSLOT], (c / Cfg::NSLOT) & 1, abort, status, kSiteQmProducer);
+    // leave only once every load this warp issued has landed
+    const int i_lo = max(0, n_units - NU);
+    for (int i = i_lo + (((i_lo & 1) != pw) ? 1 : 0); i < n_units; i += 2)
+      warp_wait<kCl>(&bars.full[i % NU], (i / NU) & 1, abort, status, kSiteQmProducer);
+  } else if (warp == kMmaWarp && !issuer) {
+    // ---------------- C = 2, odd CTA: forward each landed unit to the issuer ----------------
+    for (int i = 0; i < n_units; ++i) {
+      if (!warp_wait<kCl>(&bars.full[i % NU], (i / NU) & 1, abort, status, kSiteQmMma)) break;
+      if (lane == 0) mbar_arrive_cl(mapa_u32(&bars.peer_full[i % NU], 0));
+      __syncwarp();
+    }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer ----------------
-    constexpr uint32_t id_s = idesc_tf32(128, Cfg::BK, false, false);   // S, dP: N = BK keys
-    constexpr uint32_t id_q = idesc_tf32(128, D, false, false);         // dQ: N = d, B = K^T chunk
-    bool ok = warp_wait(&bars.qdo_ready, 0, abort, status, kSiteQmMma);
-    bool first_dq = true;
+    constexpr uint32_t id_s1 = idesc_tf32(128 * C, Cfg::BK1, false, false);   // pass 1 S, dP: N = BK1
+    constexpr uint32_t id_s2 = idesc_tf32(128 * C, Cfg::BK2, false, false);   // pass 2 S, dP: N = BK2
+    constexpr uint32_t id_q = idesc_tf32(128 * C, D, false, false);           // dQ: N = d
     const uint64_t desc0 = sdesc(smem_u32(smem), 16, 1024);
-    // a slot is free once this CTA's MMAs that read it are done, in every CTA
-    auto release = [&](int slot) {
-      if (C == 1) mma_commit(&bars.kv_empty[slot]);
-      else mma_commit_mc(&bars.kv_empty[slot], all_ctas);
+    auto unit_desc = [&](int i) { return desc0 + (uint64_t)(((i % NU) * Cfg::UNIT_BYTES) >> 4); };
+    // both CTAs' parts of unit i have landed
+    auto unit_wait = [&](int i) {
+      const uint32_t ph = (i / NU) & 1;
+      return warp_wait<kCl>(&bars.full[i % NU], ph, abort, status, kSiteQmMma) &&
+             (C == 1 || warp_wait<kCl>(&bars.peer_full[i % NU], ph, abort, status, kSiteQmMma));
     };
-    auto issue_dq = [&](int cc) -> bool {
-      const int st = cc & 1, slot = cc % Cfg::NSLOT;
-      if (!warp_wait(&bars.s_free[st], (cc / 2) & 1, abort, status, kSiteQmMma)) return false;
-      const uint64_t bkt = desc0 + (uint64_t)((slot * Cfg::SLOT_BYTES + 2 * Cfg::TILE_BYTES) >> 4);
-      const uint32_t a_ds = tmem + Cfg::t_s(st), d_q = tmem + Cfg::T_DQ;
-      const uint32_t acc0 = first_dq ? 0u : 1u;
-      if (elect_one()) {
-        tc_fence_after();
-        mma_ts(d_q, a_ds, bkt, id_q, acc0);
+    int use0 = 0, use1 = 0;       // uses of each TMEM stage so far (s_free phases)
+    // wait until the previous use of stage st has been released by its warpgroup(s)
+    auto stage_free = [&](int st) {
+      const int u = st ? use1 : use0;
+      return u == 0 || warp_wait<kCl>(&bars.s_free[st], (u - 1) & 1, abort, status, kSiteQmMma);
+    };
+    // S = Q K^T and dP = dO V^T into (ts, ts + n)
+    auto issue_sdp = [&](uint32_t ts, uint32_t n, uint32_t id, uint64_t bk, uint64_t bv) {
+      tc_fence_after();
+      mma_ts_g<C>(ts, tmem + Cfg::T_Q, bk, id, 0u);
+      mma_ts_g<C>(ts + n, tmem + Cfg::T_DO, bv, id, 0u);
 #pragma unroll
-        for (int kk = 1; kk < Cfg::BK / 8; ++kk)
-          mma_ts_acc(d_q, a_ds + 8 * kk, bkt + desc_off(kk, Cfg::KT_PANEL_BYTES), id_q);
-        release(slot);
+      for (int ks = 1; ks < D / 8; ++ks) {
+        const uint64_t o = desc_off(ks, Cfg::KV_PANEL_BYTES);
+        mma_ts_acc_g<C>(ts, tmem + Cfg::T_Q + 8 * ks, bk + o, id);
+        mma_ts_acc_g<C>(ts + n, tmem + Cfg::T_DO + 8 * ks, bv + o, id);
+      }
+    };
+    bool ok = warp_wait<kCl>(&bars.qdo_ready, 0, abort, status, kSiteQmMma);
+    // ---- pass 1: chunk c in stage c & 1 ----
+    for (int c = 0; ok && c < nk; ++c) {
+      const int st = c & 1;
+      if (!unit_wait(2 * c) || !unit_wait(2 * c + 1) || !stage_free(st)) { ok = false; break; }
+      if (elect_one()) {
+        issue_sdp(tmem + Cfg::p1_stage(st), Cfg::BK1, id_s1, unit_desc(2 * c), unit_desc(2 * c + 1));
+        mma_commit_g<C>(&bars.s_full[st]);
+        mma_commit_g<C>(&bars.empty[(2 * c) % NU]);
+        mma_commit_g<C>(&bars.empty[(2 * c + 1) % NU]);
       }
       __syncwarp();
-      first_dq = false;
+      if (st) ++use1; else ++use0;
+    }
+    // ---- pass 2: sub-chunk s (chunk s / NSUB, part s % NSUB) in stage s & 1 ----
+    int dq_use = 0;               // stage use index of the sub-chunk whose dQ is next
+    auto issue_dq = [&](int s) -> bool {
+      const int st = s & 1, j = s / Cfg::NSUB, h = s % Cfg::NSUB;
+      const int ikt = 2 * nk + 3 * j + 2;
+      if (!warp_wait<kCl>(&bars.s_free[st], dq_use & 1, abort, status, kSiteQmMma)) return false;
+      if (h == 0 && !unit_wait(ikt)) return false;
+      const uint32_t a_ds = tmem + Cfg::p2_stage(st), d_q = tmem + Cfg::T_DQ;
+      const uint64_t bkt = unit_desc(ikt);
+      if (elect_one()) {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < Cfg::BK2 / 8; ++kk) {
+          // K step kk: columns 8kk.. of the sub-chunk = keys key_of(h, 8kk).. of the chunk
+          const int key = Cfg::key_of(h, 8 * kk);
+          const uint64_t o = (uint64_t)(((key / 32) * Cfg::KT_PANEL_BYTES + (key % 32) * 4) >> 4);
+          if (kk == 0) mma_ts_g<C>(d_q, a_ds, bkt + o, id_q, s > 0 ? 1u : 0u);
+          else mma_ts_acc_g<C>(d_q, a_ds + 8 * kk, bkt + o, id_q);
+        }
+        if (h == Cfg::NSUB - 1) mma_commit_g<C>(&bars.empty[ikt % NU]);
+      }
+      __syncwarp();
       return true;
     };
-    for (int c = 0; ok && c < total; ++c) {
-      const int slot = c % Cfg::NSLOT, st = c & 1;
-      const bool pass2 = c >= nk;
-      if (!warp_wait(&bars.kv_full[slot], (c / Cfg::NSLOT) & 1, abort, status, kSiteQmMma)) break;
-      if (c >= 2 && !warp_wait(&bars.s_free[st], ((c - 2) / 2) & 1, abort, status, kSiteQmMma))
-        break;
-      const uint64_t bk = desc0 + (uint64_t)((slot * Cfg::SLOT_BYTES) >> 4);
-      const uint64_t bv = bk + ((uint64_t)Cfg::TILE_BYTES >> 4);
-      const uint32_t d_s = tmem + Cfg::t_s(st), d_dp = tmem + Cfg::t_dp(st);
-      const uint32_t a_q = tmem + Cfg::T_Q, a_do = tmem + Cfg::T_DO;
+    for (int s = 0; ok && s < n_sub; ++s) {
+      const int st = s & 1, j = s / Cfg::NSUB, h = s % Cfg::NSUB;
+      const int ik = 2 * nk + 3 * j;
+      if (h == 0 && (!unit_wait(ik) || !unit_wait(ik + 1))) { ok = false; break; }
+      if (!stage_free(st)) { ok = false; break; }
+      const uint64_t off = (uint64_t)((h * Cfg::HALF2 * 128) >> 4);   // rows h*HALF2.. of each panel
       if (elect_one()) {
-        tc_fence_after();
-        mma_ts(d_s, a_q, bk, id_s, 0u);
-        mma_ts(d_dp, a_do, bv, id_s, 0u);
-#pragma unroll
-        for (int ks = 1; ks < D / 8; ++ks) {
-          const uint64_t off = desc_off(ks, Cfg::PANEL_BYTES);
-          mma_ts_acc(d_s, a_q + 8 * ks, bk + off, id_s);
-          mma_ts_acc(d_dp, a_do + 8 * ks, bv + off, id_s);
+        issue_sdp(tmem + Cfg::p2_stage(st), Cfg::BK2, id_s2, unit_desc(ik) + off, unit_desc(ik + 1) + off);
+        mma_commit_g<C>(&bars.s_full[st]);
+        if (h == Cfg::NSUB - 1) {
+          mma_commit_g<C>(&bars.empty[ik % NU]);
+          mma_commit_g<C>(&bars.empty[(ik + 1) % NU]);
         }
-        mma_commit(&bars.s_full[st]);
-        if (!pass2) release(slot);
       }
       __syncwarp();
-      if (pass2 && c > nk && !issue_dq(c - 1)) { ok = false; break; }
+      const int this_use = st ? use1++ : use0++;
+      if (s > 0 && !issue_dq(s - 1)) { ok = false; break; }
+      dq_use = this_use;
     }
-    if (ok) ok = issue_dq(total - 1);
-    if (elect_one()) mma_commit(&bars.dq_done);     // also drains every MMA issued above
+    if (ok && n_sub > 0) ok = issue_dq(n_sub - 1);
+    if (elect_one()) mma_commit_g<C>(&bars.dq_done);   // also drains every MMA issued above
     __syncwarp();
-  } else {
+    // no MMA of the group may still run when the CTAs leave
+    warp_wait<kCl>(&bars.dq_done, 0, abort, status, kSiteQmMma);
+  } else if (warp >= kFirstCompute) {
     // ---------------- compute: two warpgroups, one TMEM lane (= one row) per thread ----------------
-    // Warpgroup wg handles the chunks that use TMEM stage wg (c % 2 == wg), so
-    // two chunks are in flight at once; each keeps a partial row sum of P dP
-    // over its pass-1 chunks, and the two partials are added through shared
-    // memory before the first dS is formed.
+    // Warpgroup wg takes the chunks / sub-chunks of TMEM stage wg, so two are
+    // in flight at once; each keeps a partial row sum of P dP over its pass-1
+    // chunks, and the two partials are added through shared memory before the
+    // first dS is formed.
     const int wg = (warp - kFirstCompute) >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int qi = r / G, q = q0 + qi;
@@ -286,35 +368,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.qdo_ready);
+      if (lane == 0) arrive_issuer<C>(&bars.qdo_ready);
     }
     const float sl2 = sh.scale * kLog2e;
     const float lse2 = valid ? __ldg(LSE + (long long)q * H + h) * kLog2e : 0.f;
     const int segq = valid ? (int)__ldg(seg + q) : 0;
-    float Dpart = 0.f, Drow = 0.f;
-    bool have_D = false, ok = true;
-    auto combine_D = [&]() {
-      bars.dx[wg][r] = Dpart;
-      asm volatile("bar.sync 2, 256;" ::: "memory");
-      Drow = bars.dx[0][r] + bars.dx[1][r];
-      have_D = true;
-    };
-    const uint32_t ts = tl + Cfg::t_s(wg), tdp = tl + Cfg::t_dp(wg);
-    for (int c = wg; c < total; c += 2) {
-      const bool pass2 = c >= nk;
-      if (pass2 && !have_D) combine_D();
-      const int k0 = (kc0 + c % nk) * Cfg::BK;
-      if (!mbar_wait(&bars.s_full[wg], (c / 2) & 1, abort, status, kSiteQmCompute)) { ok = false; break; }
-      tc_fence_after();
-      // every key of the chunk visible to this row: no per-element mask
-      const bool full = valid && k0 >= segq && k0 + Cfg::BK - 1 <= q;
+    float Dpart = 0.f;
+    bool ok = true;
+    int my_use = 0;
+    // ---- pass 1: D = rowsum(P dP) ----
+    {
+      const uint32_t ts = tl + Cfg::p1_stage(wg), tdp = ts + Cfg::BK1;
+      for (int c = wg; c < nk; c += 2) {
+        const int k0 = (kc0 + c) * Cfg::BK1;
+        if (!mbar_wait<kCl>(&bars.s_full[wg], my_use & 1, abort, status, kSiteQmCompute)) { ok = false; break; }
+        tc_fence_after();
+        // every key of the chunk visible to this row: no per-element mask
+        const bool full = valid && k0 >= segq && k0 + Cfg::BK1 - 1 <= q;
 #pragma unroll
-      for (int jb = 0; jb < Cfg::BK; jb += 32) {
-        float sv[32], dp[32];
-        tmem_ld32(ts + jb, sv);
-        tmem_ld32(tdp + jb, dp);
-        tmem_ld_wait();
-        if (!pass2) {
+        for (int jb = 0; jb < Cfg::BK1; jb += 32) {
+          float sv[32], dp[32];
+          tmem_ld32(ts + jb, sv);
+          tmem_ld32(tdp + jb, dp);
+          tmem_ld_wait();
           if (full) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) Dpart = fmaf(ex2(fmaf(sv[j], sl2, -lse2)), dp[j], Dpart);
@@ -326,7 +402,33 @@ __global__ void __launch_bounds__(kThreads, 1)
               Dpart = fmaf(vis ? ex2(fmaf(sv[j], sl2, -lse2)) : 0.f, dp[j], Dpart);
             }
           }
-        } else {
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_issuer<C>(&bars.s_free[wg]);
+        ++my_use;
+      }
+    }
+    // both warpgroups' partial sums (each has finished reading its pass-1 stage)
+    bars.dx[wg][r] = Dpart;
+    tc_fence_before();
+    asm volatile("bar.sync 2, 256;" ::: "memory");
+    const float Drow = bars.dx[0][r] + bars.dx[1][r];
+    // ---- pass 2: dS = scale P (dP - D) over S, for dQ += dS K ----
+    if (ok) {
+      const uint32_t ts = tl + Cfg::p2_stage(wg), tdp = ts + Cfg::BK2;
+      for (int s = wg; s < n_sub; s += 2) {
+        const int kc = (kc0 + s / Cfg::NSUB) * Cfg::BK1, hh = s % Cfg::NSUB;
+        if (!mbar_wait<kCl>(&bars.s_full[wg], my_use & 1, abort, status, kSiteQmCompute)) { ok = false; break; }
+        tc_fence_after();
+        // the sub-chunk's keys lie in [kc + key_of(hh, 0), kc + key_of(hh, BK2 - 1)]
+        const bool full = valid && kc + Cfg::key_of(hh, 0) >= segq && kc + Cfg::key_of(hh, Cfg::BK2 - 1) <= q;
+#pragma unroll
+        for (int jb = 0; jb < Cfg::BK2; jb += 32) {
+          float sv[32], dp[32];
+          tmem_ld32(ts + jb, sv);
+          tmem_ld32(tdp + jb, dp);
+          tmem_ld_wait();
           if (full) {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -334,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              const int key = k0 + jb + j;
+              const int key = kc + Cfg::key_of(hh, jb + j);
               const bool vis = valid && key >= segq && key <= q;
               const float pj = vis ? ex2(fmaf(sv[j], sl2, -lse2)) : 0.f;
               sv[j] = to_tf32(sh.scale * pj * (dp[j] - Drow));
@@ -342,15 +444,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st32(ts + jb, sv);
         }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_issuer<C>(&bars.s_free[wg]);
+        ++my_use;
       }
-      if (pass2) tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.s_free[wg]);
     }
-    if (!have_D) combine_D();   // a warpgroup without pass-2 chunks still joins the exchange
     // epilogue: dQ += accumulated tile (warpgroup wg: half wg of the columns), D to the workspace
-    if (ok && mbar_wait(&bars.dq_done, 0, abort, status, kSiteQmCompute)) {
+    if (ok && mbar_wait<kCl>(&bars.dq_done, 0, abort, status, kSiteQmCompute)) {
       tc_fence_after();
       for (int cc = wg * (D / 2); cc < (wg + 1) * (D / 2); cc += 16) {
         float v[16];
@@ -374,31 +476,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
-  if (C > 1) cluster_sync();   // no CTA leaves while a peer may still signal it
+  // both CTAs of a pair are done with every copy and MMA of the group before
+  // its TMEM is freed and before either leaves
+  if (C > 1) cluster_sync();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc_g<C>(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
 // Key-major kernel: dK and dV for 128 keys of one kv head, summed over the
 // query heads of its group (no atomics: the CTA owns these rows).
 //
-// Per (query, head) block of NQ rows (NQ/G queries x G heads):
+// Per (query, head) block of NQ columns (NQ/G queries x G heads):
 //   S^T  = K . Q^T        A = K (TMEM, loaded once),   B = Q block   (smem)
 //   dP^T = V . dO^T       A = V (smem, loaded once),   B = dO block  (smem)
 //   P^T, dS^T = scale P (dP - D) written back to TMEM over S^T / dP^T
 //   dV  += P^T . dO       A = P^T (TMEM),  B = dO^T block (smem, K-major copy)
 //   dK  += dS^T . Q       A = dS^T (TMEM), B = Q^T block  (smem, K-major copy)
-// The four streamed tiles each have a full/empty barrier pair, so the next
-// block's Q/dO load while dV/dK of this block run, and its Q^T/dO^T load
-// while its S^T/dP^T run. Blocks are visited from the end of the sequence
-// down to the tile's first query: CTAs that run at the same time then read
-// the same blocks at about the same time, so the per-group Q / dO / Q^T /
-// dO^T stream (larger than L2 at 16k tokens) is served mostly from L2.
+// Blocks alternate between two TMEM stages, and compute warpgroup w handles
+// the blocks of stage w, so block n's softmax runs while the tensor core does
+// S^T / dP^T of block n+1 and dV / dK of block n-1. Q / dO blocks go through
+// three shared-memory stages and Q^T / dO^T blocks through two: a block's
+// copies take ~3000 cycles to land while the tensor core is busy, and three
+// stages of the first-needed tiles cover that. Blocks are visited from the end of the sequence down to the
+// tile's first query: CTAs that run at the same time then read the same
+// blocks at about the same time, so the per-group Q / dO / Q^T / dO^T stream
+// (larger than L2 at 16k tokens) is served mostly from L2.
 // ---------------------------------------------------------------------------
 template <int D_>
 struct KmCfg {
   static constexpr int D = D_;
-  static constexpr int NQ = (D == 128) ? 64 : 128;        // (query, head) rows per block
+  static constexpr int NQ = (D == 128) ? 32 : 64;         // (query, head) columns per block
   static constexpr int V_PANEL_BYTES = 128 * 128;         // 128 keys x 32 floats
   static constexpr int V_BYTES = (D / 32) * V_PANEL_BYTES;
   static constexpr int BLK_PANEL_BYTES = NQ * 128;        // Q / dO block panel: NQ rows x 32 floats
@@ -406,25 +514,37 @@ struct KmCfg {
   static constexpr int T_PANEL_BYTES = D * 128;           // Q^T / dO^T panel: d rows x 32 columns
   static constexpr int T_PANELS = NQ / 32;
   static_assert(T_PANELS * T_PANEL_BYTES == BLK_BYTES, "transposed block size");
-  // shared memory: V | Q | dO | Q^T | dO^T
-  static constexpr int OFF_V = 0, OFF_Q = V_BYTES, OFF_DO = OFF_Q + BLK_BYTES,
-                       OFF_QT = OFF_DO + BLK_BYTES, OFF_DOT = OFF_QT + BLK_BYTES,
-                       END = OFF_DOT + BLK_BYTES;
-  static constexpr int SMEM_BYTES = (END + 1024 > 120 * 1024) ? END + 1024 : 120 * 1024;
-  // TMEM columns
-  static constexpr uint32_t T_K = 0, T_DK = D, T_DV = 2 * D, T_S = 3 * D, T_DP = 3 * D + NQ;
-  static_assert(3 * D + 2 * NQ <= 512, "TMEM budget");
+  static_assert(BLK_PANEL_BYTES % 1024 == 0 && T_PANEL_BYTES % 1024 == 0,
+                "panels must keep 1 KB swizzle alignment");
+  // shared memory: V | Q dO stages 0-2 | Q^T dO^T stages 0-1. The kernel
+  // needs the dynamic shared memory 1 KB aligned (it checks and reports an
+  // error otherwise) and takes no slack: at d = 128 the layout is 224 KB.
+  static constexpr int NSQ = 3, NST = 2;
+  static constexpr int OFF_V = 0, OFF_QDO = V_BYTES, OFF_T = OFF_QDO + NSQ * 2 * BLK_BYTES;
+  static constexpr int off_q(int b) { return OFF_QDO + b * 2 * BLK_BYTES; }
+  static constexpr int off_do(int b) { return OFF_QDO + b * 2 * BLK_BYTES + BLK_BYTES; }
+  static constexpr int off_qt(int b) { return OFF_T + b * 2 * BLK_BYTES; }
+  static constexpr int off_dot(int b) { return OFF_T + b * 2 * BLK_BYTES + BLK_BYTES; }
+  static constexpr int END = OFF_T + NST * 2 * BLK_BYTES;
+  static constexpr int SMEM_BYTES = (END > 120 * 1024) ? END : 120 * 1024;
+  static_assert(SMEM_BYTES <= 224 * 1024, "shared memory budget (with the static barriers)");
+  // TMEM columns: K | dK | dV | stage 0: S^T dP^T | stage 1: S^T dP^T
+  static constexpr uint32_t T_K = 0, T_DK = D, T_DV = 2 * D;
+  static constexpr uint32_t t_s(int b) { return 3 * D + b * 2 * NQ; }
+  static constexpr uint32_t t_dp(int b) { return 3 * D + b * 2 * NQ + NQ; }
+  static_assert(3 * D + 4 * NQ <= 512, "TMEM budget");
 };
 
 struct KmBarriers {
   uint64_t v_full, k_ready;
-  uint64_t full[4], empty[4];     // Q, dO, Q^T, dO^T blocks
-  uint64_t s_full, p_ready, acc_done;
+  uint64_t qdo_full[3], qdo_empty[3];     // Q, dO blocks of each stage
+  uint64_t t_full[2], t_empty[2];         // Q^T, dO^T blocks of each stage
+  uint64_t s_full[2], p_ready[2], acc_done;
   uint32_t tmem_base;
   int abort;
 };
 
-template <int D, int C>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_key_major(const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapQ,
                  const __grid_constant__ CUtensorMap mapDO, const __grid_constant__ CUtensorMap mapQt,
@@ -434,31 +554,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const uint32_t* __restrict__ blk_maxseg, float* __restrict__ dK,
                  float* __restrict__ dV, uint32_t* __restrict__ status, Shape sh) {
   using Cfg = KmCfg<D>;
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int NQ = Cfg::NQ;
+  extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ KmBarriers bars;
-  __shared__ float4 meta[2][Cfg::NQ];     // per block column: (lse*log2e, D, query, seg)
+  __shared__ float4 meta[2][2][NQ];       // [warpgroup][parity] per column: (lse*log2e, D, query, seg)
+  if ((smem_u32(smem) & 1023u) != 0) {    // the layout has no alignment slack
+    if (threadIdx.x == 0) atomicOr(status, 0x80000000u | kSiteKmLayout);
+    return;
+  }
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int G = sh.G, QB = Cfg::NQ / G;   // queries per block
+  const int G = sh.G, QB = NQ / G;        // queries per block
   const int S = sh.S, H = sh.H;
   const int k0 = blockIdx.x * 128, g = blockIdx.y;
-  const uint32_t rank = (C > 1) ? cluster_ctarank() : 0u;
-  const uint16_t all_ctas = (uint16_t)((1u << C) - 1u);
-  // all CTAs of a cluster (adjacent key tiles) walk the union of their blocks
-  const int k0_first = ((int)blockIdx.x - (int)rank) * 128;
-  const int k_hi = min(k0_first + 128 * C, S) - 1;
-  const int qb0 = k0_first / QB, nqb = (S + QB - 1) / QB;
+  const int k_hi = min(k0 + 128, S) - 1;
+  const int qb0 = k0 / QB, nqb = (S + QB - 1) / QB;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.v_full, 1);
     mbar_init(&bars.k_ready, kComputeWarps);
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&bars.full[i], 1);
-      mbar_init(&bars.empty[i], C);       // every CTA of the cluster releases a tile
+    for (int b = 0; b < Cfg::NSQ; ++b) {
+      mbar_init(&bars.qdo_full[b], 1);     // producer warp 0 arms both tiles
+      mbar_init(&bars.qdo_empty[b], 1);
     }
-    mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.p_ready, kComputeWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars.t_full[b], 1);       // producer warp 1 arms both tiles
+      mbar_init(&bars.t_empty[b], 1);
+      mbar_init(&bars.s_full[b], 1);
+      mbar_init(&bars.p_ready[b], kComputeWarps / 2);  // the stage's warpgroup
+    }
     mbar_init(&bars.acc_done, 1);
     bars.abort = 0;
     fence_barrier_init();
@@ -470,124 +593,126 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (C > 1) cluster_sync();   // peers' barriers are initialised before any multicast
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort = &bars.abort;
   auto visible = [&](int qb) { return __ldg(blk_minseg + qb) <= (unsigned)k_hi; };
 
   if (warp < kProducerWarps) {
-    // ---------------- TMA producers: warp 0 loads Q and Q^T, warp 1 dO, dO^T and V ----------------
+    // ---------------- TMA producers: warp 0 loads Q and dO, warp 1 Q^T, dO^T and V ----------------
+    // Each warp waits only for its own tiles' release: Q / dO of stage b are
+    // free once S^T / dP^T of block n-2 ran, Q^T / dO^T once its dV / dK ran.
     const int pw = warp;
-    const CUtensorMap* maps[4] = {&mapQ, &mapDO, &mapQt, &mapDOt};
     if (elect_one()) {
-      tma_prefetch_desc(maps[pw]);
-      tma_prefetch_desc(maps[pw + 2]);
-      if (pw == 1) {
+      if (pw == 0) {
+        tma_prefetch_desc(&mapQ);
+        tma_prefetch_desc(&mapDO);
+      } else {
+        tma_prefetch_desc(&mapQt);
+        tma_prefetch_desc(&mapDOt);
         tma_prefetch_desc(&mapV);
         mbar_arrive_expect_tx(&bars.v_full, Cfg::V_BYTES);
         tma_load_3d(smem + Cfg::OFF_V, &mapV, 0, k0, g * (D / 32), &bars.v_full);
       }
     }
     __syncwarp();
-    const int offs[4] = {Cfg::OFF_Q, Cfg::OFF_DO, Cfg::OFF_QT, Cfg::OFF_DOT};
+    uint64_t* full = pw == 0 ? bars.qdo_full : bars.t_full;
+    uint64_t* empty = pw == 0 ? bars.qdo_empty : bars.t_empty;
+    const int ns = pw == 0 ? Cfg::NSQ : Cfg::NST;      // this warp's stages
     int n = 0;
-    bool ok = true;
-    for (int qb = nqb - 1; ok && qb >= qb0; --qb) {
+    for (int qb = nqb - 1; qb >= qb0; --qb) {
       if (!visible(qb)) continue;
+      const int b = n % ns;
       const int q0 = qb * QB;
-      // one box per tile; tile t is loaded by cluster rank t % C into every CTA
-      for (int t = pw; t < 4; t += 2) {
-        if (n > 0 && !warp_wait(&bars.empty[t], (n - 1) & 1, abort, status, kSiteKmProducer)) {
-          ok = false;
-          break;
+      if (n >= ns && !warp_wait(&empty[b], ((n / ns) - 1) & 1, abort, status, kSiteKmProducer)) break;
+      if (elect_one()) {
+        mbar_arrive_expect_tx(&full[b], 2 * Cfg::BLK_BYTES);
+        if (pw == 0) {   // 4-D boxes (32 dims, G heads, QB queries, d/32 panels)
+          tma_load_4d(smem + Cfg::off_q(b), &mapQ, 0, g * G, q0, 0, &full[b]);
+          tma_load_4d(smem + Cfg::off_do(b), &mapDO, 0, g * G, q0, 0, &full[b]);
+        } else {         // d rows x NQ (query, head) columns, in 32-column panels
+          tma_load_3d(smem + Cfg::off_qt(b), &mapQt, 0, g * D, (q0 * G) / 32, &full[b]);
+          tma_load_3d(smem + Cfg::off_dot(b), &mapDOt, 0, g * D, (q0 * G) / 32, &full[b]);
         }
-        if (elect_one()) {
-          mbar_arrive_expect_tx(&bars.full[t], Cfg::BLK_BYTES);
-          if (C == 1 || t % C == (int)rank) {
-            unsigned char* dst = smem + offs[t];
-            if (t < 2) {          // Q / dO block: 4-D box (32 dims, G heads, QB queries, d/32 panels)
-              if (C == 1) tma_load_4d(dst, maps[t], 0, g * G, q0, 0, &bars.full[t]);
-              else tma_load_4d_mc(dst, maps[t], 0, g * G, q0, 0, &bars.full[t], all_ctas);
-            } else {              // Q^T / dO^T block: d rows x NQ (query, head) columns, in panels
-              if (C == 1) tma_load_3d(dst, maps[t], 0, g * D, (q0 * G) / 32, &bars.full[t]);
-              else tma_load_3d_mc(dst, maps[t], 0, g * D, (q0 * G) / 32, &bars.full[t], all_ctas);
-            }
-          }
-        }
-        __syncwarp();
       }
+      __syncwarp();
       ++n;
     }
     // leave only once every load this warp issued has landed
     if (pw == 1) warp_wait(&bars.v_full, 0, abort, status, kSiteKmProducer);
-    if (n > 0)
-      for (int t = pw; t < 4; t += 2) warp_wait(&bars.full[t], (n - 1) & 1, abort, status, kSiteKmProducer);
+    for (int m = max(0, n - ns); m < n; ++m)
+      warp_wait(&full[m % ns], (m / ns) & 1, abort, status, kSiteKmProducer);
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer (warp-converged, elected issue) ----------------
-    constexpr uint32_t id_s = idesc_tf32(128, Cfg::NQ, false, false);
+    constexpr uint32_t id_s = idesc_tf32(128, NQ, false, false);
     constexpr uint32_t id_g = idesc_tf32(128, D, false, false);
     bool ok = warp_wait(&bars.v_full, 0, abort, status, kSiteKmMma) &&
               warp_wait(&bars.k_ready, 0, abort, status, kSiteKmMma);
-    auto release = [&](int t) {     // tile t is free once every CTA's MMAs read it
-      if (C == 1) mma_commit(&bars.empty[t]);
-      else mma_commit_mc(&bars.empty[t], all_ctas);
-    };
     const uint64_t desc0 = sdesc(smem_u32(smem), 16, 1024);
-    const uint64_t av = desc0 + (uint64_t)(Cfg::OFF_V >> 4), bq = desc0 + (uint64_t)(Cfg::OFF_Q >> 4),
-                   bdo = desc0 + (uint64_t)(Cfg::OFF_DO >> 4),
-                   bqt = desc0 + (uint64_t)(Cfg::OFF_QT >> 4),
-                   bdot = desc0 + (uint64_t)(Cfg::OFF_DOT >> 4);
+    const uint64_t av = desc0 + (uint64_t)(Cfg::OFF_V >> 4);
+    // dV += P^T dO, dK += dS^T Q for block m (stage m & 1)
+    auto grad_mma = [&](int m) -> bool {
+      const int b = m & 1;
+      const uint32_t ph = (m >> 1) & 1;
+      if (!warp_wait(&bars.p_ready[b], ph, abort, status, kSiteKmMma) ||
+          !warp_wait(&bars.t_full[b], ph, abort, status, kSiteKmMma))
+        return false;
+      const uint64_t bqt = desc0 + (uint64_t)(Cfg::off_qt(b) >> 4);
+      const uint64_t bdot = desc0 + (uint64_t)(Cfg::off_dot(b) >> 4);
+      const uint32_t a_p = tmem + Cfg::t_s(b), a_ds = tmem + Cfg::t_dp(b);
+      const uint32_t acc0 = (m > 0) ? 1u : 0u;
+      if (elect_one()) {
+        tc_fence_after();
+        mma_ts(tmem + Cfg::T_DV, a_p, bdot, id_g, acc0);
+        mma_ts(tmem + Cfg::T_DK, a_ds, bqt, id_g, acc0);
+#pragma unroll
+        for (int kk = 1; kk < NQ / 8; ++kk) {
+          const uint64_t ot = desc_off(kk, Cfg::T_PANEL_BYTES);
+          mma_ts_acc(tmem + Cfg::T_DV, a_p + 8 * kk, bdot + ot, id_g);
+          mma_ts_acc(tmem + Cfg::T_DK, a_ds + 8 * kk, bqt + ot, id_g);
+        }
+        mma_commit(&bars.t_empty[b]);
+      }
+      __syncwarp();
+      return true;
+    };
     int n = 0;
     for (int qb = nqb - 1; ok && qb >= qb0; --qb) {
       if (!visible(qb)) continue;
-      const uint32_t par = n & 1;
-      if (!warp_wait(&bars.full[0], par, abort, status, kSiteKmMma) ||
-          !warp_wait(&bars.full[1], par, abort, status, kSiteKmMma)) { ok = false; break; }
+      const int b = n & 1, bs = n % Cfg::NSQ;
+      if (!warp_wait(&bars.qdo_full[bs], (n / Cfg::NSQ) & 1, abort, status, kSiteKmMma)) { ok = false; break; }
+      // TMEM stage b was last read by dV / dK of block n-2, issued earlier
+      // (MMAs run in issue order) after its warpgroup released it
+      const uint64_t bq = desc0 + (uint64_t)(Cfg::off_q(bs) >> 4);
+      const uint64_t bdo = desc0 + (uint64_t)(Cfg::off_do(bs) >> 4);
       if (elect_one()) {
         tc_fence_after();
-        mma_ts(tmem + Cfg::T_S, tmem + Cfg::T_K, bq, id_s, 0u);
-        mma_ss(tmem + Cfg::T_DP, av, bdo, id_s, 0u);
+        mma_ts(tmem + Cfg::t_s(b), tmem + Cfg::T_K, bq, id_s, 0u);
+        mma_ss(tmem + Cfg::t_dp(b), av, bdo, id_s, 0u);
 #pragma unroll
         for (int ks = 1; ks < D / 8; ++ks) {
           const uint64_t ob = desc_off(ks, Cfg::BLK_PANEL_BYTES);
-          mma_ts_acc(tmem + Cfg::T_S, tmem + Cfg::T_K + 8 * ks, bq + ob, id_s);
-          mma_ss_acc(tmem + Cfg::T_DP, av + desc_off(ks, Cfg::V_PANEL_BYTES), bdo + ob, id_s);
+          mma_ts_acc(tmem + Cfg::t_s(b), tmem + Cfg::T_K + 8 * ks, bq + ob, id_s);
+          mma_ss_acc(tmem + Cfg::t_dp(b), av + desc_off(ks, Cfg::V_PANEL_BYTES), bdo + ob, id_s);
         }
-        mma_commit(&bars.s_full);
-        release(0);
-        release(1);
+        mma_commit(&bars.s_full[b]);
+        mma_commit(&bars.qdo_empty[bs]);
       }
       __syncwarp();
-      if (!warp_wait(&bars.p_ready, par, abort, status, kSiteKmMma) ||
-          !warp_wait(&bars.full[2], par, abort, status, kSiteKmMma) ||
-          !warp_wait(&bars.full[3], par, abort, status, kSiteKmMma)) { ok = false; break; }
-      const uint32_t acc0 = (n > 0) ? 1u : 0u;
-      if (elect_one()) {
-        tc_fence_after();
-        mma_ts(tmem + Cfg::T_DV, tmem + Cfg::T_S, bdot, id_g, acc0);
-        mma_ts(tmem + Cfg::T_DK, tmem + Cfg::T_DP, bqt, id_g, acc0);
-#pragma unroll
-        for (int kk = 1; kk < Cfg::NQ / 8; ++kk) {
-          const uint64_t ot = desc_off(kk, Cfg::T_PANEL_BYTES);
-          mma_ts_acc(tmem + Cfg::T_DV, tmem + Cfg::T_S + 8 * kk, bdot + ot, id_g);
-          mma_ts_acc(tmem + Cfg::T_DK, tmem + Cfg::T_DP + 8 * kk, bqt + ot, id_g);
-        }
-        release(2);
-        release(3);
-      }
-      __syncwarp();
+      if (n >= 1 && !grad_mma(n - 1)) { ok = false; break; }
       ++n;
     }
-    if (elect_one()) mma_commit(&bars.acc_done);
+    if (ok && n >= 1) ok = grad_mma(n - 1);
+    if (elect_one()) mma_commit(&bars.acc_done);   // also drains every MMA issued above
     __syncwarp();
   } else {
-    // ---------------- compute: thread = key (TMEM lane); warpgroup wg owns half the columns ----------------
+    // ---------------- compute: thread = key (TMEM lane); warpgroup wg takes the blocks of stage wg ----------------
     const int wg = (warp - kFirstCompute) >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int key = k0 + r;
     const uint32_t tl = lane_base(tmem, warp);
-    const int ct = threadIdx.x - 32 * kFirstCompute;       // 0..255 among compute threads
+    const int wt = threadIdx.x - 32 * kFirstCompute - 128 * wg;   // 0..127 within the warpgroup
     {
+      // K rows into TMEM (A of S^T), rounded to TF32; warpgroup wg: half wg of the columns
       float v[16];
       const float* krow = K + (long long)key * sh.Hk * D + (long long)g * D;
       for (int cc = wg * (D / 2); cc < (wg + 1) * (D / 2); cc += 16) {   // D/2 >= 16
@@ -605,38 +730,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars.k_ready);
     }
     const float sl2 = sh.scale * kLog2e;
-    constexpr int HALF = Cfg::NQ / 2;
-    const int cbase = wg * HALF;
-    int n = 0;
+    const uint32_t ts = tl + Cfg::t_s(wg), tdp = tl + Cfg::t_dp(wg);
+    int n = 0, mine = 0;
     bool ok = true;
     for (int qb = nqb - 1; qb >= qb0; --qb) {
       if (!visible(qb)) continue;
-      // column metadata of this block (double-buffered; one named barrier per block)
-      if (ct < Cfg::NQ) {
-        const int q = qb * QB + ct / G, h = g * G + ct % G;
+      if ((n++ & 1) != wg) continue;
+      const int par = mine & 1;
+      // column metadata of this block (double-buffered per warpgroup; one named barrier per block)
+      if (wt < NQ) {
+        const int q = qb * QB + wt / G, h = g * G + wt % G;
         float4 m = make_float4(0.f, 0.f, __int_as_float(-1), __int_as_float(0x7fffffff));
         if (q < S)
           m = make_float4(__ldg(LSE + (long long)q * H + h) * kLog2e, Dws[(long long)q * H + h],
                           __int_as_float(q), __int_as_float((int)__ldg(seg + q)));
-        meta[n & 1][ct] = m;
+        meta[wg][par][wt] = m;
       }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (!mbar_wait(&bars.s_full, n & 1, abort, status, kSiteKmCompute)) { ok = false; break; }
+      asm volatile("bar.sync %0, 128;" ::"r"(1 + wg) : "memory");
+      if (!mbar_wait(&bars.s_full[wg], mine & 1, abort, status, kSiteKmCompute)) { ok = false; break; }
       tc_fence_after();
       // every (key, column) of the block visible: key <= first query and >= every seg
       const int q_first = qb * QB;
       const bool full = key <= q_first && key >= (int)__ldg(blk_maxseg + qb) &&
                         q_first + QB - 1 < S;
+      const float4* mt = meta[wg][par];
 #pragma unroll
-      for (int cb = 0; cb < HALF; cb += 32) {
+      for (int cb = 0; cb < NQ; cb += 32) {
         float sv[32], dp[32];
-        tmem_ld32(tl + Cfg::T_S + cbase + cb, sv);
-        tmem_ld32(tl + Cfg::T_DP + cbase + cb, dp);
+        tmem_ld32(ts + cb, sv);
+        tmem_ld32(tdp + cb, dp);
         tmem_ld_wait();
         if (full) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float4 m = meta[n & 1][cbase + cb + j];
+            const float4 m = mt[cb + j];
             const float pj = ex2(fmaf(sv[j], sl2, -m.x));
             sv[j] = to_tf32(pj);
             dp[j] = to_tf32(sh.scale * pj * (dp[j] - m.y));
@@ -644,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float4 m = meta[n & 1][cbase + cb + j];
+            const float4 m = mt[cb + j];
             const int q = __float_as_int(m.z), sq = __float_as_int(m.w);
             const bool vis = key <= q && key >= sq;        // q = -1 for padding columns
             const float pj = vis ? ex2(fmaf(sv[j], sl2, -m.x)) : 0.f;
@@ -652,14 +779,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             dp[j] = to_tf32(sh.scale * pj * (dp[j] - m.y));
           }
         }
-        tmem_st32(tl + Cfg::T_S + cbase + cb, sv);
-        tmem_st32(tl + Cfg::T_DP + cbase + cb, dp);
+        tmem_st32(ts + cb, sv);
+        tmem_st32(tdp + cb, dp);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.p_ready);
-      ++n;
+      if (lane == 0) mbar_arrive(&bars.p_ready[wg]);
+      ++mine;
     }
     // epilogue: warpgroup 0 adds dK, warpgroup 1 adds dV (owned rows)
     if (ok && mbar_wait(&bars.acc_done, 0, abort, status, kSiteKmCompute)) {
@@ -689,7 +816,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
-  if (C > 1) cluster_sync();   // no CTA leaves while a peer may still signal it
 }
 
 // ---------------------------------------------------------------------------
@@ -811,56 +937,29 @@ gqa_status launch_clustered(void (*kern)(KArgs...), dim3 grid, int cluster, int 
   return check_launch(what);
 }
 
-// Cluster size for the streamed-operand multicast (1, 2 or 4; default 1:
-// measured on the 16k workload, 2 and 4 gave no gain). GQA_TC_CLUSTER
-// overrides it (tuning).
-int cluster_size() {
-  static int c = [] {
-    const char* e = getenv("GQA_TC_CLUSTER");
-    const int v = e ? atoi(e) : 1;
-    return (v == 1 || v == 2 || v == 4) ? v : 1;
-  }();
-  return c;
-}
-
-template <int D, int C>
-gqa_status km_launch_c(const CUtensorMap& mv, const CUtensorMap& mq, const CUtensorMap& mdo,
-                       const CUtensorMap& mqt, const CUtensorMap& mdot, const float* K,
-                       const float* LSE, const float* Dws, const uint32_t* seg,
-                       const uint32_t* blk_minseg, const uint32_t* blk_maxseg, float* dK,
-                       float* dV, uint32_t* status, const Shape& sh, cudaStream_t st) {
-  using Cfg = KmCfg<D>;
-  if (cudaFuncSetAttribute(tc_key_major<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg::SMEM_BYTES) != cudaSuccess)
-    return check_launch("key-major smem attribute");
-  const int n_tiles = (sh.S + 127) / 128;
-  dim3 grid((n_tiles + C - 1) / C * C, sh.Hk);
-  return launch_clustered(tc_key_major<D, C>, grid, C, Cfg::SMEM_BYTES, st, "tensor-core key-major",
-                          mv, mq, mdo, mqt, mdot, K, LSE, Dws, seg, blk_minseg, blk_maxseg, dK, dV,
-                          status, sh);
-}
-
 template <int D>
 gqa_status km_launch(const float* Q, const float* K, const float* V, const float* dO,
                      const float* LSE, const uint32_t* seg, float* dK, float* dV, const float* Qt,
                      const float* dOt, long long ld_qt, const float* Dws, const uint32_t* blk_minseg,
                      const uint32_t* blk_maxseg, uint32_t* status, const Shape& sh,
                      cudaStream_t st) {
-  using C = KmCfg<D>;
-  const int QB = C::NQ / sh.G;
+  using Cfg = KmCfg<D>;
+  const int QB = Cfg::NQ / sh.G;
   CUtensorMap mv, mq, mdo, mqt, mdot;
   gqa_status r;
   const long long kv_panels = (long long)sh.Hk * D / 32;
   if ((r = map_panels(&mv, V, (long long)sh.Hk * D, sh.S, kv_panels, 128, D / 32)) != GQA_OK) return r;
   if ((r = map_heads(&mq, Q, D, sh.H, sh.S, sh.G, QB)) != GQA_OK) return r;
   if ((r = map_heads(&mdo, dO, D, sh.H, sh.S, sh.G, QB)) != GQA_OK) return r;
-  if ((r = map_panels(&mqt, Qt, ld_qt, (long long)sh.Hk * D, ld_qt / 32, D, C::T_PANELS)) != GQA_OK) return r;
-  if ((r = map_panels(&mdot, dOt, ld_qt, (long long)sh.Hk * D, ld_qt / 32, D, C::T_PANELS)) != GQA_OK) return r;
-  switch (cluster_size()) {
-    case 1: return km_launch_c<D, 1>(mv, mq, mdo, mqt, mdot, K, LSE, Dws, seg, blk_minseg, blk_maxseg, dK, dV, status, sh, st);
-    case 4: return km_launch_c<D, 4>(mv, mq, mdo, mqt, mdot, K, LSE, Dws, seg, blk_minseg, blk_maxseg, dK, dV, status, sh, st);
-    default: return km_launch_c<D, 2>(mv, mq, mdo, mqt, mdot, K, LSE, Dws, seg, blk_minseg, blk_maxseg, dK, dV, status, sh, st);
-  }
+  if ((r = map_panels(&mqt, Qt, ld_qt, (long long)sh.Hk * D, ld_qt / 32, D, Cfg::T_PANELS)) != GQA_OK) return r;
+  if ((r = map_panels(&mdot, dOt, ld_qt, (long long)sh.Hk * D, ld_qt / 32, D, Cfg::T_PANELS)) != GQA_OK) return r;
+  if (cudaFuncSetAttribute(tc_key_major<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg::SMEM_BYTES) != cudaSuccess)
+    return check_launch("key-major smem attribute");
+  dim3 grid((sh.S + 127) / 128, sh.Hk);
+  return launch_clustered(tc_key_major<D>, grid, 1, Cfg::SMEM_BYTES, st, "tensor-core key-major",
+                          mv, mq, mdo, mqt, mdot, K, LSE, Dws, seg, blk_minseg, blk_maxseg, dK, dV,
+                          status, sh);
 }
 
 gqa_status transpose_launch(const float* X, float* Xt, int S, int Hk, int Gx, int d, long long ld,
@@ -872,11 +971,31 @@ gqa_status transpose_launch(const float* X, float* Xt, int S, int Hk, int Gx, in
   return check_launch("group transpose");
 }
 
+// CTA group of the query-major kernel: 1 (one SM per slab) by default;
+// GQA_TC_CTA_GROUP=2 runs it on SM pairs (cta_group::2). The pair halves the
+// shared-memory traffic per SM but measured slower on this part: its
+// cross-SM handshakes (forwarded copy completions, the dS hand-back) add
+// ~800 cycles per step that two TMEM stages cannot hide. Read once per process.
+int cta_group() {
+  static int c = [] {
+    const char* e = getenv("GQA_TC_CTA_GROUP");
+    return (e != nullptr && atoi(e) == 2) ? 2 : 1;
+  }();
+  return c;
+}
+
 template <int D, int C>
-gqa_status qm_launch_c(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mkt,
-                       const float* Q, const float* dO, const float* LSE, const uint32_t* seg,
-                       float* dQ, float* Dws, uint32_t* status, const Shape& sh, cudaStream_t st) {
-  using Cfg = QmCfg<D>;
+gqa_status qm_launch_c(const float* Q, const float* K, const float* V, const float* dO,
+                       const float* LSE, const uint32_t* seg, float* dQ, const float* Kt,
+                       long long ld_kt, float* Dws, uint32_t* status, const Shape& sh,
+                       cudaStream_t st) {
+  using Cfg = QmCfg<D, C>;
+  CUtensorMap mk, mv, mkt;
+  gqa_status r;
+  const long long kv_panels = (long long)sh.Hk * D / 32;
+  if ((r = map_panels(&mk, K, (long long)sh.Hk * D, sh.S, kv_panels, Cfg::HALF1, D / 32)) != GQA_OK) return r;
+  if ((r = map_panels(&mv, V, (long long)sh.Hk * D, sh.S, kv_panels, Cfg::HALF1, D / 32)) != GQA_OK) return r;
+  if ((r = map_panels(&mkt, Kt, ld_kt, (long long)sh.Hk * D, ld_kt / 32, Cfg::KT_ROWS, Cfg::KT_PANELS)) != GQA_OK) return r;
   if (cudaFuncSetAttribute(tc_query_major<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess)
     return check_launch("query-major smem attribute");
@@ -893,18 +1012,9 @@ gqa_status qm_launch(const float* Q, const float* K, const float* V, const float
                      const float* LSE, const uint32_t* seg, float* dQ, const float* Kt,
                      long long ld_kt, float* Dws, uint32_t* status, const Shape& sh,
                      cudaStream_t st) {
-  using C = QmCfg<D>;
-  CUtensorMap mk, mv, mkt;
-  gqa_status r;
-  const long long kv_panels = (long long)sh.Hk * D / 32;
-  if ((r = map_panels(&mk, K, (long long)sh.Hk * D, sh.S, kv_panels, C::BK, D / 32)) != GQA_OK) return r;
-  if ((r = map_panels(&mv, V, (long long)sh.Hk * D, sh.S, kv_panels, C::BK, D / 32)) != GQA_OK) return r;
-  if ((r = map_panels(&mkt, Kt, ld_kt, (long long)sh.Hk * D, ld_kt / 32, D, C::KT_PANELS)) != GQA_OK) return r;
-  switch (cluster_size()) {
-    case 1: return qm_launch_c<D, 1>(mk, mv, mkt, Q, dO, LSE, seg, dQ, Dws, status, sh, st);
-    case 4: return qm_launch_c<D, 4>(mk, mv, mkt, Q, dO, LSE, seg, dQ, Dws, status, sh, st);
-    default: return qm_launch_c<D, 2>(mk, mv, mkt, Q, dO, LSE, seg, dQ, Dws, status, sh, st);
-  }
+  if (cta_group() == 1)
+    return qm_launch_c<D, 1>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, status, sh, st);
+  return qm_launch_c<D, 2>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, status, sh, st);
 }
 
 }  // namespace
@@ -933,8 +1043,9 @@ TcWsLayout tc_ws_layout(int S, int H, int Hk, int d) {
 }
 
 bool tc_supported(const Shape& sh) {
-  // G must divide the 128-row slab and the key-major (query, head) block
-  const int nq = (sh.d == 128) ? 64 : 128;
+  // G must divide the query-major slab (128 rows) and the key-major block
+  // (NQ columns: 32 at d = 128, 64 below)
+  const int nq = (sh.d == 128) ? KmCfg<128>::NQ : KmCfg<64>::NQ;
   return (sh.d == 32 || sh.d == 64 || sh.d == 128) && sh.G >= 1 && sh.G <= nq &&
          (nq % sh.G) == 0;
 }
@@ -951,7 +1062,7 @@ gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* d
   float* dOt = reinterpret_cast<float*>(ws + T.dot_off);
   uint32_t* blk = reinterpret_cast<uint32_t*>(ws + T.blk_off);
   uint32_t* blk_max = reinterpret_cast<uint32_t*>(ws + T.blkmax_off);
-  const int QB = ((sh.d == 128) ? 64 : 128) / sh.G;
+  const int QB = ((sh.d == 128) ? KmCfg<128>::NQ : KmCfg<64>::NQ) / sh.G;
   gqa_status r;
   if ((r = tile_minseg(seg, sh.S, QB, blk, st, blk_max)) != GQA_OK) return r;
   if ((r = transpose_launch(K, Kt, sh.S, sh.Hk, 1, sh.d, T.ld_kt, st)) != GQA_OK) return r;

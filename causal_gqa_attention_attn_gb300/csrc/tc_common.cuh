@@ -59,6 +59,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same with acquire at cluster scope, for barriers that the other CTA of
+// a pair arrives on.
+__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 
 // Bounded wait. Gives up after ~kWaitCycles SM cycles (or as soon as another
 // thread of the CTA gave up: *abort != 0), records `site` in the global status
@@ -66,13 +78,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // comes near the bound (waits here are microseconds).
 constexpr long long kWaitCycles = 4000000000LL;
 
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status, uint32_t site,
                                           long long limit = kWaitCycles) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto poll = [&]() { return kCluster ? mbar_try_wait_cl(bar, parity) : mbar_try_wait(bar, parity); };
+  if (poll()) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll()) return true;
     if (*abort) return false;
     if (clock64() - t0 > limit) {
       *abort = 1;
@@ -83,9 +97,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // The same wait by every lane of a warp; the result is made warp-uniform.
+template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status, uint32_t site) {
-  const bool ok = mbar_wait(bar, parity, abort, status, site);
+  const bool ok = mbar_wait<kCluster>(bar, parity, abort, status, site);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -131,35 +146,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// Multicast forms: the tile lands at the same shared-memory offset in every
-// CTA of the cluster named in `mask`, and signals each one's mbarrier at the
-// barrier's offset. Used only for tiles in this GPU's own memory.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y,
-                                               uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, int x, int y,
-                                               int z, uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_4d_mc(void* dst, const CUtensorMap* map, int x, int y,
-                                               int z, int w, uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // Thread-block clusters
 // ---------------------------------------------------------------------------
@@ -174,6 +160,18 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile(
       "barrier.cluster.arrive.release.aligned;\n\t"
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// shared::cluster address of the variable at `p`'s offset in CTA `rank`
+__device__ __forceinline__ uint32_t mapa_u32(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+// Arrive (release at cluster scope) on the mbarrier at a shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_cl(uint32_t bar_cl) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cl)
+               : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -238,13 +236,84 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
           smem_u32(bar))
       : "memory");
 }
-// The same, arriving on the barrier at `bar`'s offset in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
+
+// ---------------------------------------------------------------------------
+// The same tcgen05 operations for a CTA group of CG = 1 (one SM) or CG = 2 (an
+// SM pair of a 2-CTA cluster; a kernel uses one group size for all of its
+// tcgen05 instructions). With CG = 2:
+//  - alloc / dealloc / relinquish run in one warp of each CTA of the pair and
+//    give both CTAs the same TMEM columns;
+//  - an MMA is issued by one thread of the even CTA. M = 256: A rows 0-127
+//    come from the even CTA and 128-255 from the odd one (same TMEM columns
+//    or shared-memory offset in each), B rows [0, N/2) from the even CTA's
+//    shared memory and [N/2, N) from the odd CTA's (same offset), and each
+//    CTA's TMEM receives its 128 rows of D, all N columns;
+//  - a commit arrives on the barrier at the same offset in both CTAs.
+// (Checked on this part with a probe against an fp64 product: TS and SS
+// forms, N = 32, 64, 128.)
+// ---------------------------------------------------------------------------
+template <int CG>
+__device__ __forceinline__ void tmem_alloc_g(uint32_t* dst_smem, uint32_t ncols) {
+  if constexpr (CG == 1) {
+    tmem_alloc(dst_smem, ncols);
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+  }
+}
+template <int CG>
+__device__ __forceinline__ void tmem_relinquish_g() {
+  if constexpr (CG == 1) tmem_relinquish();
+  else asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+template <int CG>
+__device__ __forceinline__ void tmem_dealloc_g(uint32_t taddr, uint32_t ncols) {
+  if constexpr (CG == 1) {
+    tmem_dealloc(taddr, ncols);
+  } else {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  }
+}
+template <int CG>
+__device__ __forceinline__ void mma_ts_g(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  if constexpr (CG == 1) {
+    mma_ts(d_tmem, a_tmem, b_desc, idesc, accumulate);
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+template <int CG>
+__device__ __forceinline__ void mma_ts_acc_g(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc) {
+  if constexpr (CG == 1) {
+    mma_ts_acc(d_tmem, a_tmem, b_desc, idesc);
+  } else {
+    asm volatile("tcgen05.mma.cta_group::2.kind::tf32 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc)
+                 : "memory");
+  }
+}
+// Arrive on `bar` (CG = 1) or on the barrier at its offset in both CTAs of the
+// pair (CG = 2) once every MMA this thread issued so far has completed.
+template <int CG>
+__device__ __forceinline__ void mma_commit_g(uint64_t* bar) {
+  if constexpr (CG == 1) {
+    mma_commit(bar);
+  } else {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"((uint16_t)3)
+        : "memory");
+  }
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle, sm_100 descriptor version.

@@ -1,0 +1,48 @@
+"""The query-major kernel runs on SM pairs (cta_group::2, M = 256) by default;
+GQA_TC_CTA_GROUP=1 selects the one-SM-per-slab variant. The group size is read
+once per process, so the variant runs in a child process, against the oracle
+on edge shapes (ragged tails, documents, all head dims)."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+_SCRIPT = r"""
+import math, sys, numpy as np, torch
+sys.path.insert(0, {root!r})
+import oracle, workloads, causal_gqa_attention_attn_gb300 as ga
+rng = np.random.default_rng(11)
+for (S, H, Hk, d, docs) in ((777, 16, 4, 128, True), (1000, 8, 2, 64, False), (300, 8, 8, 32, True),
+                            (129, 32, 1, 128, False)):
+    seg = workloads.random_seg(S, rng) if docs else np.zeros(S, np.uint32)
+    f = lambda c: rng.standard_normal((S, c), dtype=np.float32)
+    Q, K, V, dO = f(H * d), f(Hk * d), f(Hk * d), f(H * d)
+    sc = 1 / math.sqrt(d)
+    _, lse = oracle.fwd(Q, K, V, seg, H, Hk, d, sc)
+    lse = lse.astype(np.float32)
+    ref = oracle.bwd(Q, K, V, dO, lse, seg, H, Hk, d, sc)
+    t = [torch.from_numpy(a).cuda() for a in (Q, K, V, dO, lse)]
+    out = [torch.zeros(S, n * d, device="cuda") for n in (H, Hk, Hk)]
+    ws = ga.attn_bwd(*t[:4], t[4], torch.from_numpy(seg.astype(np.int32)).cuda(), *out, H, Hk, d, sc)
+    ga.read_device_status(ws)
+    for g, r in zip(out, ref):
+        err = np.max(np.abs(g.cpu().numpy() - r)); mag = np.max(np.abs(r))
+        assert err <= 5e-3 * mag, (S, H, Hk, d, err, mag)
+print("ok")
+"""
+
+
+def test_single_sm_query_major_matches_oracle():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from causal_gqa_attention_attn_gb300 import build
+    build.build()
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, GQA_TC_CTA_GROUP="1")
+    p = subprocess.run([sys.executable, "-c", _SCRIPT.format(root=root)], env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert p.returncode == 0 and "ok" in p.stdout, p.stdout + p.stderr
