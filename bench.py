@@ -221,10 +221,16 @@ def run_gpu(args) -> dict | None:
     dV = torch.zeros(S, Hk * d, device=dev)
     ws = torch.empty(ga.workspace_bytes(S, H, Hk, d), dtype=torch.uint8, device=dev)
 
+    fused_rope = w.rope and args.path == "auto"
+
     def step():
         dQ.zero_()
         dK.zero_()
         dV.zero_()
+        if fused_rope:       # RoPE backward on dQ, dK fused into the kernels' final writes
+            ga.attn_bwd_rope(t["Q"], t["K"], t["V"], t["dO"], t["LSE"], t["seg"], dQ, dK, dV, H,
+                             Hk, d, sc, pos_offset=0, base=10000.0, workspace=ws)
+            return
         impl_fn(t["Q"], t["K"], t["V"], t["dO"], t["LSE"], t["seg"], dQ, dK, dV, H, Hk, d, sc,
                 workspace=ws)
         if w.rope:
@@ -314,7 +320,8 @@ def run_gpu(args) -> dict | None:
         "config": {"workload": w.name, "shape": w.describe, "seq_len": S, "n_heads": H,
                    "n_kv_heads": Hk, "head_dim": d, "n_pairs": pairs,
                    "counted_flop_per_step": flops,
-                   "step": "zero grads + attn_bwd" + (" + rope_bwd(dQ) + rope_bwd(dK)" if w.rope else ""),
+                   "step": ("zero grads + attn_bwd_rope (RoPE backward of dQ, dK fused)" if fused_rope else
+                            "zero grads + attn_bwd" + (" + rope_bwd(dQ) + rope_bwd(dK)" if w.rope else "")),
                    "l2": "inputs larger than L2 (129 MB)" if 4 * S * H * d > 129e6 else
                          "inputs smaller than L2: steps run back to back (warm L2)",
                    "path": stage},

@@ -50,6 +50,7 @@ def lib() -> ctypes.CDLL:
     bwd_args = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
     L.attn_bwd.argtypes = bwd_args
     L.attn_bwd_simt.argtypes = bwd_args
+    L.attn_bwd_rope.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, F, P, Z, P]
     L.attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P]
     L.attn_bwd_noalloc.restype = ctypes.c_int
     L.rope_bwd_inplace.argtypes = [P, I, I, I, I, F, P]
@@ -68,8 +69,8 @@ def lib() -> ctypes.CDLL:
     L.gqa_launch_count.restype = ctypes.c_ulonglong
     L.gqa_last_error.argtypes = []
     L.gqa_last_error.restype = ctypes.c_char_p
-    for name in ("attn_fwd_lse", "attn_bwd", "attn_bwd_simt", "rope_bwd_inplace",
-                 "attn_read_device_status"):
+    for name in ("attn_fwd_lse", "attn_bwd", "attn_bwd_simt", "attn_bwd_rope",
+                 "rope_bwd_inplace", "attn_read_device_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -152,6 +153,24 @@ def attn_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_dim, s
     workspace used (a uint8 device tensor; pass it back in to reuse it)."""
     return _bwd(lib().attn_bwd, Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads,
                 head_dim, scale, workspace, stream)
+
+
+def attn_bwd_rope(Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_dim, scale,
+                  pos_offset=0, base=10000.0, workspace=None, stream=None):
+    """:func:`attn_bwd` with the interleaved RoPE backward fused into the final
+    writes: dQ += R^T(attention dQ), dK += R^T(attention dK), dV += attention dV.
+    Returns the workspace used."""
+    torch = _torch()
+    S = Q.shape[0]
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(S, n_heads, n_kv_heads, head_dim),
+                                device=Q.device, dtype=torch.uint8)
+    _check(lib().attn_bwd_rope(
+        _f32(Q, "Q"), _f32(K, "K"), _f32(V, "V"), _f32(dO, "dO"), _f32(LSE, "LSE"), _seg(seg),
+        _f32(dQ, "dQ"), _f32(dK, "dK"), _f32(dV, "dV"), S, n_heads, n_kv_heads, head_dim,
+        float(scale), int(pos_offset), float(base), _ptr(workspace, "workspace", (torch.uint8,)),
+        workspace.numel(), _stream(stream)))
+    return workspace
 
 
 def attn_bwd_simt(Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_dim, scale,

@@ -140,27 +140,66 @@ gqa_status attn_bwd_simt(const float* Q, const float* K, const float* V, const f
   if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
     return check_launch("workspace header reset");
   Shape sh{seq_len, n_heads, n_kv_heads, head_dim, n_heads / n_kv_heads, scale};
-  return simt_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st);
+  return simt_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st, no_rope());
 }
+
+}  // extern "C"
+
+namespace gqa {
+// attn_bwd and attn_bwd_rope: tensor-core kernels where the shape allows.
+static gqa_status bwd_dispatch(const float* Q, const float* K, const float* V, const float* dO,
+                               const float* LSE, const uint32_t* seg, float* dQ, float* dK,
+                               float* dV, int seq_len, int n_heads, int n_kv_heads, int head_dim,
+                               float scale, void* workspace, size_t workspace_bytes, void* stream,
+                               const RopeParams& rope) {
+  gqa_status r = check_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, seq_len, n_heads, n_kv_heads,
+                           head_dim, scale, workspace, workspace_bytes);
+  if (r != GQA_OK || seq_len == 0) return r;
+  const Shape sh{seq_len, n_heads, n_kv_heads, head_dim, n_heads / n_kv_heads, scale};
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!tc_supported(sh)) {
+    if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
+      return check_launch("workspace header reset");
+    return simt_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st, rope);
+  }
+  const size_t need = tc_ws_layout(seq_len, n_heads, n_kv_heads, head_dim).total;
+  if (workspace_bytes < need)
+    return set_error(GQA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
+    return check_launch("workspace header reset");
+  return tc_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st, rope);
+}
+
+static gqa_status check_rope(int seq_len, int head_dim, int pos_offset, float base) {
+  if (pos_offset < 0) return set_error(GQA_ERR_INVALID_ARG, "pos_offset must be >= 0");
+  if (!(base > 0.f) || !isfinite(base)) return set_error(GQA_ERR_INVALID_ARG, "base must be > 0");
+  if ((long long)seq_len + pos_offset >= (1LL << 31))
+    return set_error(GQA_ERR_INVALID_ARG, "seq_len + pos_offset must be < 2^31");
+  (void)head_dim;
+  return GQA_OK;
+}
+}  // namespace gqa
+
+extern "C" {
 
 gqa_status attn_bwd(const float* Q, const float* K, const float* V, const float* dO,
                     const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
                     int seq_len, int n_heads, int n_kv_heads, int head_dim, float scale,
                     void* workspace, size_t workspace_bytes, void* stream) {
-  gqa_status r = check_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, seq_len, n_heads, n_kv_heads,
-                           head_dim, scale, workspace, workspace_bytes);
-  if (r != GQA_OK || seq_len == 0) return r;
-  const Shape sh{seq_len, n_heads, n_kv_heads, head_dim, n_heads / n_kv_heads, scale};
-  if (!tc_supported(sh))
-    return attn_bwd_simt(Q, K, V, dO, LSE, seg, dQ, dK, dV, seq_len, n_heads, n_kv_heads,
-                         head_dim, scale, workspace, workspace_bytes, stream);
-  const size_t need = tc_ws_layout(seq_len, n_heads, n_kv_heads, head_dim).total;
-  if (workspace_bytes < need)
-    return set_error(GQA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
-  cudaStream_t st = (cudaStream_t)stream;
-  if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
-    return check_launch("workspace header reset");
-  return tc_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st);
+  return bwd_dispatch(Q, K, V, dO, LSE, seg, dQ, dK, dV, seq_len, n_heads, n_kv_heads, head_dim,
+                      scale, workspace, workspace_bytes, stream, no_rope());
+}
+
+gqa_status attn_bwd_rope(const float* Q, const float* K, const float* V, const float* dO,
+                         const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
+                         int seq_len, int n_heads, int n_kv_heads, int head_dim, float scale,
+                         int pos_offset, float base, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  const gqa_status r = check_rope(seq_len, head_dim, pos_offset, base);
+  if (r != GQA_OK) return r;
+  return bwd_dispatch(Q, K, V, dO, LSE, seg, dQ, dK, dV, seq_len, n_heads, n_kv_heads, head_dim,
+                      scale, workspace, workspace_bytes, stream,
+                      make_rope(head_dim, pos_offset, base));
 }
 
 gqa_status rope_bwd_inplace(float* dX, int seq_len, int n_heads, int head_dim, int pos_offset,

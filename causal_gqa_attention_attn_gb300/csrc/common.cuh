@@ -6,6 +6,7 @@
 #include <stddef.h>
 
 #include "gqa_attn.h"   // include/ is on the include path (build.py)
+#include "rope_common.cuh"
 
 namespace gqa {
 
@@ -91,13 +92,12 @@ bool aligned16(const void* p);
 // SIMT (CUDA-core) kernels, simt_attn.cu
 gqa_status simt_fwd_lse(const float* Q, const float* K, const float* V, const uint32_t* seg,
                         float* O, float* LSE, const Shape& sh, cudaStream_t st);
+// With rope.on, the RoPE backward is applied to the attention gradients of Q
+// and K before they are added to dQ / dK (attn_bwd_rope).
 gqa_status simt_bwd(const float* Q, const float* K, const float* V, const float* dO,
                     const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
-                    const Shape& sh, char* ws, cudaStream_t st);
+                    const Shape& sh, char* ws, cudaStream_t st, const RopeParams& rope);
 
-gqa_status simt_bwd_key_major(const float* Q, const float* K, const float* V, const float* dO,
-                              const float* LSE, const uint32_t* seg, float* dK, float* dV,
-                              const Shape& sh, char* ws, cudaStream_t st);
 gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cudaStream_t st,
                        uint32_t* out_max = nullptr);
 
@@ -105,7 +105,7 @@ gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cuda
 bool tc_supported(const Shape& sh);
 gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* dO,
                   const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
-                  const Shape& sh, char* ws, cudaStream_t st);
+                  const Shape& sh, char* ws, cudaStream_t st, const RopeParams& rope);
 
 gqa_status wait_selftest(void* workspace, long long limit_cycles, cudaStream_t st);
 

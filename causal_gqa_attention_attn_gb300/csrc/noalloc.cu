@@ -89,5 +89,5 @@ extern "C" gqa_status attn_bwd_noalloc(const float* Q, const float* K, const flo
   if (cudaMemsetAsync(ws, 0, kWsHeader, st) != cudaSuccess)
     return check_launch("attn_bwd_noalloc scratch header reset");
   Shape sh{seq_len, n_heads, n_kv_heads, head_dim, n_heads / n_kv_heads, scale};
-  return simt_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)ws, st);
+  return simt_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)ws, st, no_rope());
 }

@@ -26,6 +26,17 @@
 namespace gqa {
 namespace {
 
+// RoPE backward on a gradient row held by the 16 threads of a half-warp:
+// column c = tx + 16n, so pair (2p, 2p+1) sits in lanes tx and tx ^ 1. Every
+// lane of the warp calls it (it shuffles).
+__device__ __forceinline__ void rope_pair_shfl(float& v, int c, long long tpos, int tx,
+                                               const RopeParams& rope) {
+  const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+  float x0 = (tx & 1) ? other : v, x1 = (tx & 1) ? v : other;
+  rope_rotate(x0, x1, tpos, c >> 1, rope);
+  v = (tx & 1) ? x1 : x0;
+}
+
 constexpr int BT = 64;          // tile rows / cols
 constexpr int NT = 256;         // threads per block
 constexpr int PS = BT + 1;      // row stride of 64x64 score tiles
@@ -226,7 +237,8 @@ template <int DP>
 __global__ void __launch_bounds__(NT) bwd_query_major(
     const float* __restrict__ Q, const float* __restrict__ K, const float* __restrict__ V,
     const float* __restrict__ dO, const float* __restrict__ LSE, const uint32_t* __restrict__ seg,
-    float* __restrict__ dQ, float* __restrict__ Dws, uint32_t* __restrict__ minseg64, Shape sh) {
+    float* __restrict__ dQ, float* __restrict__ Dws, uint32_t* __restrict__ minseg64, Shape sh,
+    const RopeParams rope) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   QmSmem<DP>& sm = *reinterpret_cast<QmSmem<DP>*>(smem_raw);
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
@@ -308,15 +320,13 @@ __global__ void __launch_bounds__(NT) bwd_query_major(
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    if (row[i] >= S) continue;
 #pragma unroll
     for (int n = 0; n < DP / 16; ++n) {
       const int c = tx + 16 * n;
-      if (c < d) {
-        float* p = dQ + (long long)row[i] * ldq + h * d + c;
-        const float v = acc[i][n];
-        *p += (v == v) ? v : 0.f;   // NaN guard on the final write, as the pages do
-      }
+      float v = acc[i][n];
+      v = (v == v) ? v : 0.f;   // NaN guard on the final write, as the pages do
+      if (rope.on) rope_pair_shfl(v, c, (long long)row[i] + rope.pos_offset, tx, rope);
+      if (row[i] < S && c < d) dQ[(long long)row[i] * ldq + h * d + c] += v;
     }
   }
 }
@@ -335,7 +345,7 @@ __global__ void __launch_bounds__(NT) bwd_key_major(
     const float* __restrict__ Q, const float* __restrict__ K, const float* __restrict__ V,
     const float* __restrict__ dO, const float* __restrict__ LSE, const uint32_t* __restrict__ seg,
     const float* __restrict__ Dws, const uint32_t* __restrict__ minseg64, float* __restrict__ dK,
-    float* __restrict__ dV, Shape sh) {
+    float* __restrict__ dV, Shape sh, const RopeParams rope) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   KmSmem<DP>& sm = *reinterpret_cast<KmSmem<DP>*>(smem_raw);
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
@@ -397,14 +407,16 @@ __global__ void __launch_bounds__(NT) bwd_key_major(
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int key = k0 + 4 * ty + i;
-    if (key >= S) continue;
 #pragma unroll
     for (int n = 0; n < DP / 16; ++n) {
       const int c = tx + 16 * n;
-      if (c < d) {
+      float a = dk[i][n];
+      const float b = dv[i][n];
+      a = (a == a) ? a : 0.f;
+      if (rope.on) rope_pair_shfl(a, c, (long long)key + rope.pos_offset, tx, rope);
+      if (key < S && c < d) {
         const long long o = (long long)key * ldk + g * d + c;
-        const float a = dk[i][n], b = dv[i][n];
-        dK[o] += (a == a) ? a : 0.f;
+        dK[o] += a;
         dV[o] += (b == b) ? b : 0.f;
       }
     }
@@ -430,7 +442,7 @@ gqa_status fwd_launch(const float* Q, const float* K, const float* V, const uint
 template <int DP>
 gqa_status bwd_launch(const float* Q, const float* K, const float* V, const float* dO,
                       const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
-                      const Shape& sh, char* ws, cudaStream_t st) {
+                      const Shape& sh, char* ws, cudaStream_t st, const RopeParams& rope) {
   const WsLayout L = ws_layout(sh.S, sh.H);
   float* Dws = reinterpret_cast<float*>(ws + L.d_off);
   uint32_t* minseg = reinterpret_cast<uint32_t*>(ws + L.minseg64);
@@ -439,11 +451,11 @@ gqa_status bwd_launch(const float* Q, const float* K, const float* V, const floa
   if (allow_smem(bwd_key_major<DP>, s2) != cudaSuccess) return check_launch("bwd smem attribute");
   const int nt = (sh.S + BT - 1) / BT;
   profile_before(st, "simt_bwd_query_major+key_major");
-  bwd_query_major<DP><<<dim3(nt, sh.H), NT, s1, st>>>(Q, K, V, dO, LSE, seg, dQ, Dws, minseg, sh);
+  bwd_query_major<DP><<<dim3(nt, sh.H), NT, s1, st>>>(Q, K, V, dO, LSE, seg, dQ, Dws, minseg, sh, rope);
   note_launch();
   gqa_status r = check_launch("simt backward (query-major)");
   if (r != GQA_OK) return r;
-  bwd_key_major<DP><<<dim3(nt, sh.Hk), NT, s2, st>>>(Q, K, V, dO, LSE, seg, Dws, minseg, dK, dV, sh);
+  bwd_key_major<DP><<<dim3(nt, sh.Hk), NT, s2, st>>>(Q, K, V, dO, LSE, seg, Dws, minseg, dK, dV, sh, rope);
   note_launch();
   profile_after(st);
   return check_launch("simt backward (key-major)");
@@ -474,21 +486,6 @@ __global__ void tile_minseg_kernel(const uint32_t* __restrict__ seg, int S, int 
   }
 }
 
-template <int DP>
-gqa_status key_major_launch(const float* Q, const float* K, const float* V, const float* dO,
-                            const float* LSE, const uint32_t* seg, float* dK, float* dV,
-                            const Shape& sh, char* ws, cudaStream_t st) {
-  const WsLayout L = ws_layout(sh.S, sh.H);
-  const float* Dws = reinterpret_cast<const float*>(ws + L.d_off);
-  const uint32_t* minseg = reinterpret_cast<const uint32_t*>(ws + L.minseg64);
-  const size_t s2 = sizeof(KmSmem<DP>);
-  if (allow_smem(bwd_key_major<DP>, s2) != cudaSuccess) return check_launch("bwd smem attribute");
-  const int nt = (sh.S + BT - 1) / BT;
-  bwd_key_major<DP><<<dim3(nt, sh.Hk), NT, s2, st>>>(Q, K, V, dO, LSE, seg, Dws, minseg, dK, dV, sh);
-  note_launch();
-  return check_launch("simt backward (key-major)");
-}
-
 }  // namespace
 
 gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cudaStream_t st,
@@ -501,13 +498,6 @@ gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cuda
   return check_launch("tile min seg");
 }
 
-gqa_status simt_bwd_key_major(const float* Q, const float* K, const float* V, const float* dO,
-                              const float* LSE, const uint32_t* seg, float* dK, float* dV,
-                              const Shape& sh, char* ws, cudaStream_t st) {
-  if (sh.d <= 32) return key_major_launch<32>(Q, K, V, dO, LSE, seg, dK, dV, sh, ws, st);
-  if (sh.d <= 64) return key_major_launch<64>(Q, K, V, dO, LSE, seg, dK, dV, sh, ws, st);
-  return key_major_launch<128>(Q, K, V, dO, LSE, seg, dK, dV, sh, ws, st);
-}
 
 gqa_status simt_fwd_lse(const float* Q, const float* K, const float* V, const uint32_t* seg,
                         float* O, float* LSE, const Shape& sh, cudaStream_t st) {
@@ -518,10 +508,10 @@ gqa_status simt_fwd_lse(const float* Q, const float* K, const float* V, const ui
 
 gqa_status simt_bwd(const float* Q, const float* K, const float* V, const float* dO,
                     const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
-                    const Shape& sh, char* ws, cudaStream_t st) {
-  if (sh.d <= 32) return bwd_launch<32>(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, ws, st);
-  if (sh.d <= 64) return bwd_launch<64>(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, ws, st);
-  return bwd_launch<128>(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, ws, st);
+                    const Shape& sh, char* ws, cudaStream_t st, const RopeParams& rope) {
+  if (sh.d <= 32) return bwd_launch<32>(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, ws, st, rope);
+  if (sh.d <= 64) return bwd_launch<64>(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, ws, st, rope);
+  return bwd_launch<128>(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, ws, st, rope);
 }
 
 }  // namespace gqa

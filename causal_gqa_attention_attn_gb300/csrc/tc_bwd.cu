@@ -134,8 +134,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap mapKt,
                    const float* __restrict__ Q, const float* __restrict__ dO,
                    const float* __restrict__ LSE, const uint32_t* __restrict__ seg,
-                   float* __restrict__ dQ, float* __restrict__ Dws, uint32_t* __restrict__ status,
-                   Shape sh) {
+                   float* __restrict__ dQ, float* __restrict__ Dws, float* __restrict__ Qt,
+                   float* __restrict__ dOt, long long ld_qt, uint32_t* __restrict__ status,
+                   Shape sh, const RopeParams rope) {
   using Cfg = QmCfg<D, C>;
   constexpr int NU = Cfg::NUNIT;
   constexpr bool kCl = C > 1;
@@ -351,9 +352,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = lane_base(tmem, warp);
     const long long row_off = (long long)q * H * D + (long long)h * D;
     // Q (warpgroup 0) or dO (warpgroup 1) rows into TMEM, rounded to TF32:
-    // the A operands of S and dP
+    // the A operands of S and dP. The same rows go, unrounded, to the
+    // transposed copy Q^T / dO^T that the key-major kernel reads (column
+    // q0*G + r of kv group g; a warp's 32 rows are 32 adjacent columns, so
+    // each store instruction writes 128 contiguous bytes). Rows past the
+    // sequence write the zero padding columns.
     {
       const float* src = (wg == 0) ? Q : dO;
+      float* xt = (wg == 0) ? Qt : dOt;
+      const long long col = (long long)q0 * G + r;
+      const bool in_ld = col < ld_qt;
       const uint32_t col0 = (wg == 0) ? Cfg::T_Q : Cfg::T_DO;
       float v[32];
       for (int cc = 0; cc < D; cc += 32) {
@@ -361,6 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 32; i += 4) {
           float4 x = valid ? __ldg(reinterpret_cast<const float4*>(src + row_off + cc + i))
                            : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (in_ld) {
+            float* p = xt + (long long)(g * D + cc + i) * ld_qt + col;
+            p[0] = x.x; p[ld_qt] = x.y; p[2 * ld_qt] = x.z; p[3 * ld_qt] = x.w;
+          }
           v[i] = to_tf32(x.x); v[i + 1] = to_tf32(x.y); v[i + 2] = to_tf32(x.z); v[i + 3] = to_tf32(x.w);
         }
         tmem_st32(tl + col0 + cc, v);
@@ -451,7 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++my_use;
       }
     }
-    // epilogue: dQ += accumulated tile (warpgroup wg: half wg of the columns), D to the workspace
+    // epilogue: dQ += accumulated tile (warpgroup wg: half wg of the columns),
+    // NaN-guarded and, with rope.on, rotated by the RoPE backward of row q;
+    // D to the workspace
     if (ok && mbar_wait<kCl>(&bars.dq_done, 0, abort, status, kSiteQmCompute)) {
       tc_fence_after();
       for (int cc = wg * (D / 2); cc < (wg + 1) * (D / 2); cc += 16) {
@@ -459,14 +473,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(tl + Cfg::T_DQ + cc, v);
         tmem_ld_wait();
         if (valid) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = (v[i] == v[i]) ? v[i] : 0.f;
+          if (rope.on) {
+            const long long tpos = (long long)q + rope.pos_offset;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) rope_rotate(v[2 * j], v[2 * j + 1], tpos, cc / 2 + j, rope);
+          }
           float4* dst = reinterpret_cast<float4*>(dQ + row_off + cc);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             float4 o = dst[i];
-            o.x += (v[4 * i] == v[4 * i]) ? v[4 * i] : 0.f;
-            o.y += (v[4 * i + 1] == v[4 * i + 1]) ? v[4 * i + 1] : 0.f;
-            o.z += (v[4 * i + 2] == v[4 * i + 2]) ? v[4 * i + 2] : 0.f;
-            o.w += (v[4 * i + 3] == v[4 * i + 3]) ? v[4 * i + 3] : 0.f;
+            o.x += v[4 * i];
+            o.y += v[4 * i + 1];
+            o.z += v[4 * i + 2];
+            o.w += v[4 * i + 3];
             dst[i] = o;
           }
         }
@@ -552,7 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const float* __restrict__ LSE, const float* __restrict__ Dws,
                  const uint32_t* __restrict__ seg, const uint32_t* __restrict__ blk_minseg,
                  const uint32_t* __restrict__ blk_maxseg, float* __restrict__ dK,
-                 float* __restrict__ dV, uint32_t* __restrict__ status, Shape sh) {
+                 float* __restrict__ dV, uint32_t* __restrict__ status, Shape sh,
+                 const RopeParams rope) {
   using Cfg = KmCfg<D>;
   constexpr int NQ = Cfg::NQ;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -788,7 +810,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars.p_ready[wg]);
       ++mine;
     }
-    // epilogue: warpgroup 0 adds dK, warpgroup 1 adds dV (owned rows)
+    // epilogue: warpgroup 0 adds dK (rotated by the RoPE backward of the key's
+    // position when rope.on), warpgroup 1 adds dV (owned rows, NaN-guarded)
     if (ok && mbar_wait(&bars.acc_done, 0, abort, status, kSiteKmCompute)) {
       tc_fence_after();
       const long long row = (long long)key * sh.Hk * D + (long long)g * D;
@@ -799,14 +822,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(src + cc, a);
         tmem_ld_wait();
         if (key < S && n > 0) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = (a[i] == a[i]) ? a[i] : 0.f;
+          if (wg == 0 && rope.on) {
+            const long long tpos = (long long)key + rope.pos_offset;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) rope_rotate(a[2 * j], a[2 * j + 1], tpos, cc / 2 + j, rope);
+          }
           float4* pk = reinterpret_cast<float4*>(dst_row + cc);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             float4 o = pk[i];
-            o.x += (a[4 * i] == a[4 * i]) ? a[4 * i] : 0.f;
-            o.y += (a[4 * i + 1] == a[4 * i + 1]) ? a[4 * i + 1] : 0.f;
-            o.z += (a[4 * i + 2] == a[4 * i + 2]) ? a[4 * i + 2] : 0.f;
-            o.w += (a[4 * i + 3] == a[4 * i + 3]) ? a[4 * i + 3] : 0.f;
+            o.x += a[4 * i];
+            o.y += a[4 * i + 1];
+            o.z += a[4 * i + 2];
+            o.w += a[4 * i + 3];
             pk[i] = o;
           }
         }
@@ -942,7 +972,7 @@ gqa_status km_launch(const float* Q, const float* K, const float* V, const float
                      const float* LSE, const uint32_t* seg, float* dK, float* dV, const float* Qt,
                      const float* dOt, long long ld_qt, const float* Dws, const uint32_t* blk_minseg,
                      const uint32_t* blk_maxseg, uint32_t* status, const Shape& sh,
-                     cudaStream_t st) {
+                     cudaStream_t st, const RopeParams& rope) {
   using Cfg = KmCfg<D>;
   const int QB = Cfg::NQ / sh.G;
   CUtensorMap mv, mq, mdo, mqt, mdot;
@@ -959,7 +989,7 @@ gqa_status km_launch(const float* Q, const float* K, const float* V, const float
   dim3 grid((sh.S + 127) / 128, sh.Hk);
   return launch_clustered(tc_key_major<D>, grid, 1, Cfg::SMEM_BYTES, st, "tensor-core key-major",
                           mv, mq, mdo, mqt, mdot, K, LSE, Dws, seg, blk_minseg, blk_maxseg, dK, dV,
-                          status, sh);
+                          status, sh, rope);
 }
 
 gqa_status transpose_launch(const float* X, float* Xt, int S, int Hk, int Gx, int d, long long ld,
@@ -987,8 +1017,9 @@ int cta_group() {
 template <int D, int C>
 gqa_status qm_launch_c(const float* Q, const float* K, const float* V, const float* dO,
                        const float* LSE, const uint32_t* seg, float* dQ, const float* Kt,
-                       long long ld_kt, float* Dws, uint32_t* status, const Shape& sh,
-                       cudaStream_t st) {
+                       long long ld_kt, float* Dws, float* Qt, float* dOt, long long ld_qt,
+                       uint32_t* status, const Shape& sh, cudaStream_t st,
+                       const RopeParams& rope) {
   using Cfg = QmCfg<D, C>;
   CUtensorMap mk, mv, mkt;
   gqa_status r;
@@ -1003,18 +1034,18 @@ gqa_status qm_launch_c(const float* Q, const float* K, const float* V, const flo
   const int n_slabs = (sh.S + QR - 1) / QR;
   dim3 grid((n_slabs + C - 1) / C * C, sh.Hk);
   return launch_clustered(tc_query_major<D, C>, grid, C, Cfg::SMEM_BYTES, st,
-                          "tensor-core query-major", mk, mv, mkt, Q, dO, LSE, seg, dQ, Dws, status,
-                          sh);
+                          "tensor-core query-major", mk, mv, mkt, Q, dO, LSE, seg, dQ, Dws, Qt, dOt,
+                          ld_qt, status, sh, rope);
 }
 
 template <int D>
 gqa_status qm_launch(const float* Q, const float* K, const float* V, const float* dO,
                      const float* LSE, const uint32_t* seg, float* dQ, const float* Kt,
-                     long long ld_kt, float* Dws, uint32_t* status, const Shape& sh,
-                     cudaStream_t st) {
+                     long long ld_kt, float* Dws, float* Qt, float* dOt, long long ld_qt,
+                     uint32_t* status, const Shape& sh, cudaStream_t st, const RopeParams& rope) {
   if (cta_group() == 1)
-    return qm_launch_c<D, 1>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, status, sh, st);
-  return qm_launch_c<D, 2>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, status, sh, st);
+    return qm_launch_c<D, 1>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
+  return qm_launch_c<D, 2>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
 }
 
 }  // namespace
@@ -1052,7 +1083,7 @@ bool tc_supported(const Shape& sh) {
 
 gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* dO,
                   const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
-                  const Shape& sh, char* ws, cudaStream_t st) {
+                  const Shape& sh, char* ws, cudaStream_t st, const RopeParams& rope) {
   const WsLayout L = ws_layout(sh.S, sh.H);
   const TcWsLayout T = tc_ws_layout(sh.S, sh.H, sh.Hk, sh.d);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
@@ -1065,25 +1096,25 @@ gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* d
   const int QB = ((sh.d == 128) ? KmCfg<128>::NQ : KmCfg<64>::NQ) / sh.G;
   gqa_status r;
   if ((r = tile_minseg(seg, sh.S, QB, blk, st, blk_max)) != GQA_OK) return r;
+  // K^T for the query-major kernel; Q^T and dO^T are written by the
+  // query-major kernel itself for the key-major one
   if ((r = transpose_launch(K, Kt, sh.S, sh.Hk, 1, sh.d, T.ld_kt, st)) != GQA_OK) return r;
-  if ((r = transpose_launch(Q, Qt, sh.S, sh.Hk, sh.G, sh.d, T.ld_qt, st)) != GQA_OK) return r;
-  if ((r = transpose_launch(dO, dOt, sh.S, sh.Hk, sh.G, sh.d, T.ld_qt, st)) != GQA_OK) return r;
   profile_before(st, "tc_query_major+tc_key_major");
   switch (sh.d) {
     case 32:
-      r = qm_launch<32>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, status, sh, st);
+      r = qm_launch<32>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope);
       if (r == GQA_OK)
-        r = km_launch<32>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st);
+        r = km_launch<32>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope);
       break;
     case 64:
-      r = qm_launch<64>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, status, sh, st);
+      r = qm_launch<64>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope);
       if (r == GQA_OK)
-        r = km_launch<64>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st);
+        r = km_launch<64>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope);
       break;
     default:
-      r = qm_launch<128>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, status, sh, st);
+      r = qm_launch<128>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope);
       if (r == GQA_OK)
-        r = km_launch<128>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st);
+        r = km_launch<128>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope);
       break;
   }
   profile_after(st);

@@ -89,6 +89,27 @@ gqa_status attn_bwd(const float* Q, const float* K, const float* V, const float*
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_bwd_rope — attn_bwd followed by the interleaved RoPE backward on the
+ * attention gradients of Q and K (the step of a RoPE model: the pages apply
+ * rope_q_backward / rope_k_backward of backward_attention.wgsl, and tang
+ * llm.rs interleaved_rope_backward, to dQ and dK after the attention
+ * backward). The rotation is fused into the kernels' final writes:
+ *   dQ[i,h] += R_i^T (attention dQ[i,h]),  dK[j,g] += R_j^T (attention dK[j,g]),
+ *   dV[j,g] += attention dV[j,g]
+ * where R_t rotates pair p of a head by t*base^(-2p/head_dim), t = pos_offset
+ * + row (the same rotation as rope_bwd_inplace). With dQ, dK zeroed first
+ * this equals attn_bwd then rope_bwd_inplace on dQ and dK; with non-zero
+ * dQ / dK only the new contribution is rotated. Same arguments, workspace,
+ * paths and errors as attn_bwd, plus pos_offset >= 0 and base > 0
+ * (GQA_ERR_INVALID_ARG otherwise).
+ */
+gqa_status attn_bwd_rope(const float* Q, const float* K, const float* V, const float* dO,
+                         const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
+                         int seq_len, int n_heads, int n_kv_heads, int head_dim, float scale,
+                         int pos_offset, float base, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
  * attn_bwd_simt — the same operation and contract as attn_bwd, computed with
  * fp32 FFMA on CUDA cores only (no tensor cores): exact fp32 products, any
  * head_dim that is a multiple of 4 up to 128. Deterministic.

@@ -1,6 +1,7 @@
 """Full-size parity on the 16k-token workload (S=16384, H=32, Hk=8, d=128,
 N(0, 0.5^2), pure causal) in the launch configuration the benchmark times:
-attention backward followed by the RoPE backward on dQ and dK.
+the attention backward with the RoPE backward on dQ and dK fused into its
+final writes (attn_bwd_rope).
 
 The fp64 oracle cannot form the whole backward at this size in a test's time,
 so it forms sampled outputs one by one: dQ rows (every head) spread over the
@@ -54,9 +55,8 @@ def test_causal16k_sampled_with_rope(ga):
     dQ = torch.zeros(S, H * d, device="cuda")
     dK = torch.zeros(S, Hk * d, device="cuda")
     dV = torch.zeros(S, Hk * d, device="cuda")
-    ws = ga.attn_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, H, Hk, d, sc)
-    ga.rope_bwd_inplace(dQ, H, d, 0, 10000.0)
-    ga.rope_bwd_inplace(dK, Hk, d, 0, 10000.0)
+    ws = ga.attn_bwd_rope(Q, K, V, dO, LSE, seg, dQ, dK, dV, H, Hk, d, sc, pos_offset=0,
+                          base=10000.0)
     ga.read_device_status(ws)
     torch.cuda.synchronize()
     assert bool(torch.isfinite(dQ).all()) and bool(torch.isfinite(dK).all())

@@ -174,3 +174,33 @@ def test_rope_backward_matches_oracle(ga, pos_offset):
     ref = oracle.rope_bwd(X, H, d, pos_offset=pos_offset, base=10000.0)
     got = t.cpu().numpy()
     assert np.max(np.abs(got - ref)) <= 2e-6 * np.max(np.abs(ref))
+
+
+FUSED_ROPE = [
+    (300, 8, 2, 128, "docs", 0), (200, 16, 4, 64, "causal", 7), (129, 4, 2, 32, "nonmonotone", 0),
+    (97, 4, 2, 100, "docs", 0), (256, 8, 2, 128, "causal", 40000), (65, 4, 1, 64, "docs", 40000),
+]
+
+
+@pytest.mark.parametrize("S,H,Hk,d,seg_kind,pos", FUSED_ROPE)
+def test_fused_rope_backward_matches_oracle(ga, S, H, Hk, d, seg_kind, pos):
+    """attn_bwd_rope: dQ += R^T(attention dQ), dK += R^T(attention dK), dV += dV
+    on non-zero initial gradients (only the new contribution is rotated);
+    tensor-core shapes and a CUDA-core one (d = 100), both angle paths."""
+    x = _edge_inputs(S, H, Hk, d, seg_kind, seed=S * 7 + d + pos)
+    _, lse = oracle.fwd(x["Q"], x["K"], x["V"], x["seg"], H, Hk, d, x["scale"])
+    lse32 = lse.astype(np.float32)
+    rq, rk, rv = oracle.bwd(x["Q"], x["K"], x["V"], x["dO"], lse32, x["seg"], H, Hk, d, x["scale"])
+    rng = np.random.default_rng(S + pos)
+    init = [rng.standard_normal(a.shape).astype(np.float32) for a in (rq, rk, rv)]
+    t = {k: _dev(x[k]) for k in ("Q", "K", "V", "dO")}
+    dQ, dK, dV = (_dev(a) for a in init)
+    ws = ga.attn_bwd_rope(t["Q"], t["K"], t["V"], t["dO"], _dev(lse32), _seg_dev(x["seg"]),
+                          dQ, dK, dV, H, Hk, d, x["scale"], pos_offset=pos, base=10000.0)
+    ga.read_device_status(ws)
+    torch.cuda.synchronize()
+    want_q = init[0] + oracle.rope_bwd(rq, H, d, pos_offset=pos, base=10000.0)
+    want_k = init[1] + oracle.rope_bwd(rk, Hk, d, pos_offset=pos, base=10000.0)
+    assert_parity("dQ", dQ.cpu().numpy() - init[0], want_q - init[0], scale_ref=rv)
+    assert_parity("dK", dK.cpu().numpy() - init[1], want_k - init[1], scale_ref=rv)
+    assert_parity("dV", dV.cpu().numpy() - init[2], rv)

@@ -96,6 +96,22 @@ def test_fwd_and_rope_reject_bad_arguments(L):
     assert rope(FAKE, 0, 4, 8, 0, 10000.0, None) == 0
 
 
+def test_fused_rope_rejects_bad_arguments(L):
+    def call(S=128, H=4, Hk=2, d=32, pos=0, base=10000.0, ws_bytes=None, ptrs=None):
+        p = [FAKE] * 10 if ptrs is None else ptrs
+        if ws_bytes is None:
+            ws_bytes = L.attn_bwd_workspace_bytes(S, H, Hk, d)
+        return L.attn_bwd_rope(*p[:9], S, H, Hk, d, 0.17, pos, base, p[9], ws_bytes, None)
+    assert call(pos=-1) == 1
+    assert call(base=0.0) == 1 and call(base=-2.0) == 1 and call(base=float("inf")) == 1
+    assert call(H=6, Hk=4) == 1 and call(d=30) == 1 and call(d=132) == 2
+    assert call(ws_bytes=16) == 1
+    p = [FAKE] * 10
+    p[6] = None                                                  # dQ
+    assert call(ptrs=p) == 1
+    assert call(S=0) == 0
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ga, "_lib", None)
     monkeypatch.setattr(ga, "_LIB_PATH", str(tmp_path / "missing.so"))
