@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.s_free[i], C * kComputeWarps / 2);   // the stage's warpgroup in each CTA
+      mbar_init(&bars.s_free[i], C * kComputeWarps);   // every compute warp of each CTA
     }
     mbar_init(&bars.qdo_ready, C * kComputeWarps);
     mbar_init(&bars.dq_done, 1);
@@ -318,7 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = s & 1, j = s / Cfg::NSUB, h = s % Cfg::NSUB;
       const int ik = 2 * nk + 3 * j;
       if (h == 0 && (!unit_wait(ik) || !unit_wait(ik + 1))) { ok = false; break; }
-      if (!stage_free(st)) { ok = false; break; }
+      // the stage's previous use: pass 1 for s < 2, else sub-chunk s-2, whose
+      // release issue_dq(s-2) has already waited for
+      if (s < 2 && !stage_free(st)) { ok = false; break; }
       const uint64_t off = (uint64_t)((h * Cfg::HALF2 * 128) >> 4);   // rows h*HALF2.. of each panel
       if (elect_one()) {
         issue_sdp(tmem + Cfg::p2_stage(st), Cfg::BK2, id_s2, unit_desc(ik) + off, unit_desc(ik + 1) + off);
@@ -387,81 +389,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int segq = valid ? (int)__ldg(seg + q) : 0;
     float Dpart = 0.f;
     bool ok = true;
-    int my_use = 0;
+    // Both warpgroups take every chunk / sub-chunk, warpgroup wg the columns
+    // [wg*W/2, (wg+1)*W/2) of it: the softmax of a chunk then finishes in
+    // half the time, which is what the MMA warp waits for before dQ.
     // ---- pass 1: D = rowsum(P dP) ----
-    {
-      const uint32_t ts = tl + Cfg::p1_stage(wg), tdp = ts + Cfg::BK1;
-      for (int c = wg; c < nk; c += 2) {
-        const int k0 = (kc0 + c) * Cfg::BK1;
-        if (!mbar_wait<kCl>(&bars.s_full[wg], my_use & 1, abort, status, kSiteQmCompute)) { ok = false; break; }
-        tc_fence_after();
-        // every key of the chunk visible to this row: no per-element mask
-        const bool full = valid && k0 >= segq && k0 + Cfg::BK1 - 1 <= q;
+    constexpr int H1 = Cfg::BK1 / 2, H2 = Cfg::BK2 / 2;
+    static_assert(H1 == 32 && (H2 == 16 || H2 == 32), "column split");
+    for (int c = 0; c < nk; ++c) {
+      const int st = c & 1;
+      if (!mbar_wait<kCl>(&bars.s_full[st], (c >> 1) & 1, abort, status, kSiteQmCompute)) { ok = false; break; }
+      tc_fence_after();
+      const int k0 = (kc0 + c) * Cfg::BK1 + wg * H1;          // this warpgroup's first key
+      // every key of these columns visible to this row: no per-element mask
+      const bool full = valid && k0 >= segq && k0 + H1 - 1 <= q;
+      const uint32_t ts = tl + Cfg::p1_stage(st) + wg * H1;
+      float sv[32], dp[32];
+      tmem_ld32(ts, sv);
+      tmem_ld32(ts + Cfg::BK1, dp);
+      tmem_ld_wait();
+      if (full) {
 #pragma unroll
-        for (int jb = 0; jb < Cfg::BK1; jb += 32) {
-          float sv[32], dp[32];
-          tmem_ld32(ts + jb, sv);
-          tmem_ld32(tdp + jb, dp);
-          tmem_ld_wait();
-          if (full) {
+        for (int j = 0; j < 32; ++j) Dpart = fmaf(ex2(fmaf(sv[j], sl2, -lse2)), dp[j], Dpart);
+      } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) Dpart = fmaf(ex2(fmaf(sv[j], sl2, -lse2)), dp[j], Dpart);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int key = k0 + jb + j;
-              const bool vis = valid && key >= segq && key <= q;
-              Dpart = fmaf(vis ? ex2(fmaf(sv[j], sl2, -lse2)) : 0.f, dp[j], Dpart);
-            }
-          }
+        for (int j = 0; j < 32; ++j) {
+          const int key = k0 + j;
+          const bool vis = valid && key >= segq && key <= q;
+          Dpart = fmaf(vis ? ex2(fmaf(sv[j], sl2, -lse2)) : 0.f, dp[j], Dpart);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) arrive_issuer<C>(&bars.s_free[wg]);
-        ++my_use;
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_issuer<C>(&bars.s_free[st]);
     }
-    // both warpgroups' partial sums (each has finished reading its pass-1 stage)
+    // both warpgroups' partial sums (each has finished reading the pass-1 stages)
     bars.dx[wg][r] = Dpart;
     tc_fence_before();
     asm volatile("bar.sync 2, 256;" ::: "memory");
     const float Drow = bars.dx[0][r] + bars.dx[1][r];
     // ---- pass 2: dS = scale P (dP - D) over S, for dQ += dS K ----
-    if (ok) {
-      const uint32_t ts = tl + Cfg::p2_stage(wg), tdp = ts + Cfg::BK2;
-      for (int s = wg; s < n_sub; s += 2) {
-        const int kc = (kc0 + s / Cfg::NSUB) * Cfg::BK1, hh = s % Cfg::NSUB;
-        if (!mbar_wait<kCl>(&bars.s_full[wg], my_use & 1, abort, status, kSiteQmCompute)) { ok = false; break; }
-        tc_fence_after();
-        // the sub-chunk's keys lie in [kc + key_of(hh, 0), kc + key_of(hh, BK2 - 1)]
-        const bool full = valid && kc + Cfg::key_of(hh, 0) >= segq && kc + Cfg::key_of(hh, Cfg::BK2 - 1) <= q;
-#pragma unroll
-        for (int jb = 0; jb < Cfg::BK2; jb += 32) {
-          float sv[32], dp[32];
-          tmem_ld32(ts + jb, sv);
-          tmem_ld32(tdp + jb, dp);
-          tmem_ld_wait();
-          if (full) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              sv[j] = to_tf32(sh.scale * ex2(fmaf(sv[j], sl2, -lse2)) * (dp[j] - Drow));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int key = kc + Cfg::key_of(hh, jb + j);
-              const bool vis = valid && key >= segq && key <= q;
-              const float pj = vis ? ex2(fmaf(sv[j], sl2, -lse2)) : 0.f;
-              sv[j] = to_tf32(sh.scale * pj * (dp[j] - Drow));
-            }
-          }
-          tmem_st32(ts + jb, sv);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) arrive_issuer<C>(&bars.s_free[wg]);
-        ++my_use;
+    for (int s = 0; ok && s < n_sub; ++s) {
+      const int st = s & 1;
+      const int u1 = st ? nk / 2 : (nk + 1) / 2;              // pass-1 uses of this stage
+      if (!mbar_wait<kCl>(&bars.s_full[st], (u1 + (s >> 1)) & 1, abort, status, kSiteQmCompute)) {
+        ok = false;
+        break;
       }
+      tc_fence_after();
+      const int kc = (kc0 + s / Cfg::NSUB) * Cfg::BK1, hh = s % Cfg::NSUB;
+      const int n0 = wg * H2;                                  // this warpgroup's first column
+      // these columns' keys lie in [kc + key_of(hh, n0), kc + key_of(hh, n0 + H2 - 1)]
+      const bool full = valid && kc + Cfg::key_of(hh, n0) >= segq &&
+                        kc + Cfg::key_of(hh, n0 + H2 - 1) <= q;
+      const uint32_t ts = tl + Cfg::p2_stage(st) + n0;
+      float sv[H2], dp[H2];
+      if constexpr (H2 == 16) {
+        tmem_ld16(ts, sv);
+        tmem_ld16(ts + Cfg::BK2, dp);
+      } else {
+        tmem_ld32(ts, sv);
+        tmem_ld32(ts + Cfg::BK2, dp);
+      }
+      tmem_ld_wait();
+      if (full) {
+#pragma unroll
+        for (int j = 0; j < H2; ++j)
+          sv[j] = to_tf32(sh.scale * ex2(fmaf(sv[j], sl2, -lse2)) * (dp[j] - Drow));
+      } else {
+#pragma unroll
+        for (int j = 0; j < H2; ++j) {
+          const int key = kc + Cfg::key_of(hh, n0 + j);
+          const bool vis = valid && key >= segq && key <= q;
+          const float pj = vis ? ex2(fmaf(sv[j], sl2, -lse2)) : 0.f;
+          sv[j] = to_tf32(sh.scale * pj * (dp[j] - Drow));
+        }
+      }
+      if constexpr (H2 == 16) tmem_st16(ts, sv);
+      else tmem_st32(ts, sv);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_issuer<C>(&bars.s_free[st]);
     }
     // epilogue: dQ += accumulated tile (warpgroup wg: half wg of the columns),
     // NaN-guarded and, with rope.on, rotated by the RoPE backward of row q;
