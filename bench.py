@@ -49,6 +49,13 @@ def counted_flops(head_dim: int, n_heads: int, pairs: int) -> float:
     return 10.0 * head_dim * n_heads * pairs
 
 
+def executed_flops(head_dim: int, n_heads: int, pairs: int, contractions: int = 9) -> float:
+    """What the tensor-core path multiplies: the query-major kernel forms S and
+    dP twice (D pass, dS pass) plus dS K, the key-major kernel S^T and dP^T
+    again plus P^T dO and dS^T Q: nine d-deep contractions per pair and head."""
+    return 2.0 * contractions * head_dim * n_heads * pairs
+
+
 def dist_env() -> tuple[int, int, int]:
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -357,6 +364,11 @@ def run_gpu(args) -> dict | None:
     roof.update({"kernel": stage, "achieved": achieved, "peak": peak, "frac": achieved / peak,
                  "traffic": _traffic(stage, w.name), "stage_ms": stage_ms,
                  "flops_per_launch": flops})
+    if tensor_path:
+        ex = executed_flops(d, H, pairs)
+        roof.update({"executed_flops_per_launch": ex,
+                     "executed_tflops": ex / (stage_ms / 1e3) / 1e12,
+                     "executed_frac": ex / (stage_ms / 1e3) / 1e12 / peak})
     tf32 = tf32_peak(peaks, sustained=False)
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,

@@ -15,6 +15,8 @@ def test_counted_flops_and_pairs():
     pairs = workloads.n_pairs(x)
     assert pairs == w.seq_len * (w.seq_len + 1) // 2 == 134225920
     assert bench.counted_flops(128, 32, pairs) == pytest.approx(5.4978936832e12)
+    # nine executed contractions against five counted
+    assert bench.executed_flops(128, 32, pairs) == pytest.approx(bench.counted_flops(128, 32, pairs) * 9 / 5)
 
 
 def test_tf32_peak_from_measured_bf16():
