@@ -228,7 +228,10 @@ def run_gpu(args) -> dict | None:
     dV = torch.zeros(S, Hk * d, device=dev)
     ws = torch.empty(ga.workspace_bytes(S, H, Hk, d), dtype=torch.uint8, device=dev)
 
-    fused_rope = w.rope and args.path == "auto"
+    fused_rope = w.rope and args.path == "auto" and not args.given_o
+    O_dev = None
+    if args.given_o:       # the forward output O, as a training step keeps it (setup, untimed)
+        O_dev, _ = ga.attn_fwd_lse(t["Q"], t["K"], t["V"], t["seg"], H, Hk, d, sc)
 
     def step():
         dQ.zero_()
@@ -238,8 +241,12 @@ def run_gpu(args) -> dict | None:
             ga.attn_bwd_rope(t["Q"], t["K"], t["V"], t["dO"], t["LSE"], t["seg"], dQ, dK, dV, H,
                              Hk, d, sc, pos_offset=0, base=10000.0, workspace=ws)
             return
-        impl_fn(t["Q"], t["K"], t["V"], t["dO"], t["LSE"], t["seg"], dQ, dK, dV, H, Hk, d, sc,
-                workspace=ws)
+        if args.given_o:
+            ga.attn_bwd_o(t["Q"], t["K"], t["V"], t["dO"], O_dev, t["LSE"], t["seg"], dQ, dK, dV,
+                          H, Hk, d, sc, workspace=ws)
+        else:
+            impl_fn(t["Q"], t["K"], t["V"], t["dO"], t["LSE"], t["seg"], dQ, dK, dV, H, Hk, d, sc,
+                    workspace=ws)
         if w.rope:
             ga.rope_bwd_inplace(dQ, H, d, 0, 10000.0)
             ga.rope_bwd_inplace(dK, Hk, d, 0, 10000.0)
@@ -281,6 +288,11 @@ def run_gpu(args) -> dict | None:
     # on copy streams while step k computes.
     h2d = sum(host[k].numel() * host[k].element_size() for k in ("Q", "K", "V", "dO", "LSE", "seg"))
     names = ("Q", "K", "V", "dO", "LSE", "seg")
+    if args.given_o:
+        host["O"] = O_dev.cpu().pin_memory()
+        t["O"] = O_dev
+        names = names + ("O",)
+        h2d += host["O"].numel() * host["O"].element_size()
     ins = [t, {k: torch.empty_like(t[k]) for k in names}]
     grads = [(dQ, dK, dV), tuple(torch.empty_like(g) for g in (dQ, dK, dV))]
     outs = [tuple(torch.empty(g.shape, pin_memory=True) for g in (dQ, dK, dV)) for _ in range(2)]
@@ -312,8 +324,12 @@ def run_gpu(args) -> dict | None:
             ga.attn_bwd_rope(x["Q"], x["K"], x["V"], x["dO"], x["LSE"], x["seg"], gq, gk, gv, H,
                              Hk, d, sc, pos_offset=0, base=10000.0, workspace=ws)
         else:
-            impl_fn(x["Q"], x["K"], x["V"], x["dO"], x["LSE"], x["seg"], gq, gk, gv, H, Hk, d, sc,
-                    workspace=ws)
+            if args.given_o:
+                ga.attn_bwd_o(x["Q"], x["K"], x["V"], x["dO"], x["O"], x["LSE"], x["seg"], gq, gk,
+                              gv, H, Hk, d, sc, workspace=ws)
+            else:
+                impl_fn(x["Q"], x["K"], x["V"], x["dO"], x["LSE"], x["seg"], gq, gk, gv, H, Hk, d,
+                        sc, workspace=ws)
             if w.rope:
                 ga.rope_bwd_inplace(gq, H, d, 0, 10000.0)
                 ga.rope_bwd_inplace(gk, Hk, d, 0, 10000.0)
@@ -365,7 +381,7 @@ def run_gpu(args) -> dict | None:
                  "traffic": _traffic(stage, w.name), "stage_ms": stage_ms,
                  "flops_per_launch": flops})
     if tensor_path:
-        ex = executed_flops(d, H, pairs)
+        ex = executed_flops(d, H, pairs, 7 if args.given_o else 9)
         roof.update({"executed_flops_per_launch": ex,
                      "executed_tflops": ex / (stage_ms / 1e3) / 1e12,
                      "executed_frac": ex / (stage_ms / 1e3) / 1e12 / peak})
@@ -380,7 +396,8 @@ def run_gpu(args) -> dict | None:
                    "n_kv_heads": Hk, "head_dim": d, "n_pairs": pairs,
                    "counted_flop_per_step": flops,
                    "step": ("zero grads + attn_bwd_rope (RoPE backward of dQ, dK fused)" if fused_rope else
-                            "zero grads + attn_bwd" + (" + rope_bwd(dQ) + rope_bwd(dK)" if w.rope else "")),
+                            "zero grads + " + ("attn_bwd_o (D from the forward's O)" if args.given_o else "attn_bwd") +
+                            (" + rope_bwd(dQ) + rope_bwd(dK)" if w.rope else "")),
                    "l2": "inputs larger than L2 (129 MB)" if 4 * S * H * d > 129e6 else
                          "inputs smaller than L2: steps run back to back (warm L2)",
                    "path": stage},
@@ -479,6 +496,8 @@ def main(argv=None):
     ap.add_argument("--path", choices=["auto", "simt"], default="auto",
                     help="auto: attn_bwd (tensor cores where built); simt: attn_bwd_simt")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--given-o", action="store_true",
+                    help="time attn_bwd_o (D = rowsum(dO*O) from the forward's O) instead of the LSE-only call")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

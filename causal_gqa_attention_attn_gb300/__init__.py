@@ -51,6 +51,7 @@ def lib() -> ctypes.CDLL:
     L.attn_bwd.argtypes = bwd_args
     L.attn_bwd_simt.argtypes = bwd_args
     L.attn_bwd_rope.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, F, P, Z, P]
+    L.attn_bwd_o.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
     L.attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P]
     L.attn_bwd_noalloc.restype = ctypes.c_int
     L.rope_bwd_inplace.argtypes = [P, I, I, I, I, F, P]
@@ -69,7 +70,7 @@ def lib() -> ctypes.CDLL:
     L.gqa_launch_count.restype = ctypes.c_ulonglong
     L.gqa_last_error.argtypes = []
     L.gqa_last_error.restype = ctypes.c_char_p
-    for name in ("attn_fwd_lse", "attn_bwd", "attn_bwd_simt", "attn_bwd_rope",
+    for name in ("attn_fwd_lse", "attn_bwd", "attn_bwd_simt", "attn_bwd_rope", "attn_bwd_o",
                  "rope_bwd_inplace", "attn_read_device_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -153,6 +154,23 @@ def attn_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_dim, s
     workspace used (a uint8 device tensor; pass it back in to reuse it)."""
     return _bwd(lib().attn_bwd, Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads,
                 head_dim, scale, workspace, stream)
+
+
+def attn_bwd_o(Q, K, V, dO, O, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_dim, scale,
+               workspace=None, stream=None):
+    """:func:`attn_bwd` given the forward output O: D = rowsum(dO * O) replaces
+    the D pass. Returns the workspace used."""
+    torch = _torch()
+    S = Q.shape[0]
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(S, n_heads, n_kv_heads, head_dim),
+                                device=Q.device, dtype=torch.uint8)
+    _check(lib().attn_bwd_o(
+        _f32(Q, "Q"), _f32(K, "K"), _f32(V, "V"), _f32(dO, "dO"), _f32(O, "O"), _f32(LSE, "LSE"),
+        _seg(seg), _f32(dQ, "dQ"), _f32(dK, "dK"), _f32(dV, "dV"), S, n_heads, n_kv_heads,
+        head_dim, float(scale), _ptr(workspace, "workspace", (torch.uint8,)), workspace.numel(),
+        _stream(stream)))
+    return workspace
 
 
 def attn_bwd_rope(Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_dim, scale,

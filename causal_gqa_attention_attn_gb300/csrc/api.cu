@@ -151,7 +151,7 @@ static gqa_status bwd_dispatch(const float* Q, const float* K, const float* V, c
                                const float* LSE, const uint32_t* seg, float* dQ, float* dK,
                                float* dV, int seq_len, int n_heads, int n_kv_heads, int head_dim,
                                float scale, void* workspace, size_t workspace_bytes, void* stream,
-                               const RopeParams& rope) {
+                               const RopeParams& rope, const float* O = nullptr) {
   gqa_status r = check_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, seq_len, n_heads, n_kv_heads,
                            head_dim, scale, workspace, workspace_bytes);
   if (r != GQA_OK || seq_len == 0) return r;
@@ -167,7 +167,7 @@ static gqa_status bwd_dispatch(const float* Q, const float* K, const float* V, c
     return set_error(GQA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
   if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
     return check_launch("workspace header reset");
-  return tc_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st, rope);
+  return tc_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st, rope, O);
 }
 
 static gqa_status check_rope(int seq_len, int head_dim, int pos_offset, float base) {
@@ -188,6 +188,18 @@ gqa_status attn_bwd(const float* Q, const float* K, const float* V, const float*
                     void* workspace, size_t workspace_bytes, void* stream) {
   return bwd_dispatch(Q, K, V, dO, LSE, seg, dQ, dK, dV, seq_len, n_heads, n_kv_heads, head_dim,
                       scale, workspace, workspace_bytes, stream, no_rope());
+}
+
+gqa_status attn_bwd_o(const float* Q, const float* K, const float* V, const float* dO,
+                      const float* O, const float* LSE, const uint32_t* seg, float* dQ, float* dK,
+                      float* dV, int seq_len, int n_heads, int n_kv_heads, int head_dim,
+                      float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (seq_len > 0) {
+    if (O == nullptr) return set_error(GQA_ERR_INVALID_ARG, "O is NULL");
+    if (!aligned16(O)) return set_error(GQA_ERR_INVALID_ARG, "O is not 16-byte aligned");
+  }
+  return bwd_dispatch(Q, K, V, dO, LSE, seg, dQ, dK, dV, seq_len, n_heads, n_kv_heads, head_dim,
+                      scale, workspace, workspace_bytes, stream, no_rope(), O);
 }
 
 gqa_status attn_bwd_rope(const float* Q, const float* K, const float* V, const float* dO,

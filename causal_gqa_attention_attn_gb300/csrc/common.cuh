@@ -103,9 +103,12 @@ gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cuda
 
 // Tensor-core backward, tc_bwd.cu: true if this shape has a tensor-core path.
 bool tc_supported(const Shape& sh);
+// With O != nullptr, D = rowsum(dO * O) is formed by a row-dot pass instead
+// of the query-major kernel's first pass (attn_bwd_o).
 gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* dO,
                   const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
-                  const Shape& sh, char* ws, cudaStream_t st, const RopeParams& rope);
+                  const Shape& sh, char* ws, cudaStream_t st, const RopeParams& rope,
+                  const float* O = nullptr);
 
 gqa_status wait_selftest(void* workspace, long long limit_cycles, cudaStream_t st);
 

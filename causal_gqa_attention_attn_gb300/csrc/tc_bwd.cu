@@ -128,7 +128,8 @@ __device__ __forceinline__ void arrive_issuer(uint64_t* bar) {
   else mbar_arrive_cl(mapa_u32(bar, 0));
 }
 
-template <int D, int C>
+// GD: D is given (precomputed from O, attn_bwd_o): pass 1 is skipped.
+template <int D, int C, bool GD>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_query_major(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                    const __grid_constant__ CUtensorMap mapKt,
@@ -196,7 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q_last = min(top_slab * QR + QR, S) - 1;
   const int kc0 = (int)(min(bars.kmin, (unsigned)q_last) / Cfg::BK1);
   const int nk = q_last / Cfg::BK1 - kc0 + 1;          // chunks per pass
-  const int n_units = 5 * nk;                          // 2 per pass-1 chunk, 3 per pass-2 chunk
+  const int p2_base = GD ? 0 : 2 * nk;                 // first pass-2 unit
+  const int n_units = p2_base + 3 * nk;                // 2 per pass-1 chunk, 3 per pass-2 chunk
   const int n_sub = Cfg::NSUB * nk;                    // pass-2 sub-chunks
   volatile int* abort = &bars.abort;
 
@@ -219,9 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           !warp_wait<kCl>(&bars.empty[u], ((i / NU) - 1) & 1, abort, status, kSiteQmProducer))
         break;
       // unit i: pass-1 chunk i/2 (K, V) or pass-2 chunk (i - 2nk)/3 (K, V, K^T)
-      const bool p1 = i < 2 * nk;
-      const int chunk = p1 ? i / 2 : (i - 2 * nk) / 3;
-      const int kind = p1 ? i % 2 : (i - 2 * nk) % 3;
+      const bool p1 = i < p2_base;
+      const int chunk = p1 ? i / 2 : (i - p2_base) / 3;
+      const int kind = p1 ? i % 2 : (i - p2_base) % 3;
       const int key0 = (kc0 + chunk) * Cfg::BK1;
       unsigned char* dst = smem + u * Cfg::UNIT_BYTES;
       if (elect_one()) {
@@ -278,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = warp_wait<kCl>(&bars.qdo_ready, 0, abort, status, kSiteQmMma);
     // ---- pass 1: chunk c in stage c & 1 ----
-    for (int c = 0; ok && c < nk; ++c) {
+    for (int c = 0; ok && !GD && c < nk; ++c) {
       const int st = c & 1;
       if (!unit_wait(2 * c) || !unit_wait(2 * c + 1) || !stage_free(st)) { ok = false; break; }
       if (elect_one()) {
@@ -294,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int dq_use = 0;               // stage use index of the sub-chunk whose dQ is next
     auto issue_dq = [&](int s) -> bool {
       const int st = s & 1, j = s / Cfg::NSUB, h = s % Cfg::NSUB;
-      const int ikt = 2 * nk + 3 * j + 2;
+      const int ikt = p2_base + 3 * j + 2;
       if (!warp_wait<kCl>(&bars.s_free[st], dq_use & 1, abort, status, kSiteQmMma)) return false;
       if (h == 0 && !unit_wait(ikt)) return false;
       const uint32_t a_ds = tmem + Cfg::p2_stage(st), d_q = tmem + Cfg::T_DQ;
@@ -316,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (int s = 0; ok && s < n_sub; ++s) {
       const int st = s & 1, j = s / Cfg::NSUB, h = s % Cfg::NSUB;
-      const int ik = 2 * nk + 3 * j;
+      const int ik = p2_base + 3 * j;
       if (h == 0 && (!unit_wait(ik) || !unit_wait(ik + 1))) { ok = false; break; }
       // the stage's previous use: pass 1 for s < 2, else sub-chunk s-2, whose
       // release issue_dq(s-2) has already waited for
@@ -395,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- pass 1: D = rowsum(P dP) ----
     constexpr int H1 = Cfg::BK1 / 2, H2 = Cfg::BK2 / 2;
     static_assert(H1 == 32 && (H2 == 16 || H2 == 32), "column split");
-    for (int c = 0; c < nk; ++c) {
+    for (int c = 0; !GD && c < nk; ++c) {
       const int st = c & 1;
       if (!mbar_wait<kCl>(&bars.s_full[st], (c >> 1) & 1, abort, status, kSiteQmCompute)) { ok = false; break; }
       tc_fence_after();
@@ -422,15 +424,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) arrive_issuer<C>(&bars.s_free[st]);
     }
-    // both warpgroups' partial sums (each has finished reading the pass-1 stages)
-    bars.dx[wg][r] = Dpart;
-    tc_fence_before();
-    asm volatile("bar.sync 2, 256;" ::: "memory");
-    const float Drow = bars.dx[0][r] + bars.dx[1][r];
+    // both warpgroups' partial sums (each has finished reading the pass-1
+    // stages), or the given D
+    float Drow;
+    if constexpr (GD) {
+      Drow = valid ? Dws[(long long)q * H + h] : 0.f;
+    } else {
+      bars.dx[wg][r] = Dpart;
+      tc_fence_before();
+      asm volatile("bar.sync 2, 256;" ::: "memory");
+      Drow = bars.dx[0][r] + bars.dx[1][r];
+    }
     // ---- pass 2: dS = scale P (dP - D) over S, for dQ += dS K ----
     for (int s = 0; ok && s < n_sub; ++s) {
       const int st = s & 1;
-      const int u1 = st ? nk / 2 : (nk + 1) / 2;              // pass-1 uses of this stage
+      const int u1 = GD ? 0 : (st ? nk / 2 : (nk + 1) / 2);   // pass-1 uses of this stage
       if (!mbar_wait<kCl>(&bars.s_full[st], (u1 + (s >> 1)) & 1, abort, status, kSiteQmCompute)) {
         ok = false;
         break;
@@ -500,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (valid && wg == 0) Dws[(long long)q * H + h] = Drow;
+      if (!GD && valid && wg == 0) Dws[(long long)q * H + h] = Drow;
     }
   }
   tc_fence_before();
@@ -888,6 +896,27 @@ __global__ void __launch_bounds__(256) group_transpose(const float* __restrict__
   }
 }
 
+// D[i, h] = sum_e dO[i, h, e] * O[i, h, e]: one warp per (query, head) row,
+// float4 loads. Equal to sum_j P_ij dP_ij when O is the forward's output for
+// the same LSE (O_i = sum_j P_ij v_j, so dO_i . O_i = sum_j P_ij dO_i . v_j).
+__global__ void __launch_bounds__(256) row_dot_kernel(const float* __restrict__ dO,
+                                                      const float* __restrict__ O,
+                                                      float* __restrict__ Dws, long long rows,
+                                                      int d) {
+  const long long row = (long long)blockIdx.x * 8 + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= rows) return;
+  const float4* a = reinterpret_cast<const float4*>(dO + row * d);
+  const float4* b = reinterpret_cast<const float4*>(O + row * d);
+  float acc = 0.f;
+  for (int v = lane; v < d / 4; v += 32) {
+    const float4 x = __ldg(a + v), y = __ldg(b + v);
+    acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
+  }
+  for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) Dws[row] = acc;
+}
+
 // Self-test of the bounded wait: one thread waits on an mbarrier that nothing
 // arrives on, with a short limit, and must give up and record the site.
 __global__ void wait_selftest_kernel(uint32_t* status, long long limit) {
@@ -1022,7 +1051,7 @@ int cta_group() {
   return c;
 }
 
-template <int D, int C>
+template <int D, int C, bool GD>
 gqa_status qm_launch_c(const float* Q, const float* K, const float* V, const float* dO,
                        const float* LSE, const uint32_t* seg, float* dQ, const float* Kt,
                        long long ld_kt, float* Dws, float* Qt, float* dOt, long long ld_qt,
@@ -1035,13 +1064,13 @@ gqa_status qm_launch_c(const float* Q, const float* K, const float* V, const flo
   if ((r = map_panels(&mk, K, (long long)sh.Hk * D, sh.S, kv_panels, Cfg::HALF1, D / 32)) != GQA_OK) return r;
   if ((r = map_panels(&mv, V, (long long)sh.Hk * D, sh.S, kv_panels, Cfg::HALF1, D / 32)) != GQA_OK) return r;
   if ((r = map_panels(&mkt, Kt, ld_kt, (long long)sh.Hk * D, ld_kt / 32, Cfg::KT_ROWS, Cfg::KT_PANELS)) != GQA_OK) return r;
-  if (cudaFuncSetAttribute(tc_query_major<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tc_query_major<D, C, GD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess)
     return check_launch("query-major smem attribute");
   const int QR = 128 / sh.G;
   const int n_slabs = (sh.S + QR - 1) / QR;
   dim3 grid((n_slabs + C - 1) / C * C, sh.Hk);
-  return launch_clustered(tc_query_major<D, C>, grid, C, Cfg::SMEM_BYTES, st,
+  return launch_clustered(tc_query_major<D, C, GD>, grid, C, Cfg::SMEM_BYTES, st,
                           "tensor-core query-major", mk, mv, mkt, Q, dO, LSE, seg, dQ, Dws, Qt, dOt,
                           ld_qt, status, sh, rope);
 }
@@ -1050,10 +1079,13 @@ template <int D>
 gqa_status qm_launch(const float* Q, const float* K, const float* V, const float* dO,
                      const float* LSE, const uint32_t* seg, float* dQ, const float* Kt,
                      long long ld_kt, float* Dws, float* Qt, float* dOt, long long ld_qt,
-                     uint32_t* status, const Shape& sh, cudaStream_t st, const RopeParams& rope) {
+                     uint32_t* status, const Shape& sh, cudaStream_t st, const RopeParams& rope,
+                     bool given_d) {
+  if (given_d)
+    return qm_launch_c<D, 1, true>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
   if (cta_group() == 1)
-    return qm_launch_c<D, 1>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
-  return qm_launch_c<D, 2>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
+    return qm_launch_c<D, 1, false>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
+  return qm_launch_c<D, 2, false>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
 }
 
 }  // namespace
@@ -1091,7 +1123,8 @@ bool tc_supported(const Shape& sh) {
 
 gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* dO,
                   const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
-                  const Shape& sh, char* ws, cudaStream_t st, const RopeParams& rope) {
+                  const Shape& sh, char* ws, cudaStream_t st, const RopeParams& rope,
+                  const float* O) {
   const WsLayout L = ws_layout(sh.S, sh.H);
   const TcWsLayout T = tc_ws_layout(sh.S, sh.H, sh.Hk, sh.d);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
@@ -1107,20 +1140,30 @@ gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* d
   // K^T for the query-major kernel; Q^T and dO^T are written by the
   // query-major kernel itself for the key-major one
   if ((r = transpose_launch(K, Kt, sh.S, sh.Hk, 1, sh.d, T.ld_kt, st)) != GQA_OK) return r;
+  // with O given, D = rowsum(dO * O) replaces the query-major kernel's pass 1
+  if (O != nullptr) {
+    const long long rows = (long long)sh.S * sh.H;
+    row_dot_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(dO, O, Dws, rows, sh.d);
+    note_launch();
+    if ((r = check_launch("row dot (D from O)")) != GQA_OK) return r;
+  }
   profile_before(st, "tc_query_major+tc_key_major");
   switch (sh.d) {
     case 32:
-      r = qm_launch<32>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope);
+      r = qm_launch<32>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope,
+                        O != nullptr);
       if (r == GQA_OK)
         r = km_launch<32>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope);
       break;
     case 64:
-      r = qm_launch<64>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope);
+      r = qm_launch<64>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope,
+                        O != nullptr);
       if (r == GQA_OK)
         r = km_launch<64>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope);
       break;
     default:
-      r = qm_launch<128>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope);
+      r = qm_launch<128>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope,
+                        O != nullptr);
       if (r == GQA_OK)
         r = km_launch<128>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope);
       break;

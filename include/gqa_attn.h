@@ -89,6 +89,23 @@ gqa_status attn_bwd(const float* Q, const float* K, const float* V, const float*
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_bwd_o — attn_bwd for callers that kept the forward output O [seq_len,
+ * n_heads * head_dim] (e.g. from attn_fwd_lse): D_i = sum_j P_ij dP_ij is
+ * formed as the row dot product dO_i . O_i (equal when O and LSE come from
+ * the same forward: O_i = sum_j P_ij v_j; cf. backward_attention.wgsl, where
+ * D is the Pass A row sum), which replaces the query-major kernel's first
+ * pass and its two contractions (S and dP). The pages have no separate
+ * entry point for this; it is this library's addition. Same arguments,
+ * workspace, semantics (+=) and errors as attn_bwd, plus O (non-NULL, 16-byte
+ * aligned). Where the CUDA-core path runs (head_dim not 32/64/128), O is not
+ * read and D is formed as in attn_bwd.
+ */
+gqa_status attn_bwd_o(const float* Q, const float* K, const float* V, const float* dO,
+                      const float* O, const float* LSE, const uint32_t* seg, float* dQ, float* dK,
+                      float* dV, int seq_len, int n_heads, int n_kv_heads, int head_dim,
+                      float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * attn_bwd_rope — attn_bwd followed by the interleaved RoPE backward on the
  * attention gradients of Q and K (the step of a RoPE model: the pages apply
  * rope_q_backward / rope_k_backward of backward_attention.wgsl, and tang

@@ -204,3 +204,41 @@ def test_fused_rope_backward_matches_oracle(ga, S, H, Hk, d, seg_kind, pos):
     assert_parity("dQ", dQ.cpu().numpy() - init[0], want_q - init[0], scale_ref=rv)
     assert_parity("dK", dK.cpu().numpy() - init[1], want_k - init[1], scale_ref=rv)
     assert_parity("dV", dV.cpu().numpy() - init[2], rv)
+
+
+@pytest.mark.parametrize("name", ["causal512", "docs2k", "docs4k"])
+def test_backward_given_o_matches_oracle(ga, name):
+    """attn_bwd_o: D from the row dot dO . O (O from the oracle forward,
+    rounded to fp32) instead of the D pass; same result as attn_bwd."""
+    x, O_ref, _, lse32, (rq, rk, rv) = reference(name)
+    S, H, Hk, d = x["seq_len"], x["n_heads"], x["n_kv_heads"], x["head_dim"]
+    t = {k: _dev(x[k]) for k in ("Q", "K", "V", "dO")}
+    out = [torch.zeros(S, n * d, device="cuda") for n in (H, Hk, Hk)]
+    ws = ga.attn_bwd_o(t["Q"], t["K"], t["V"], t["dO"], _dev(O_ref.astype(np.float32)), _dev(lse32),
+                       _seg_dev(x["seg"]), *out, H, Hk, d, x["scale"])
+    ga.read_device_status(ws)
+    torch.cuda.synchronize()
+    for nm, g, r in (("dQ", out[0], rq), ("dK", out[1], rk), ("dV", out[2], rv)):
+        assert_parity(nm, g.cpu().numpy(), r)
+
+
+@pytest.mark.parametrize("S,H,Hk,d,seg_kind", [(300, 8, 2, 128, "docs"), (129, 4, 2, 32, "nonmonotone"),
+                                               (97, 4, 2, 100, "docs"), (200, 16, 4, 64, "causal")])
+def test_backward_given_o_from_gpu_forward(ga, S, H, Hk, d, seg_kind):
+    """attn_bwd_o fed this library's own forward (O, LSE), on non-zero initial
+    gradients, against the oracle backward with the same fp32 LSE."""
+    x = _edge_inputs(S, H, Hk, d, seg_kind, seed=S * 13 + d)
+    t = {k: _dev(x[k]) for k in ("Q", "K", "V", "dO")}
+    seg = _seg_dev(x["seg"])
+    O, LSE = ga.attn_fwd_lse(t["Q"], t["K"], t["V"], seg, H, Hk, d, x["scale"])
+    torch.cuda.synchronize()
+    lse32 = LSE.cpu().numpy()
+    rq, rk, rv = oracle.bwd(x["Q"], x["K"], x["V"], x["dO"], lse32, x["seg"], H, Hk, d, x["scale"])
+    rng = np.random.default_rng(S)
+    init = [rng.standard_normal(a.shape).astype(np.float32) for a in (rq, rk, rv)]
+    out = [_dev(a) for a in init]
+    ws = ga.attn_bwd_o(t["Q"], t["K"], t["V"], t["dO"], O, LSE, seg, *out, H, Hk, d, x["scale"])
+    ga.read_device_status(ws)
+    torch.cuda.synchronize()
+    for nm, g, r, i0 in (("dQ", out[0], rq, init[0]), ("dK", out[1], rk, init[1]), ("dV", out[2], rv, init[2])):
+        assert_parity(nm, g.cpu().numpy() - i0, r, scale_ref=rv)

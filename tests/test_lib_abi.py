@@ -112,6 +112,22 @@ def test_fused_rope_rejects_bad_arguments(L):
     assert call(S=0) == 0
 
 
+def test_given_o_rejects_bad_arguments(L):
+    def call(S=128, H=4, Hk=2, d=32, ptrs=None, ws_bytes=None):
+        p = [FAKE] * 11 if ptrs is None else ptrs
+        if ws_bytes is None:
+            ws_bytes = L.attn_bwd_workspace_bytes(S, H, Hk, d)
+        return L.attn_bwd_o(*p[:10], S, H, Hk, d, 0.17, p[10], ws_bytes, None)
+    for k in range(11):
+        p = [FAKE] * 11
+        p[k] = None
+        assert call(ptrs=p) == 1
+        p[k] = FAKE + 4
+        assert call(ptrs=p) == 1
+    assert call(H=6, Hk=4) == 1 and call(d=132) == 2 and call(ws_bytes=16) == 1
+    assert call(S=0) == 0
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ga, "_lib", None)
     monkeypatch.setattr(ga, "_LIB_PATH", str(tmp_path / "missing.so"))
