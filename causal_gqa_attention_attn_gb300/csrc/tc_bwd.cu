@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NQ = Cfg::NQ;
   extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ KmBarriers bars;
-  __shared__ float4 meta[2][2][NQ];       // [warpgroup][parity] per column: (lse*log2e, D, query, seg)
+  __shared__ float4 meta[2][2][NQ / 2];   // [warpgroup][block parity] per column: (lse*log2e, D, query, seg)
   if ((smem_u32(smem) & 1023u) != 0) {    // the layout has no alignment slack
     if (threadIdx.x == 0) atomicOr(status, 0x80000000u | kSiteKmLayout);
     return;
@@ -618,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.t_full[b], 1);       // producer warp 1 arms both tiles
       mbar_init(&bars.t_empty[b], 1);
       mbar_init(&bars.s_full[b], 1);
-      mbar_init(&bars.p_ready[b], kComputeWarps / 2);  // the stage's warpgroup
+      mbar_init(&bars.p_ready[b], kComputeWarps);      // both warpgroups
     }
     mbar_init(&bars.acc_done, 1);
     bars.abort = 0;
@@ -767,64 +767,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.k_ready);
     }
+    // Both warpgroups take every block, warpgroup wg the columns
+    // [wg*NQ/2, (wg+1)*NQ/2) of it: the softmax of a block then finishes in
+    // half the time, which is what the MMA warp waits for before dV / dK.
     const float sl2 = sh.scale * kLog2e;
-    const uint32_t ts = tl + Cfg::t_s(wg), tdp = tl + Cfg::t_dp(wg);
-    int n = 0, mine = 0;
+    constexpr int HQ = NQ / 2;
+    static_assert(HQ == 16 || HQ == 32, "column split");
+    int n = 0;
     bool ok = true;
     for (int qb = nqb - 1; qb >= qb0; --qb) {
       if (!visible(qb)) continue;
-      if ((n++ & 1) != wg) continue;
-      const int par = mine & 1;
-      // column metadata of this block (double-buffered per warpgroup; one named barrier per block)
-      if (wt < NQ) {
-        const int q = qb * QB + wt / G, h = g * G + wt % G;
+      const int b = n & 1;
+      // this warpgroup's columns' metadata (double-buffered; one named barrier per block)
+      if (wt < HQ) {
+        const int col = wg * HQ + wt;
+        const int q = qb * QB + col / G, h = g * G + col % G;
         float4 m = make_float4(0.f, 0.f, __int_as_float(-1), __int_as_float(0x7fffffff));
         if (q < S)
           m = make_float4(__ldg(LSE + (long long)q * H + h) * kLog2e, Dws[(long long)q * H + h],
                           __int_as_float(q), __int_as_float((int)__ldg(seg + q)));
-        meta[wg][par][wt] = m;
+        meta[wg][b][wt] = m;
       }
       asm volatile("bar.sync %0, 128;" ::"r"(1 + wg) : "memory");
-      if (!mbar_wait(&bars.s_full[wg], mine & 1, abort, status, kSiteKmCompute)) { ok = false; break; }
+      if (!mbar_wait(&bars.s_full[b], (n >> 1) & 1, abort, status, kSiteKmCompute)) { ok = false; break; }
       tc_fence_after();
       // every (key, column) of the block visible: key <= first query and >= every seg
       const int q_first = qb * QB;
       const bool full = key <= q_first && key >= (int)__ldg(blk_maxseg + qb) &&
                         q_first + QB - 1 < S;
-      const float4* mt = meta[wg][par];
+      const float4* mt = meta[wg][b];
+      const uint32_t ts = tl + Cfg::t_s(b) + wg * HQ, tdp = tl + Cfg::t_dp(b) + wg * HQ;
+      float sv[HQ], dp[HQ];
+      if constexpr (HQ == 16) {
+        tmem_ld16(ts, sv);
+        tmem_ld16(tdp, dp);
+      } else {
+        tmem_ld32(ts, sv);
+        tmem_ld32(tdp, dp);
+      }
+      tmem_ld_wait();
+      if (full) {
 #pragma unroll
-      for (int cb = 0; cb < NQ; cb += 32) {
-        float sv[32], dp[32];
-        tmem_ld32(ts + cb, sv);
-        tmem_ld32(tdp + cb, dp);
-        tmem_ld_wait();
-        if (full) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float4 m = mt[cb + j];
-            const float pj = ex2(fmaf(sv[j], sl2, -m.x));
-            sv[j] = to_tf32(pj);
-            dp[j] = to_tf32(sh.scale * pj * (dp[j] - m.y));
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float4 m = mt[cb + j];
-            const int q = __float_as_int(m.z), sq = __float_as_int(m.w);
-            const bool vis = key <= q && key >= sq;        // q = -1 for padding columns
-            const float pj = vis ? ex2(fmaf(sv[j], sl2, -m.x)) : 0.f;
-            sv[j] = to_tf32(pj);
-            dp[j] = to_tf32(sh.scale * pj * (dp[j] - m.y));
-          }
+        for (int j = 0; j < HQ; ++j) {
+          const float4 m = mt[j];
+          const float pj = ex2(fmaf(sv[j], sl2, -m.x));
+          sv[j] = to_tf32(pj);
+          dp[j] = to_tf32(sh.scale * pj * (dp[j] - m.y));
         }
-        tmem_st32(ts + cb, sv);
-        tmem_st32(tdp + cb, dp);
+      } else {
+#pragma unroll
+        for (int j = 0; j < HQ; ++j) {
+          const float4 m = mt[j];
+          const int q = __float_as_int(m.z), sq = __float_as_int(m.w);
+          const bool vis = key <= q && key >= sq;        // q = -1 for padding columns
+          const float pj = vis ? ex2(fmaf(sv[j], sl2, -m.x)) : 0.f;
+          sv[j] = to_tf32(pj);
+          dp[j] = to_tf32(sh.scale * pj * (dp[j] - m.y));
+        }
+      }
+      if constexpr (HQ == 16) {
+        tmem_st16(ts, sv);
+        tmem_st16(tdp, dp);
+      } else {
+        tmem_st32(ts, sv);
+        tmem_st32(tdp, dp);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.p_ready[wg]);
-      ++mine;
+      if (lane == 0) mbar_arrive(&bars.p_ready[b]);
+      ++n;
     }
     // epilogue: warpgroup 0 adds dK (rotated by the RoPE backward of the key's
     // position when rope.on), warpgroup 1 adds dV (owned rows, NaN-guarded)
