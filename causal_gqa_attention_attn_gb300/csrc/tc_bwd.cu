@@ -1050,15 +1050,13 @@ gqa_status transpose_launch(const float* X, float* Xt, int S, int Hk, int Gx, in
   return check_launch("group transpose");
 }
 
-// CTA group of the query-major kernel: 1 (one SM per slab) by default;
-// GQA_TC_CTA_GROUP=2 runs it on SM pairs (cta_group::2). The pair halves the
-// shared-memory traffic per SM but measured slower on this part: its
-// cross-SM handshakes (forwarded copy completions, the dS hand-back) add
-// ~800 cycles per step that two TMEM stages cannot hide. Read once per process.
+// CTA group of the query-major kernel: 2 (SM pairs,
+// cta_group::2: half the shared-memory traffic per SM per flop) by default;
+// GQA_TC_CTA_GROUP=1 selects one SM per slab. Read once per process.
 int cta_group() {
   static int c = [] {
     const char* e = getenv("GQA_TC_CTA_GROUP");
-    return (e != nullptr && atoi(e) == 2) ? 2 : 1;
+    return (e != nullptr && atoi(e) == 1) ? 1 : 2;
   }();
   return c;
 }
@@ -1093,8 +1091,11 @@ gqa_status qm_launch(const float* Q, const float* K, const float* V, const float
                      long long ld_kt, float* Dws, float* Qt, float* dOt, long long ld_qt,
                      uint32_t* status, const Shape& sh, cudaStream_t st, const RopeParams& rope,
                      bool given_d) {
-  if (given_d)
-    return qm_launch_c<D, 1, true>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
+  if (given_d) {
+    if (cta_group() == 1)
+      return qm_launch_c<D, 1, true>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
+    return qm_launch_c<D, 2, true>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
+  }
   if (cta_group() == 1)
     return qm_launch_c<D, 1, false>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
   return qm_launch_c<D, 2, false>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);

@@ -168,9 +168,18 @@ __device__ __forceinline__ uint32_t mapa_u32(const void* p, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
   return r;
 }
-// Arrive (release at cluster scope) on the mbarrier at a shared::cluster address.
+// Arrive on the mbarrier at a shared::cluster address (the other CTA of a
+// pair), relaxed. Every use hands over data that is already complete before
+// the arrive issues and is read only by tcgen05 MMAs issued after the waiter
+// observes the phase: TMEM written or read by the sender is finished
+// (tcgen05.wait::st / ::ld, then tcgen05.fence::before_thread_sync), or the
+// sender observed its own TMA barrier complete; the receiver issues the MMA
+// after tcgen05.fence::after_thread_sync. The arrive orders execution only,
+// and carries no data. (A release arrive to the other CTA of the pair cost
+// ~320 cycles of blocking on this part, a relaxed one ~5; the release cost
+// is what made the SM-pair kernel slower than one SM.)
 __device__ __forceinline__ void mbar_arrive_cl(uint32_t bar_cl) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cl)
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cl)
                : "memory");
 }
 

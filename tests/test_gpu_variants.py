@@ -1,5 +1,5 @@
-"""The query-major kernel runs one SM per slab by default; GQA_TC_CTA_GROUP=2
-selects the SM-pair variant (cta_group::2, M = 256). The group size is read
+"""The query-major kernel runs on SM pairs (cta_group::2, M = 256) by default;
+GQA_TC_CTA_GROUP=1 selects the one-SM-per-slab variant. The group size is read
 once per process, so the variant runs in a child process, against the oracle
 on edge shapes (ragged tails, documents, all head dims)."""
 import os
@@ -36,13 +36,13 @@ print("ok")
 """
 
 
-def test_sm_pair_query_major_matches_oracle():
+def test_single_sm_query_major_matches_oracle():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from causal_gqa_attention_attn_gb300 import build
     build.build()
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, GQA_TC_CTA_GROUP="2")
+    env = dict(os.environ, GQA_TC_CTA_GROUP="1")
     p = subprocess.run([sys.executable, "-c", _SCRIPT.format(root=root)], env=env,
                        capture_output=True, text=True, timeout=600)
     assert p.returncode == 0 and "ok" in p.stdout, p.stdout + p.stderr
