@@ -220,7 +220,7 @@ def run_gpu(args) -> dict | None:
             for k in ("Q", "K", "V", "dO")}
     host["seg"] = torch.from_numpy(x["seg"].astype(np.int32)).pin_memory()
     t = {k: v.to(dev) for k, v in host.items()}
-    _, LSE = ga.attn_fwd_lse(t["Q"], t["K"], t["V"], t["seg"], H, Hk, d, sc)   # setup, untimed
+    _, LSE = ga.attn_fwd(t["Q"], t["K"], t["V"], t["seg"], H, Hk, d, sc)   # setup, untimed
     host["LSE"] = LSE.cpu().pin_memory()
     t["LSE"] = LSE
     dQ = torch.zeros(S, H * d, device=dev)
@@ -231,7 +231,7 @@ def run_gpu(args) -> dict | None:
     fused_rope = w.rope and args.path == "auto" and not args.given_o
     O_dev = None
     if args.given_o:       # the forward output O, as a training step keeps it (setup, untimed)
-        O_dev, _ = ga.attn_fwd_lse(t["Q"], t["K"], t["V"], t["seg"], H, Hk, d, sc)
+        O_dev, _ = ga.attn_fwd(t["Q"], t["K"], t["V"], t["seg"], H, Hk, d, sc)
 
     def step():
         dQ.zero_()

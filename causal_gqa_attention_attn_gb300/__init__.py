@@ -47,6 +47,9 @@ def lib() -> ctypes.CDLL:
     L = ctypes.CDLL(_LIB_PATH)
     P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.attn_fwd_lse.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P]
+    L.attn_fwd.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
+    L.attn_fwd_workspace_bytes.argtypes = [I, I, I, I]
+    L.attn_fwd_workspace_bytes.restype = Z
     bwd_args = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
     L.attn_bwd.argtypes = bwd_args
     L.attn_bwd_simt.argtypes = bwd_args
@@ -70,7 +73,7 @@ def lib() -> ctypes.CDLL:
     L.gqa_launch_count.restype = ctypes.c_ulonglong
     L.gqa_last_error.argtypes = []
     L.gqa_last_error.restype = ctypes.c_char_p
-    for name in ("attn_fwd_lse", "attn_bwd", "attn_bwd_simt", "attn_bwd_rope", "attn_bwd_o",
+    for name in ("attn_fwd_lse", "attn_fwd", "attn_bwd", "attn_bwd_simt", "attn_bwd_rope", "attn_bwd_o",
                  "rope_bwd_inplace", "attn_read_device_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -131,6 +134,27 @@ def attn_fwd_lse(Q, K, V, seg, n_heads, n_kv_heads, head_dim, scale, O=None, LSE
     _check(lib().attn_fwd_lse(_f32(Q, "Q"), _f32(K, "K"), _f32(V, "V"), _seg(seg), _f32(O, "O"),
                               _f32(LSE, "LSE"), S, n_heads, n_kv_heads, head_dim, float(scale),
                               _stream(stream)))
+    return O, LSE
+
+
+def attn_fwd(Q, K, V, seg, n_heads, n_kv_heads, head_dim, scale, O=None, LSE=None,
+             workspace=None, stream=None):
+    """Forward attention on tensor cores where the shape allows: returns (O, LSE).
+    Pass `workspace` (attn_fwd_workspace_bytes) to reuse it or to read the
+    device status afterwards (read_device_status)."""
+    torch = _torch()
+    S = Q.shape[0]
+    if O is None:
+        O = torch.empty(S, n_heads * head_dim, device=Q.device, dtype=torch.float32)
+    if LSE is None:
+        LSE = torch.empty(S, n_heads, device=Q.device, dtype=torch.float32)
+    need = int(lib().attn_fwd_workspace_bytes(S, n_heads, n_kv_heads, head_dim))
+    if workspace is None:
+        workspace = torch.empty(need, device=Q.device, dtype=torch.uint8)
+    _check(lib().attn_fwd(_f32(Q, "Q"), _f32(K, "K"), _f32(V, "V"), _seg(seg), _f32(O, "O"),
+                          _f32(LSE, "LSE"), S, n_heads, n_kv_heads, head_dim, float(scale),
+                          _ptr(workspace, "workspace", (torch.uint8,)), workspace.numel(),
+                          _stream(stream)))
     return O, LSE
 
 

@@ -129,6 +129,32 @@ gqa_status attn_fwd_lse(const float* Q, const float* K, const float* V, const ui
   return simt_fwd_lse(Q, K, V, seg, O, LSE, sh, (cudaStream_t)stream);
 }
 
+size_t attn_fwd_workspace_bytes(int seq_len, int n_heads, int n_kv_heads, int head_dim) {
+  if (seq_len <= 0 || n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads) return kWsHeader;
+  const Shape sh{seq_len, n_heads, n_kv_heads, head_dim, n_heads / n_kv_heads, 1.f};
+  if (tc_fwd_supported(sh)) return tc_fwd_ws_bytes(seq_len, n_kv_heads, head_dim);
+  return kWsHeader;
+}
+
+gqa_status attn_fwd(const float* Q, const float* K, const float* V, const uint32_t* seg, float* O,
+                    float* LSE, int seq_len, int n_heads, int n_kv_heads, int head_dim, float scale,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  gqa_status r = check_attn_args(seq_len, n_heads, n_kv_heads, head_dim, scale, 128);
+  if (r != GQA_OK || seq_len == 0) return r;
+  const void* p[] = {Q, K, V, seg, O, LSE, workspace};
+  const char* nm[] = {"Q", "K", "V", "seg", "O", "LSE", "workspace"};
+  if ((r = check_ptrs(p, nm, 7)) != GQA_OK) return r;
+  const size_t need = attn_fwd_workspace_bytes(seq_len, n_heads, n_kv_heads, head_dim);
+  if (workspace_bytes < need)
+    return set_error(GQA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  const Shape sh{seq_len, n_heads, n_kv_heads, head_dim, n_heads / n_kv_heads, scale};
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
+    return check_launch("workspace header reset");
+  if (!tc_fwd_supported(sh)) return simt_fwd_lse(Q, K, V, seg, O, LSE, sh, st);
+  return tc_fwd(Q, K, V, seg, O, LSE, sh, (char*)workspace, st);
+}
+
 gqa_status attn_bwd_simt(const float* Q, const float* K, const float* V, const float* dO,
                          const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
                          int seq_len, int n_heads, int n_kv_heads, int head_dim, float scale,

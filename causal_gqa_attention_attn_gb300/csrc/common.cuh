@@ -1,6 +1,7 @@
 // Internal definitions shared by the translation units of libgqa_attn.so.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stddef.h>
@@ -111,6 +112,22 @@ gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* d
                   const float* O = nullptr);
 
 gqa_status wait_selftest(void* workspace, long long limit_cycles, cudaStream_t st);
+
+// Tensor-core host helpers (tc_bwd.cu): the 128-byte-swizzled panel view of a
+// row-major matrix (dims 32 floats x rows x panels; one box fills box_panels
+// panels of box_rows x 128 B) and the group transpose Xt [Hk*d][ld] of
+// X [S][Hk*Gx][d].
+gqa_status tc_map_panels(CUtensorMap* m, const float* base, long long ld, long long rows,
+                         long long n_panels, int box_rows, int box_panels);
+gqa_status tc_transpose(const float* X, float* Xt, int S, int Hk, int Gx, int d, long long ld,
+                        cudaStream_t st);
+
+// Tensor-core forward, tc_fwd.cu: O and LSE (d in {32, 64, 128}); the
+// workspace holds the status header and V^T.
+bool tc_fwd_supported(const Shape& sh);
+size_t tc_fwd_ws_bytes(int S, int Hk, int d);
+gqa_status tc_fwd(const float* Q, const float* K, const float* V, const uint32_t* seg, float* O,
+                  float* LSE, const Shape& sh, char* ws, cudaStream_t st);
 
 // RoPE backward, rope_bwd.cu
 gqa_status rope_bwd_launch(float* X, int S, int H, int d, int pos_offset, float base,

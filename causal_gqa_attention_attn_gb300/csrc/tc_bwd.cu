@@ -1111,6 +1111,16 @@ gqa_status wait_selftest(void* workspace, long long limit_cycles, cudaStream_t s
   return check_launch("wait self-test");
 }
 
+gqa_status tc_map_panels(CUtensorMap* m, const float* base, long long ld, long long rows,
+                         long long n_panels, int box_rows, int box_panels) {
+  return map_panels(m, base, ld, rows, n_panels, box_rows, box_panels);
+}
+
+gqa_status tc_transpose(const float* X, float* Xt, int S, int Hk, int Gx, int d, long long ld,
+                        cudaStream_t st) {
+  return transpose_launch(X, Xt, S, Hk, Gx, d, ld, st);
+}
+
 TcWsLayout tc_ws_layout(int S, int H, int Hk, int d) {
   TcWsLayout t;
   const WsLayout base = ws_layout(S, H);

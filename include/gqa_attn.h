@@ -56,10 +56,26 @@ typedef enum {
  *   O[i, h]   = sum_j exp(scale*q_i.k_j - LSE[i,h]) v_j   over visible j
  *   LSE[i, h] = ln sum_j exp(scale*q_i.k_j)               (natural log, scale in)
  * In:  Q, K, V, seg. Out (overwritten): O, LSE. head_dim: 4..128, multiple of 4.
+ * fp32 on CUDA cores; needs no workspace (attn_fwd is the tensor-core form).
  */
 gqa_status attn_fwd_lse(const float* Q, const float* K, const float* V, const uint32_t* seg,
                         float* O, float* LSE, int seq_len, int n_heads, int n_kv_heads,
                         int head_dim, float scale, void* stream);
+
+/*
+ * attn_fwd_workspace_bytes / attn_fwd — the same forward as attn_fwd_lse (O
+ * and LSE overwritten, same definitions and arguments), on tensor cores for
+ * head_dim 32, 64, 128 (tcgen05 kind::tf32: S = scale Q.K^T with TF32
+ * operands, fp32 accumulation; LSE from a first pass over the keys, then O =
+ * sum_j exp(s_ij - LSE) v_j with P rounded to TF32), else on CUDA cores.
+ * workspace: >= attn_fwd_workspace_bytes(...) device bytes, caller-owned (a
+ * status header and a transposed copy of V). Bounded device waits report
+ * through attn_read_device_status(workspace) as for attn_bwd.
+ */
+size_t attn_fwd_workspace_bytes(int seq_len, int n_heads, int n_kv_heads, int head_dim);
+gqa_status attn_fwd(const float* Q, const float* K, const float* V, const uint32_t* seg, float* O,
+                    float* LSE, int seq_len, int n_heads, int n_kv_heads, int head_dim, float scale,
+                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * attn_bwd_workspace_bytes — bytes of device workspace attn_bwd needs for this

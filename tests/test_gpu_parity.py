@@ -97,15 +97,43 @@ def test_backward_matches_oracle(ga, name, fn):
     assert_parity("dV", dV, rv)
 
 
-@pytest.mark.parametrize("name", ["tiny", "causal512", "docs2k", "docs4k"])
-def test_forward_matches_oracle(ga, name):
-    x, O_ref, lse_ref, _, _ = reference(name)
-    H, Hk, d = x["n_heads"], x["n_kv_heads"], x["head_dim"]
-    O, LSE = ga.attn_fwd_lse(_dev(x["Q"]), _dev(x["K"]), _dev(x["V"]), _seg_dev(x["seg"]),
-                             H, Hk, d, x["scale"])
+def gpu_fwd(ga, fn, x):
+    """The forward through attn_fwd (tensor cores where built; device status
+    checked) or attn_fwd_lse (CUDA cores, no workspace)."""
+    S, H, Hk, d = x["seq_len"], x["n_heads"], x["n_kv_heads"], x["head_dim"]
+    args = (_dev(x["Q"]), _dev(x["K"]), _dev(x["V"]), _seg_dev(x["seg"]), H, Hk, d, x["scale"])
+    if fn == "attn_fwd":
+        ws = torch.empty(int(ga.lib().attn_fwd_workspace_bytes(S, H, Hk, d)), dtype=torch.uint8,
+                         device="cuda")
+        O, LSE = ga.attn_fwd(*args, workspace=ws)
+        ga.read_device_status(ws)
+    else:
+        O, LSE = ga.attn_fwd_lse(*args)
     torch.cuda.synchronize()
-    assert_parity("O", O.cpu().numpy(), O_ref)
-    assert_parity("LSE", LSE.cpu().numpy(), lse_ref)
+    return O.cpu().numpy(), LSE.cpu().numpy()
+
+
+@pytest.mark.parametrize("fn", ["attn_fwd", "attn_fwd_lse"])
+@pytest.mark.parametrize("name", ["tiny", "causal512", "docs2k", "docs4k"])
+def test_forward_matches_oracle(ga, name, fn):
+    x, O_ref, lse_ref, _, _ = reference(name)
+    O, LSE = gpu_fwd(ga, fn, x)
+    assert_parity("O", O, O_ref)
+    assert_parity("LSE", LSE, lse_ref)
+
+
+@pytest.mark.parametrize("S,H,Hk,d,seg_kind", [
+    (1, 4, 2, 32, "causal"), (65, 8, 2, 128, "docs"), (127, 4, 1, 32, "nonmonotone"),
+    (129, 6, 3, 64, "docs"), (333, 16, 2, 64, "nonmonotone"), (97, 4, 2, 100, "docs"),
+    (300, 8, 1, 128, "docs"), (513, 4, 2, 32, "docs"), (200, 32, 1, 128, "causal")])
+def test_forward_edge_shapes(ga, S, H, Hk, d, seg_kind):
+    """attn_fwd on ragged tails, documents, non-monotone seg, G up to 32, the
+    CUDA-core fallback (d = 100) and seq_len 1."""
+    x = _edge_inputs(S, H, Hk, d, seg_kind, seed=S * 17 + d)
+    O_ref, lse_ref = oracle.fwd(x["Q"], x["K"], x["V"], x["seg"], H, Hk, d, x["scale"])
+    O, LSE = gpu_fwd(ga, "attn_fwd", x)
+    assert_parity("O", O, O_ref)
+    assert_parity("LSE", LSE, lse_ref)
 
 
 def _edge_inputs(S, H, Hk, d, seg_kind, seed):

@@ -128,6 +128,23 @@ def test_given_o_rejects_bad_arguments(L):
     assert call(S=0) == 0
 
 
+def test_tensor_core_forward_rejects_bad_arguments(L):
+    def call(S=128, H=4, Hk=2, d=32, s=0.2, ptrs=None, ws_bytes=None):
+        p = [FAKE] * 7 if ptrs is None else ptrs
+        if ws_bytes is None:
+            ws_bytes = L.attn_fwd_workspace_bytes(S, H, Hk, d)
+        return L.attn_fwd(*p[:6], S, H, Hk, d, s, p[6], ws_bytes, None)
+    assert call(H=5) == 1 and call(d=136) == 2 and call(S=-3) == 1 and call(S=0) == 0
+    assert call(s=float("inf")) == 1 and call(ws_bytes=16) == 1
+    for k in range(7):
+        p = [FAKE] * 7
+        p[k] = None
+        assert call(ptrs=p) == 1
+    # tensor-core shapes need the V^T copy; other head dims only the header
+    assert L.attn_fwd_workspace_bytes(4096, 32, 8, 128) >= 256 + 8 * 128 * 4096 * 4
+    assert L.attn_fwd_workspace_bytes(4096, 32, 8, 100) == 256
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ga, "_lib", None)
     monkeypatch.setattr(ga, "_LIB_PATH", str(tmp_path / "missing.so"))
