@@ -530,40 +530,55 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   P^T, dS^T = scale P (dP - D) written back to TMEM over S^T / dP^T
 //   dV  += P^T . dO       A = P^T (TMEM),  B = dO^T block (smem, K-major copy)
 //   dK  += dS^T . Q       A = dS^T (TMEM), B = Q^T block  (smem, K-major copy)
-// Blocks alternate between two TMEM stages, and compute warpgroup w handles
-// the blocks of stage w, so block n's softmax runs while the tensor core does
-// S^T / dP^T of block n+1 and dV / dK of block n-1. Q / dO blocks go through
-// three shared-memory stages and Q^T / dO^T blocks through two: a block's
-// copies take ~3000 cycles to land while the tensor core is busy, and three
-// stages of the first-needed tiles cover that. Blocks are visited from the end of the sequence down to the
-// tile's first query: CTAs that run at the same time then read the same
-// blocks at about the same time, so the per-group Q / dO / Q^T / dO^T stream
-// (larger than L2 at 16k tokens) is served mostly from L2.
+// Blocks alternate between two TMEM stages, so block n's softmax runs while
+// the tensor core does S^T / dP^T of block n+1 and dV / dK of block n-1; both
+// compute warpgroups take every block, half its columns each. Q / dO blocks
+// and Q^T / dO^T blocks stream through their own shared-memory stages (a
+// block's copies take thousands of cycles to land while the tensor core is
+// busy). Blocks are visited from the end of the sequence down to the tile's
+// first query: CTAs that run at the same time then read the same blocks at
+// about the same time, so the per-group Q / dO / Q^T / dO^T stream (larger
+// than L2 at 16k tokens) is served mostly from L2.
+//
+// C = CTA group. With C = 2 an SM pair takes two adjacent key tiles (M = 256)
+// with cta_group::2 MMAs: each CTA stages half of every B operand (NQ/2
+// columns of a Q / dO block, d/2 rows of a Q^T / dO^T block), which halves
+// the TMA writes and the B-operand reads per SM. Those, with the reads of V
+// as the A operand of dP^T, are what limits the one-SM kernel: its
+// shared-memory traffic per block is about twice what the tensor core needs
+// of it per flop. The pair walks the union of the two tiles' query blocks.
+// The odd CTA's MMA warp forwards each of its landed copies to the even
+// (issuing) CTA, in the order the issuer consumes them.
 // ---------------------------------------------------------------------------
-template <int D_>
+template <int D_, int C_>
 struct KmCfg {
-  static constexpr int D = D_;
+  static constexpr int D = D_, C = C_;
   static constexpr int NQ = (D == 128) ? 32 : 64;         // (query, head) columns per block
+  static constexpr int NQH = NQ / C;                      // this CTA's columns of a Q / dO block
+  static constexpr int DH = D / C;                        // this CTA's rows of a Q^T / dO^T block
   static constexpr int V_PANEL_BYTES = 128 * 128;         // 128 keys x 32 floats
   static constexpr int V_BYTES = (D / 32) * V_PANEL_BYTES;
-  static constexpr int BLK_PANEL_BYTES = NQ * 128;        // Q / dO block panel: NQ rows x 32 floats
+  static constexpr int BLK_PANEL_BYTES = NQH * 128;       // Q / dO block panel: NQH rows x 32 floats
   static constexpr int BLK_BYTES = (D / 32) * BLK_PANEL_BYTES;
-  static constexpr int T_PANEL_BYTES = D * 128;           // Q^T / dO^T panel: d rows x 32 columns
+  static constexpr int T_PANEL_BYTES = DH * 128;          // Q^T / dO^T panel: d/C rows x 32 columns
   static constexpr int T_PANELS = NQ / 32;
   static_assert(T_PANELS * T_PANEL_BYTES == BLK_BYTES, "transposed block size");
   static_assert(BLK_PANEL_BYTES % 1024 == 0 && T_PANEL_BYTES % 1024 == 0,
                 "panels must keep 1 KB swizzle alignment");
-  // shared memory: V | Q dO stages 0-2 | Q^T dO^T stages 0-1. The kernel
-  // needs the dynamic shared memory 1 KB aligned (it checks and reports an
-  // error otherwise) and takes no slack: at d = 128 the layout is 224 KB.
-  static constexpr int NSQ = 3, NST = 2;
+  // shared memory: V | Q dO stages | Q^T dO^T stages. With C = 1 the layout
+  // is 224 KB at d = 128 and has no alignment slack (the kernel checks that
+  // its dynamic shared memory starts 1 KB aligned and reports an error
+  // otherwise); with C = 2 the halved blocks leave room for deeper staging
+  // and the slack.
+  static constexpr int NSQ = (C == 1) ? 3 : 4, NST = (C == 1) ? 2 : 4;
+  static constexpr int SLACK = (C == 1) ? 0 : 1024;
   static constexpr int OFF_V = 0, OFF_QDO = V_BYTES, OFF_T = OFF_QDO + NSQ * 2 * BLK_BYTES;
   static constexpr int off_q(int b) { return OFF_QDO + b * 2 * BLK_BYTES; }
   static constexpr int off_do(int b) { return OFF_QDO + b * 2 * BLK_BYTES + BLK_BYTES; }
   static constexpr int off_qt(int b) { return OFF_T + b * 2 * BLK_BYTES; }
   static constexpr int off_dot(int b) { return OFF_T + b * 2 * BLK_BYTES + BLK_BYTES; }
   static constexpr int END = OFF_T + NST * 2 * BLK_BYTES;
-  static constexpr int SMEM_BYTES = (END > 120 * 1024) ? END : 120 * 1024;
+  static constexpr int SMEM_BYTES = (END + SLACK > 120 * 1024) ? END + SLACK : 120 * 1024;
   static_assert(SMEM_BYTES <= 224 * 1024, "shared memory budget (with the static barriers)");
   // TMEM columns: K | dK | dV | stage 0: S^T dP^T | stage 1: S^T dP^T
   static constexpr uint32_t T_K = 0, T_DK = D, T_DV = 2 * D;
@@ -573,15 +588,49 @@ struct KmCfg {
 };
 
 struct KmBarriers {
-  uint64_t v_full, k_ready;
-  uint64_t qdo_full[3], qdo_empty[3];     // Q, dO blocks of each stage
-  uint64_t t_full[2], t_empty[2];         // Q^T, dO^T blocks of each stage
+  uint64_t v_full, peer_v, k_ready;
+  uint64_t qdo_full[4], qdo_empty[4], peer_qdo[4];   // Q, dO blocks of each stage
+  uint64_t t_full[4], t_empty[4], peer_t[4];         // Q^T, dO^T blocks of each stage
   uint64_t s_full[2], p_ready[2], acc_done;
   uint32_t tmem_base;
   int abort;
 };
 
-template <int D>
+// Visible query blocks of a key tile (or of an SM pair's two tiles), from the
+// last block down to qb0, found 32 at a time: lane i of the warp tests block
+// base - i and a ballot gives every lane the batch's mask. The next batch's
+// per-block loads are issued a batch ahead, so no loop waits on them.
+// Every lane of the warp calls next() together.
+struct BlockWalk {
+  const uint32_t* minseg;
+  unsigned k_hi;
+  int qb0, base;
+  uint32_t mask;
+  unsigned pend;   // this lane's min seg of the batch below `base`, in flight
+  __device__ unsigned load(int b) const {
+    const int qb = b - (int)(threadIdx.x % 32);
+    return qb >= qb0 ? __ldg(minseg + qb) : 0xffffffffu;
+  }
+  __device__ BlockWalk(const uint32_t* m, unsigned kh, int q0, int nqb)
+      : minseg(m), k_hi(kh), qb0(q0), base(nqb - 1) {
+    mask = __ballot_sync(0xffffffffu, load(base) <= k_hi);
+    pend = load(base - 32);
+  }
+  // next visible block, or -1 after the last
+  __device__ int next() {
+    while (mask == 0) {
+      base -= 32;
+      if (base < qb0) return -1;
+      mask = __ballot_sync(0xffffffffu, pend <= k_hi);
+      pend = load(base - 32);
+    }
+    const int i = __ffs(mask) - 1;
+    mask &= mask - 1;
+    return base - i;
+  }
+};
+
+template <int D, int C>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_key_major(const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapQ,
                  const __grid_constant__ CUtensorMap mapDO, const __grid_constant__ CUtensorMap mapQt,
@@ -591,54 +640,73 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const uint32_t* __restrict__ blk_maxseg, float* __restrict__ dK,
                  float* __restrict__ dV, uint32_t* __restrict__ status, Shape sh,
                  const RopeParams rope) {
-  using Cfg = KmCfg<D>;
+  using Cfg = KmCfg<D, C>;
   constexpr int NQ = Cfg::NQ;
-  extern __shared__ __align__(1024) unsigned char smem[];
+  constexpr bool kCl = C > 1;
+  static_assert(Cfg::NSQ <= 4 && Cfg::NST <= 4, "barrier arrays");
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ KmBarriers bars;
   __shared__ float4 meta[2][2][NQ / 2];   // [warpgroup][block parity] per column: (lse*log2e, D, query, seg)
-  if ((smem_u32(smem) & 1023u) != 0) {    // the layout has no alignment slack
-    if (threadIdx.x == 0) atomicOr(status, 0x80000000u | kSiteKmLayout);
-    return;
+  unsigned char* smem = smem_raw;
+  if constexpr (C == 1) {
+    if ((smem_u32(smem) & 1023u) != 0) {  // the layout has no alignment slack
+      if (threadIdx.x == 0) atomicOr(status, 0x80000000u | kSiteKmLayout);
+      return;
+    }
+  } else {
+    // the same offset in both CTAs of the pair (same kernel, same static layout)
+    smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~uintptr_t(1023));
   }
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int G = sh.G, QB = NQ / G;        // queries per block
   const int S = sh.S, H = sh.H;
+  const uint32_t rank = (C > 1) ? cluster_ctarank() : 0u;
+  const bool issuer = rank == 0;          // issues the group's MMAs
   const int k0 = blockIdx.x * 128, g = blockIdx.y;
-  const int k_hi = min(k0 + 128, S) - 1;
-  const int qb0 = k0 / QB, nqb = (S + QB - 1) / QB;
+  const int kg0 = ((int)blockIdx.x - (int)rank) * 128;   // the group's first key
+  const int k_hi = min(kg0 + 128 * C, S) - 1;             // the group's last key
+  const int qb0 = kg0 / QB, nqb = (S + QB - 1) / QB;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.v_full, 1);
-    mbar_init(&bars.k_ready, kComputeWarps);
+    mbar_init(&bars.peer_v, 1);
+    mbar_init(&bars.k_ready, C * kComputeWarps);          // every compute warp of each CTA
     for (int b = 0; b < Cfg::NSQ; ++b) {
       mbar_init(&bars.qdo_full[b], 1);     // producer warp 0 arms both tiles
-      mbar_init(&bars.qdo_empty[b], 1);
+      mbar_init(&bars.qdo_empty[b], 1);    // released by the issuer's MMA commit
+      mbar_init(&bars.peer_qdo[b], 1);     // C = 2: the odd CTA's tiles landed (forwarded)
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < Cfg::NST; ++b) {
       mbar_init(&bars.t_full[b], 1);       // producer warp 1 arms both tiles
       mbar_init(&bars.t_empty[b], 1);
+      mbar_init(&bars.peer_t[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&bars.s_full[b], 1);
-      mbar_init(&bars.p_ready[b], kComputeWarps);      // both warpgroups
+      mbar_init(&bars.p_ready[b], C * kComputeWarps);
     }
     mbar_init(&bars.acc_done, 1);
     bars.abort = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(&bars.tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_g<C>(&bars.tmem_base, kTmemCols);
+    tmem_relinquish_g<C>();
   }
   tc_fence_before();
   __syncthreads();
+  if (C > 1) cluster_sync();   // the issuer's barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort = &bars.abort;
-  auto visible = [&](int qb) { return __ldg(blk_minseg + qb) <= (unsigned)k_hi; };
+  BlockWalk walk(blk_minseg, (unsigned)k_hi, qb0, nqb);
 
   if (warp < kProducerWarps) {
     // ---------------- TMA producers: warp 0 loads Q and dO, warp 1 Q^T, dO^T and V ----------------
-    // Each warp waits only for its own tiles' release: Q / dO of stage b are
-    // free once S^T / dP^T of block n-2 ran, Q^T / dO^T once its dV / dK ran.
+    // Each warp waits only for its own tiles' release: Q / dO of a stage are
+    // free once its S^T / dP^T ran, Q^T / dO^T once its dV / dK ran. With
+    // C = 2 this CTA loads its half of each block.
     const int pw = warp;
     if (elect_one()) {
       if (pw == 0) {
@@ -657,93 +725,124 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* empty = pw == 0 ? bars.qdo_empty : bars.t_empty;
     const int ns = pw == 0 ? Cfg::NSQ : Cfg::NST;      // this warp's stages
     int n = 0;
-    for (int qb = nqb - 1; qb >= qb0; --qb) {
-      if (!visible(qb)) continue;
+    for (int qb = walk.next(); qb >= 0; qb = walk.next()) {
       const int b = n % ns;
       const int q0 = qb * QB;
-      if (n >= ns && !warp_wait(&empty[b], ((n / ns) - 1) & 1, abort, status, kSiteKmProducer)) break;
+      if (n >= ns && !warp_wait<kCl>(&empty[b], ((n / ns) - 1) & 1, abort, status, kSiteKmProducer)) break;
       if (elect_one()) {
         mbar_arrive_expect_tx(&full[b], 2 * Cfg::BLK_BYTES);
-        if (pw == 0) {   // 4-D boxes (32 dims, G heads, QB queries, d/32 panels)
-          tma_load_4d(smem + Cfg::off_q(b), &mapQ, 0, g * G, q0, 0, &full[b]);
-          tma_load_4d(smem + Cfg::off_do(b), &mapDO, 0, g * G, q0, 0, &full[b]);
-        } else {         // d rows x NQ (query, head) columns, in 32-column panels
-          tma_load_3d(smem + Cfg::off_qt(b), &mapQt, 0, g * D, (q0 * G) / 32, &full[b]);
-          tma_load_3d(smem + Cfg::off_dot(b), &mapDOt, 0, g * D, (q0 * G) / 32, &full[b]);
+        if (pw == 0) {   // 4-D boxes (32 dims, G heads, QB/C queries, d/32 panels)
+          const int qh = q0 + (int)rank * (QB / C);
+          tma_load_4d(smem + Cfg::off_q(b), &mapQ, 0, g * G, qh, 0, &full[b]);
+          tma_load_4d(smem + Cfg::off_do(b), &mapDO, 0, g * G, qh, 0, &full[b]);
+        } else {         // d/C rows x NQ (query, head) columns, in 32-column panels
+          const int row = g * D + (int)rank * Cfg::DH;
+          tma_load_3d(smem + Cfg::off_qt(b), &mapQt, 0, row, (q0 * G) / 32, &full[b]);
+          tma_load_3d(smem + Cfg::off_dot(b), &mapDOt, 0, row, (q0 * G) / 32, &full[b]);
         }
       }
       __syncwarp();
       ++n;
     }
     // leave only once every load this warp issued has landed
-    if (pw == 1) warp_wait(&bars.v_full, 0, abort, status, kSiteKmProducer);
+    if (pw == 1) warp_wait<kCl>(&bars.v_full, 0, abort, status, kSiteKmProducer);
     for (int m = max(0, n - ns); m < n; ++m)
-      warp_wait(&full[m % ns], (m / ns) & 1, abort, status, kSiteKmProducer);
+      warp_wait<kCl>(&full[m % ns], (m / ns) & 1, abort, status, kSiteKmProducer);
+  } else if (warp == kMmaWarp && !issuer) {
+    // ---------------- C = 2, odd CTA: forward each landed copy to the issuer ----------------
+    // in the issuer's order of use: V, then Q/dO of block n before Q^T/dO^T
+    // of block n-1
+    auto forward = [&](uint64_t* bar, uint32_t ph, uint64_t* peer) {
+      if (!warp_wait<kCl>(bar, ph, abort, status, kSiteKmMma)) return false;
+      if (lane == 0) mbar_arrive_cl(mapa_u32(peer, 0));
+      __syncwarp();
+      return true;
+    };
+    bool ok = forward(&bars.v_full, 0, &bars.peer_v);
+    int n = 0;
+    for (int qb = walk.next(); ok && qb >= 0; qb = walk.next()) {
+      const int bs = n % Cfg::NSQ;
+      ok = forward(&bars.qdo_full[bs], (n / Cfg::NSQ) & 1, &bars.peer_qdo[bs]);
+      if (ok && n >= 1) {
+        const int m = n - 1, bt = m % Cfg::NST;
+        ok = forward(&bars.t_full[bt], (m / Cfg::NST) & 1, &bars.peer_t[bt]);
+      }
+      ++n;
+    }
+    if (ok && n >= 1) {
+      const int m = n - 1, bt = m % Cfg::NST;
+      forward(&bars.t_full[bt], (m / Cfg::NST) & 1, &bars.peer_t[bt]);
+    }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer (warp-converged, elected issue) ----------------
-    constexpr uint32_t id_s = idesc_tf32(128, NQ, false, false);
-    constexpr uint32_t id_g = idesc_tf32(128, D, false, false);
-    bool ok = warp_wait(&bars.v_full, 0, abort, status, kSiteKmMma) &&
-              warp_wait(&bars.k_ready, 0, abort, status, kSiteKmMma);
+    constexpr uint32_t id_s = idesc_tf32(128 * C, NQ, false, false);
+    constexpr uint32_t id_g = idesc_tf32(128 * C, D, false, false);
+    // this CTA's copy and, with C = 2, the odd CTA's have landed
+    auto landed = [&](uint64_t* bar, uint64_t* peer, uint32_t ph) {
+      return warp_wait<kCl>(bar, ph, abort, status, kSiteKmMma) &&
+             (C == 1 || warp_wait<kCl>(peer, ph, abort, status, kSiteKmMma));
+    };
+    bool ok = landed(&bars.v_full, &bars.peer_v, 0) &&
+              warp_wait<kCl>(&bars.k_ready, 0, abort, status, kSiteKmMma);
     const uint64_t desc0 = sdesc(smem_u32(smem), 16, 1024);
     const uint64_t av = desc0 + (uint64_t)(Cfg::OFF_V >> 4);
-    // dV += P^T dO, dK += dS^T Q for block m (stage m & 1)
+    // dV += P^T dO, dK += dS^T Q for block m (TMEM stage m & 1, Q^T / dO^T stage m % NST)
     auto grad_mma = [&](int m) -> bool {
-      const int b = m & 1;
-      const uint32_t ph = (m >> 1) & 1;
-      if (!warp_wait(&bars.p_ready[b], ph, abort, status, kSiteKmMma) ||
-          !warp_wait(&bars.t_full[b], ph, abort, status, kSiteKmMma))
+      const int b = m & 1, bt = m % Cfg::NST;
+      if (!warp_wait<kCl>(&bars.p_ready[b], (m >> 1) & 1, abort, status, kSiteKmMma) ||
+          !landed(&bars.t_full[bt], &bars.peer_t[bt], (m / Cfg::NST) & 1))
         return false;
-      const uint64_t bqt = desc0 + (uint64_t)(Cfg::off_qt(b) >> 4);
-      const uint64_t bdot = desc0 + (uint64_t)(Cfg::off_dot(b) >> 4);
+      const uint64_t bqt = desc0 + (uint64_t)(Cfg::off_qt(bt) >> 4);
+      const uint64_t bdot = desc0 + (uint64_t)(Cfg::off_dot(bt) >> 4);
       const uint32_t a_p = tmem + Cfg::t_s(b), a_ds = tmem + Cfg::t_dp(b);
       const uint32_t acc0 = (m > 0) ? 1u : 0u;
       if (elect_one()) {
         tc_fence_after();
-        mma_ts(tmem + Cfg::T_DV, a_p, bdot, id_g, acc0);
-        mma_ts(tmem + Cfg::T_DK, a_ds, bqt, id_g, acc0);
+        mma_ts_g<C>(tmem + Cfg::T_DV, a_p, bdot, id_g, acc0);
+        mma_ts_g<C>(tmem + Cfg::T_DK, a_ds, bqt, id_g, acc0);
 #pragma unroll
         for (int kk = 1; kk < NQ / 8; ++kk) {
           const uint64_t ot = desc_off(kk, Cfg::T_PANEL_BYTES);
-          mma_ts_acc(tmem + Cfg::T_DV, a_p + 8 * kk, bdot + ot, id_g);
-          mma_ts_acc(tmem + Cfg::T_DK, a_ds + 8 * kk, bqt + ot, id_g);
+          mma_ts_acc_g<C>(tmem + Cfg::T_DV, a_p + 8 * kk, bdot + ot, id_g);
+          mma_ts_acc_g<C>(tmem + Cfg::T_DK, a_ds + 8 * kk, bqt + ot, id_g);
         }
-        mma_commit(&bars.t_empty[b]);
+        mma_commit_g<C>(&bars.t_empty[bt]);
       }
       __syncwarp();
       return true;
     };
     int n = 0;
-    for (int qb = nqb - 1; ok && qb >= qb0; --qb) {
-      if (!visible(qb)) continue;
+    for (int qb = walk.next(); ok && qb >= 0; qb = walk.next()) {
       const int b = n & 1, bs = n % Cfg::NSQ;
-      if (!warp_wait(&bars.qdo_full[bs], (n / Cfg::NSQ) & 1, abort, status, kSiteKmMma)) { ok = false; break; }
+      if (!landed(&bars.qdo_full[bs], &bars.peer_qdo[bs], (n / Cfg::NSQ) & 1)) { ok = false; break; }
       // TMEM stage b was last read by dV / dK of block n-2, issued earlier
-      // (MMAs run in issue order) after its warpgroup released it
+      // (MMAs run in issue order) after its softmax released it
       const uint64_t bq = desc0 + (uint64_t)(Cfg::off_q(bs) >> 4);
       const uint64_t bdo = desc0 + (uint64_t)(Cfg::off_do(bs) >> 4);
       if (elect_one()) {
         tc_fence_after();
-        mma_ts(tmem + Cfg::t_s(b), tmem + Cfg::T_K, bq, id_s, 0u);
-        mma_ss(tmem + Cfg::t_dp(b), av, bdo, id_s, 0u);
+        mma_ts_g<C>(tmem + Cfg::t_s(b), tmem + Cfg::T_K, bq, id_s, 0u);
+        mma_ss_g<C>(tmem + Cfg::t_dp(b), av, bdo, id_s, 0u);
 #pragma unroll
         for (int ks = 1; ks < D / 8; ++ks) {
           const uint64_t ob = desc_off(ks, Cfg::BLK_PANEL_BYTES);
-          mma_ts_acc(tmem + Cfg::t_s(b), tmem + Cfg::T_K + 8 * ks, bq + ob, id_s);
-          mma_ss_acc(tmem + Cfg::t_dp(b), av + desc_off(ks, Cfg::V_PANEL_BYTES), bdo + ob, id_s);
+          mma_ts_acc_g<C>(tmem + Cfg::t_s(b), tmem + Cfg::T_K + 8 * ks, bq + ob, id_s);
+          mma_ss_acc_g<C>(tmem + Cfg::t_dp(b), av + desc_off(ks, Cfg::V_PANEL_BYTES), bdo + ob, id_s);
         }
-        mma_commit(&bars.s_full[b]);
-        mma_commit(&bars.qdo_empty[bs]);
+        mma_commit_g<C>(&bars.s_full[b]);
+        mma_commit_g<C>(&bars.qdo_empty[bs]);
       }
       __syncwarp();
       if (n >= 1 && !grad_mma(n - 1)) { ok = false; break; }
       ++n;
     }
     if (ok && n >= 1) ok = grad_mma(n - 1);
-    if (elect_one()) mma_commit(&bars.acc_done);   // also drains every MMA issued above
+    if (elect_one()) mma_commit_g<C>(&bars.acc_done);   // also drains every MMA issued above
     __syncwarp();
+    // no MMA of the group may still run when the CTAs leave
+    warp_wait<kCl>(&bars.acc_done, 0, abort, status, kSiteKmMma);
   } else {
-    // ---------------- compute: thread = key (TMEM lane); warpgroup wg takes the blocks of stage wg ----------------
+    // ---------------- compute: thread = key (TMEM lane) ----------------
     const int wg = (warp - kFirstCompute) >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int key = k0 + r;
@@ -765,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.k_ready);
+      if (lane == 0) arrive_issuer<C>(&bars.k_ready);
     }
     // Both warpgroups take every block, warpgroup wg the columns
     // [wg*NQ/2, (wg+1)*NQ/2) of it: the softmax of a block then finishes in
@@ -775,9 +874,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert(HQ == 16 || HQ == 32, "column split");
     int n = 0;
     bool ok = true;
-    for (int qb = nqb - 1; qb >= qb0; --qb) {
-      if (!visible(qb)) continue;
+    for (int qb = walk.next(); qb >= 0; qb = walk.next()) {
       const int b = n & 1;
+      const unsigned maxseg = __ldg(blk_maxseg + qb);   // loaded ahead of the waits below
       // this warpgroup's columns' metadata (double-buffered; one named barrier per block)
       if (wt < HQ) {
         const int col = wg * HQ + wt;
@@ -789,12 +888,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         meta[wg][b][wt] = m;
       }
       asm volatile("bar.sync %0, 128;" ::"r"(1 + wg) : "memory");
-      if (!mbar_wait(&bars.s_full[b], (n >> 1) & 1, abort, status, kSiteKmCompute)) { ok = false; break; }
+      // warp-uniform: every lane leaves the loop together (walk.next() is warp-collective)
+      if (!warp_wait<kCl>(&bars.s_full[b], (n >> 1) & 1, abort, status, kSiteKmCompute)) { ok = false; break; }
       tc_fence_after();
       // every (key, column) of the block visible: key <= first query and >= every seg
       const int q_first = qb * QB;
-      const bool full = key <= q_first && key >= (int)__ldg(blk_maxseg + qb) &&
-                        q_first + QB - 1 < S;
+      const bool full = key <= q_first && key >= (int)maxseg && q_first + QB - 1 < S;
       const float4* mt = meta[wg][b];
       const uint32_t ts = tl + Cfg::t_s(b) + wg * HQ, tdp = tl + Cfg::t_dp(b) + wg * HQ;
       float sv[HQ], dp[HQ];
@@ -835,12 +934,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.p_ready[b]);
+      if (lane == 0) arrive_issuer<C>(&bars.p_ready[b]);
       ++n;
     }
     // epilogue: warpgroup 0 adds dK (rotated by the RoPE backward of the key's
     // position when rope.on), warpgroup 1 adds dV (owned rows, NaN-guarded)
-    if (ok && mbar_wait(&bars.acc_done, 0, abort, status, kSiteKmCompute)) {
+    if (ok && mbar_wait<kCl>(&bars.acc_done, 0, abort, status, kSiteKmCompute)) {
       tc_fence_after();
       const long long row = (long long)key * sh.Hk * D + (long long)g * D;
       float* dst_row = (wg == 0 ? dK : dV) + row;
@@ -873,7 +972,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  // both CTAs of a pair are done with every copy and MMA of the group before
+  // its TMEM is freed and before either leaves
+  if (C > 1) cluster_sync();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc_g<C>(tmem, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -1016,27 +1119,28 @@ gqa_status launch_clustered(void (*kern)(KArgs...), dim3 grid, int cluster, int 
   return check_launch(what);
 }
 
-template <int D>
-gqa_status km_launch(const float* Q, const float* K, const float* V, const float* dO,
-                     const float* LSE, const uint32_t* seg, float* dK, float* dV, const float* Qt,
-                     const float* dOt, long long ld_qt, const float* Dws, const uint32_t* blk_minseg,
-                     const uint32_t* blk_maxseg, uint32_t* status, const Shape& sh,
-                     cudaStream_t st, const RopeParams& rope) {
-  using Cfg = KmCfg<D>;
+template <int D, int C>
+gqa_status km_launch_c(const float* Q, const float* K, const float* V, const float* dO,
+                       const float* LSE, const uint32_t* seg, float* dK, float* dV, const float* Qt,
+                       const float* dOt, long long ld_qt, const float* Dws, const uint32_t* blk_minseg,
+                       const uint32_t* blk_maxseg, uint32_t* status, const Shape& sh,
+                       cudaStream_t st, const RopeParams& rope) {
+  using Cfg = KmCfg<D, C>;
   const int QB = Cfg::NQ / sh.G;
   CUtensorMap mv, mq, mdo, mqt, mdot;
   gqa_status r;
   const long long kv_panels = (long long)sh.Hk * D / 32;
   if ((r = map_panels(&mv, V, (long long)sh.Hk * D, sh.S, kv_panels, 128, D / 32)) != GQA_OK) return r;
-  if ((r = map_heads(&mq, Q, D, sh.H, sh.S, sh.G, QB)) != GQA_OK) return r;
-  if ((r = map_heads(&mdo, dO, D, sh.H, sh.S, sh.G, QB)) != GQA_OK) return r;
-  if ((r = map_panels(&mqt, Qt, ld_qt, (long long)sh.Hk * D, ld_qt / 32, D, Cfg::T_PANELS)) != GQA_OK) return r;
-  if ((r = map_panels(&mdot, dOt, ld_qt, (long long)sh.Hk * D, ld_qt / 32, D, Cfg::T_PANELS)) != GQA_OK) return r;
-  if (cudaFuncSetAttribute(tc_key_major<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if ((r = map_heads(&mq, Q, D, sh.H, sh.S, sh.G, QB / C)) != GQA_OK) return r;
+  if ((r = map_heads(&mdo, dO, D, sh.H, sh.S, sh.G, QB / C)) != GQA_OK) return r;
+  if ((r = map_panels(&mqt, Qt, ld_qt, (long long)sh.Hk * D, ld_qt / 32, Cfg::DH, Cfg::T_PANELS)) != GQA_OK) return r;
+  if ((r = map_panels(&mdot, dOt, ld_qt, (long long)sh.Hk * D, ld_qt / 32, Cfg::DH, Cfg::T_PANELS)) != GQA_OK) return r;
+  if (cudaFuncSetAttribute(tc_key_major<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess)
     return check_launch("key-major smem attribute");
-  dim3 grid((sh.S + 127) / 128, sh.Hk);
-  return launch_clustered(tc_key_major<D>, grid, 1, Cfg::SMEM_BYTES, st, "tensor-core key-major",
+  const int n_tiles = (sh.S + 127) / 128;
+  dim3 grid((n_tiles + C - 1) / C * C, sh.Hk);
+  return launch_clustered(tc_key_major<D, C>, grid, C, Cfg::SMEM_BYTES, st, "tensor-core key-major",
                           mv, mq, mdo, mqt, mdot, K, LSE, Dws, seg, blk_minseg, blk_maxseg, dK, dV,
                           status, sh, rope);
 }
@@ -1050,15 +1154,30 @@ gqa_status transpose_launch(const float* X, float* Xt, int S, int Hk, int Gx, in
   return check_launch("group transpose");
 }
 
-// CTA group of the query-major kernel: 2 (SM pairs,
-// cta_group::2: half the shared-memory traffic per SM per flop) by default;
-// GQA_TC_CTA_GROUP=1 selects one SM per slab. Read once per process.
+// CTA group of both backward kernels: 2 (SM pairs, cta_group::2: half the
+// shared-memory traffic per SM per flop) by default; GQA_TC_CTA_GROUP=1
+// selects one SM per slab / key tile. Read once per process.
 int cta_group() {
   static int c = [] {
     const char* e = getenv("GQA_TC_CTA_GROUP");
     return (e != nullptr && atoi(e) == 1) ? 1 : 2;
   }();
   return c;
+}
+
+// The key-major kernel runs on SM pairs when the pair's half block holds
+// whole queries (G divides NQ/2), else on one SM per key tile.
+template <int D>
+gqa_status km_launch(const float* Q, const float* K, const float* V, const float* dO,
+                     const float* LSE, const uint32_t* seg, float* dK, float* dV, const float* Qt,
+                     const float* dOt, long long ld_qt, const float* Dws, const uint32_t* blk_minseg,
+                     const uint32_t* blk_maxseg, uint32_t* status, const Shape& sh,
+                     cudaStream_t st, const RopeParams& rope) {
+  if (cta_group() == 2 && (KmCfg<D, 2>::NQH % sh.G) == 0)
+    return km_launch_c<D, 2>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, ld_qt, Dws, blk_minseg,
+                             blk_maxseg, status, sh, st, rope);
+  return km_launch_c<D, 1>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, ld_qt, Dws, blk_minseg,
+                           blk_maxseg, status, sh, st, rope);
 }
 
 template <int D, int C, bool GD>
@@ -1139,7 +1258,7 @@ TcWsLayout tc_ws_layout(int S, int H, int Hk, int d) {
 bool tc_supported(const Shape& sh) {
   // G must divide the query-major slab (128 rows) and the key-major block
   // (NQ columns: 32 at d = 128, 64 below)
-  const int nq = (sh.d == 128) ? KmCfg<128>::NQ : KmCfg<64>::NQ;
+  const int nq = (sh.d == 128) ? KmCfg<128, 1>::NQ : KmCfg<64, 1>::NQ;
   return (sh.d == 32 || sh.d == 64 || sh.d == 128) && sh.G >= 1 && sh.G <= nq &&
          (nq % sh.G) == 0;
 }
@@ -1157,7 +1276,7 @@ gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* d
   float* dOt = reinterpret_cast<float*>(ws + T.dot_off);
   uint32_t* blk = reinterpret_cast<uint32_t*>(ws + T.blk_off);
   uint32_t* blk_max = reinterpret_cast<uint32_t*>(ws + T.blkmax_off);
-  const int QB = ((sh.d == 128) ? KmCfg<128>::NQ : KmCfg<64>::NQ) / sh.G;
+  const int QB = ((sh.d == 128) ? KmCfg<128, 1>::NQ : KmCfg<64, 1>::NQ) / sh.G;
   gqa_status r;
   if ((r = tile_minseg(seg, sh.S, QB, blk, st, blk_max)) != GQA_OK) return r;
   // K^T for the query-major kernel; Q^T and dO^T are written by the

@@ -310,6 +310,30 @@ __device__ __forceinline__ void mma_ts_acc_g(uint32_t d_tmem, uint32_t a_tmem, u
                  : "memory");
   }
 }
+template <int CG>
+__device__ __forceinline__ void mma_ss_g(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  if constexpr (CG == 1) {
+    mma_ss(d_tmem, a_desc, b_desc, idesc, accumulate);
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+template <int CG>
+__device__ __forceinline__ void mma_ss_acc_g(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc) {
+  if constexpr (CG == 1) {
+    mma_ss_acc(d_tmem, a_desc, b_desc, idesc);
+  } else {
+    asm volatile("tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, 1;" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc)
+                 : "memory");
+  }
+}
 // Arrive on `bar` (CG = 1) or on the barrier at its offset in both CTAs of the
 // pair (CG = 2) once every MMA this thread issued so far has completed.
 template <int CG>

@@ -1,7 +1,8 @@
-"""The query-major kernel runs on SM pairs (cta_group::2, M = 256) by default;
-GQA_TC_CTA_GROUP=1 selects the one-SM-per-slab variant. The group size is read
-once per process, so the variant runs in a child process, against the oracle
-on edge shapes (ragged tails, documents, all head dims)."""
+"""Both tensor-core backward kernels run on SM pairs (cta_group::2, M = 256) by
+default; GQA_TC_CTA_GROUP=1 selects the one-SM variants (one query slab / one
+key tile per SM). The group size is read once per process, so the variant runs
+in a child process, against the oracle on edge shapes (ragged tails, documents,
+all head dims)."""
 import os
 import subprocess
 import sys
@@ -36,7 +37,7 @@ print("ok")
 """
 
 
-def test_single_sm_query_major_matches_oracle():
+def test_single_sm_kernels_match_oracle():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from causal_gqa_attention_attn_gb300 import build
