@@ -109,7 +109,7 @@ struct QmCfg {
 };
 
 struct QmBarriers {
-  uint64_t full[12], empty[12], peer_full[12], s_full[2], s_free[2], qdo_ready, dq_done;
+  uint64_t full[12], empty[12], s_full[2], s_free[2], qdo_ready, dq_done;
   uint32_t tmem_base;
   int abort;
   unsigned kmin;
@@ -158,9 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NU; ++i) {
-      mbar_init(&bars.full[i], 1);        // the producer warp of the unit arms its bytes
+      // the producer warp of the unit arms its bytes; in the issuing CTA of a
+      // pair the odd CTA's forward of its half is the second arrival
+      mbar_init(&bars.full[i], issuer ? C : 1);
       mbar_init(&bars.empty[i], 1);       // released by the issuer's MMA commit
-      mbar_init(&bars.peer_full[i], 1);   // C = 2: the odd CTA's unit landed (forwarded)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.s_full[i], 1);
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- C = 2, odd CTA: forward each landed unit to the issuer ----------------
     for (int i = 0; i < n_units; ++i) {
       if (!warp_wait<kCl>(&bars.full[i % NU], (i / NU) & 1, abort, status, kSiteQmMma)) break;
-      if (lane == 0) mbar_arrive_cl(mapa_u32(&bars.peer_full[i % NU], 0));
+      if (lane == 0) mbar_arrive_cl(mapa_u32(&bars.full[i % NU], 0));
       __syncwarp();
     }
   } else if (warp == kMmaWarp) {
@@ -256,11 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto unit_desc = [&](int i) { return desc0 + (uint64_t)(((i % NU) * Cfg::UNIT_BYTES) >> 4); };
     // both CTAs' parts of unit i have landed
     auto unit_wait = [&](int i) {
-      const uint32_t ph = (i / NU) & 1;
-      return warp_wait<kCl>(&bars.full[i % NU], ph, abort, status, kSiteQmMma) &&
-             (C == 1 || warp_wait<kCl>(&bars.peer_full[i % NU], ph, abort, status, kSiteQmMma));
+      return warp_wait<kCl>(&bars.full[i % NU], (i / NU) & 1, abort, status, kSiteQmMma);
     };
-    int use0 = 0, use1 = 0;       // uses of each TMEM stage so far (s_free phases)
+    int use0 = 0, use1 = 0;       // pass-1 uses of each TMEM stage (s_free phases)
     // wait until the previous use of stage st has been released by its warpgroup(s)
     auto stage_free = [&](int st) {
       const int u = st ? use1 : use0;
@@ -293,12 +292,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (st) ++use1; else ++use0;
     }
     // ---- pass 2: sub-chunk s (chunk s / NSUB, part s % NSUB) in stage s & 1 ----
-    int dq_use = 0;               // stage use index of the sub-chunk whose dQ is next
-    auto issue_dq = [&](int s) -> bool {
-      const int st = s & 1, j = s / Cfg::NSUB, h = s % Cfg::NSUB;
+    // dQ(s) and S / dP of sub-chunk s + 2 (the same stage: MMAs run in issue
+    // order, so the stage is rewritten only after dQ(s) has read dS(s)) go out
+    // as one burst once the softmax has handed dS(s) back; the tensor core's
+    // order is the same as issuing them apart, with one wait and one burst
+    // fewer per sub-chunk on the issuing warp.
+    static_assert(!Cfg::P1_IN_DQ || Cfg::NSUB >= 2,
+                  "the prologue must release both pass-1 stages before the first dQ");
+    // S / dP of sub-chunk s2 into stage s2 & 1, with its commits
+    auto sdp2 = [&](int s2) {
+      const int j = s2 / Cfg::NSUB, h = s2 % Cfg::NSUB, ik = p2_base + 3 * j;
+      const uint64_t off = (uint64_t)((h * Cfg::HALF2 * 128) >> 4);   // rows h*HALF2.. of each panel
+      issue_sdp(tmem + Cfg::p2_stage(s2 & 1), Cfg::BK2, id_s2, unit_desc(ik) + off, unit_desc(ik + 1) + off);
+      mma_commit_g<C>(&bars.s_full[s2 & 1]);
+      if (h == Cfg::NSUB - 1) {
+        mma_commit_g<C>(&bars.empty[ik % NU]);
+        mma_commit_g<C>(&bars.empty[(ik + 1) % NU]);
+      }
+    };
+    // K and V of sub-chunk s2's chunk, waited for at the chunk's first sub-chunk
+    auto kv_wait = [&](int s2) {
+      const int ik = p2_base + 3 * (s2 / Cfg::NSUB);
+      return s2 % Cfg::NSUB != 0 || (unit_wait(ik) && unit_wait(ik + 1));
+    };
+    // prologue: sub-chunks 0 and 1, each after the last pass-1 use of its stage
+    for (int s = 0; ok && s < 2 && s < n_sub; ++s) {
+      if (!kv_wait(s) || !stage_free(s & 1)) { ok = false; break; }
+      if (elect_one()) sdp2(s);   // issue_sdp fences after the waits
+      __syncwarp();
+    }
+    for (int s = 0; ok && s < n_sub; ++s) {
+      const int st = s & 1, j = s / Cfg::NSUB, h = s % Cfg::NSUB, s2 = s + 2;
       const int ikt = p2_base + 3 * j + 2;
-      if (!warp_wait<kCl>(&bars.s_free[st], dq_use & 1, abort, status, kSiteQmMma)) return false;
-      if (h == 0 && !unit_wait(ikt)) return false;
+      const int u = (st ? use1 : use0) + (s >> 1);      // this sub-chunk's use of stage st
+      if (!warp_wait<kCl>(&bars.s_free[st], u & 1, abort, status, kSiteQmMma) ||
+          (h == 0 && !unit_wait(ikt)) || (s2 < n_sub && !kv_wait(s2))) {
+        ok = false;
+        break;
+      }
       const uint32_t a_ds = tmem + Cfg::p2_stage(st), d_q = tmem + Cfg::T_DQ;
       const uint64_t bkt = unit_desc(ikt);
       if (elect_one()) {
@@ -312,32 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           else mma_ts_acc_g<C>(d_q, a_ds + 8 * kk, bkt + o, id_q);
         }
         if (h == Cfg::NSUB - 1) mma_commit_g<C>(&bars.empty[ikt % NU]);
+        if (s2 < n_sub) sdp2(s2);
       }
       __syncwarp();
-      return true;
-    };
-    for (int s = 0; ok && s < n_sub; ++s) {
-      const int st = s & 1, j = s / Cfg::NSUB, h = s % Cfg::NSUB;
-      const int ik = p2_base + 3 * j;
-      if (h == 0 && (!unit_wait(ik) || !unit_wait(ik + 1))) { ok = false; break; }
-      // the stage's previous use: pass 1 for s < 2, else sub-chunk s-2, whose
-      // release issue_dq(s-2) has already waited for
-      if (s < 2 && !stage_free(st)) { ok = false; break; }
-      const uint64_t off = (uint64_t)((h * Cfg::HALF2 * 128) >> 4);   // rows h*HALF2.. of each panel
-      if (elect_one()) {
-        issue_sdp(tmem + Cfg::p2_stage(st), Cfg::BK2, id_s2, unit_desc(ik) + off, unit_desc(ik + 1) + off);
-        mma_commit_g<C>(&bars.s_full[st]);
-        if (h == Cfg::NSUB - 1) {
-          mma_commit_g<C>(&bars.empty[ik % NU]);
-          mma_commit_g<C>(&bars.empty[(ik + 1) % NU]);
-        }
-      }
-      __syncwarp();
-      const int this_use = st ? use1++ : use0++;
-      if (s > 0 && !issue_dq(s - 1)) { ok = false; break; }
-      dq_use = this_use;
     }
-    if (ok && n_sub > 0) ok = issue_dq(n_sub - 1);
     if (elect_one()) mma_commit_g<C>(&bars.dq_done);   // also drains every MMA issued above
     __syncwarp();
     // no MMA of the group may still run when the CTAs leave
@@ -588,9 +597,9 @@ struct KmCfg {
 };
 
 struct KmBarriers {
-  uint64_t v_full, peer_v, k_ready;
-  uint64_t qdo_full[4], qdo_empty[4], peer_qdo[4];   // Q, dO blocks of each stage
-  uint64_t t_full[4], t_empty[4], peer_t[4];         // Q^T, dO^T blocks of each stage
+  uint64_t v_full, k_ready;
+  uint64_t qdo_full[4], qdo_empty[4];   // Q, dO blocks of each stage
+  uint64_t t_full[4], t_empty[4];       // Q^T, dO^T blocks of each stage
   uint64_t s_full[2], p_ready[2], acc_done;
   uint32_t tmem_base;
   int abort;
@@ -669,18 +678,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qb0 = kg0 / QB, nqb = (S + QB - 1) / QB;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars.v_full, 1);
-    mbar_init(&bars.peer_v, 1);
+    // A copy barrier is armed by this CTA's producer warp; in the issuing CTA
+    // of a pair the odd CTA's forward of its half is the second arrival.
+    const uint32_t nfull = issuer ? C : 1;
+    mbar_init(&bars.v_full, nfull);
     mbar_init(&bars.k_ready, C * kComputeWarps);          // every compute warp of each CTA
     for (int b = 0; b < Cfg::NSQ; ++b) {
-      mbar_init(&bars.qdo_full[b], 1);     // producer warp 0 arms both tiles
-      mbar_init(&bars.qdo_empty[b], 1);    // released by the issuer's MMA commit
-      mbar_init(&bars.peer_qdo[b], 1);     // C = 2: the odd CTA's tiles landed (forwarded)
+      mbar_init(&bars.qdo_full[b], nfull);   // producer warp 0 arms both tiles
+      mbar_init(&bars.qdo_empty[b], 1);      // released by the issuer's MMA commit
     }
     for (int b = 0; b < Cfg::NST; ++b) {
-      mbar_init(&bars.t_full[b], 1);       // producer warp 1 arms both tiles
+      mbar_init(&bars.t_full[b], nfull);     // producer warp 1 arms both tiles
       mbar_init(&bars.t_empty[b], 1);
-      mbar_init(&bars.peer_t[b], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars.s_full[b], 1);
@@ -752,91 +761,112 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- C = 2, odd CTA: forward each landed copy to the issuer ----------------
     // in the issuer's order of use: V, then Q/dO of block n before Q^T/dO^T
     // of block n-1
-    auto forward = [&](uint64_t* bar, uint32_t ph, uint64_t* peer) {
+    // (this CTA's barrier landed -> an arrive on the same barrier of the issuer)
+    auto forward = [&](uint64_t* bar, uint32_t ph) {
       if (!warp_wait<kCl>(bar, ph, abort, status, kSiteKmMma)) return false;
-      if (lane == 0) mbar_arrive_cl(mapa_u32(peer, 0));
+      if (lane == 0) mbar_arrive_cl(mapa_u32(bar, 0));
       __syncwarp();
       return true;
     };
-    bool ok = forward(&bars.v_full, 0, &bars.peer_v);
+    bool ok = forward(&bars.v_full, 0);
     int n = 0;
     for (int qb = walk.next(); ok && qb >= 0; qb = walk.next()) {
       const int bs = n % Cfg::NSQ;
-      ok = forward(&bars.qdo_full[bs], (n / Cfg::NSQ) & 1, &bars.peer_qdo[bs]);
+      ok = forward(&bars.qdo_full[bs], (n / Cfg::NSQ) & 1);
       if (ok && n >= 1) {
-        const int m = n - 1, bt = m % Cfg::NST;
-        ok = forward(&bars.t_full[bt], (m / Cfg::NST) & 1, &bars.peer_t[bt]);
+        const int m = n - 1;
+        ok = forward(&bars.t_full[m % Cfg::NST], (m / Cfg::NST) & 1);
       }
       ++n;
     }
     if (ok && n >= 1) {
-      const int m = n - 1, bt = m % Cfg::NST;
-      forward(&bars.t_full[bt], (m / Cfg::NST) & 1, &bars.peer_t[bt]);
+      const int m = n - 1;
+      forward(&bars.t_full[m % Cfg::NST], (m / Cfg::NST) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer (warp-converged, elected issue) ----------------
     constexpr uint32_t id_s = idesc_tf32(128 * C, NQ, false, false);
     constexpr uint32_t id_g = idesc_tf32(128 * C, D, false, false);
-    // this CTA's copy and, with C = 2, the odd CTA's have landed
-    auto landed = [&](uint64_t* bar, uint64_t* peer, uint32_t ph) {
-      return warp_wait<kCl>(bar, ph, abort, status, kSiteKmMma) &&
-             (C == 1 || warp_wait<kCl>(peer, ph, abort, status, kSiteKmMma));
+    // this CTA's copy and, with C = 2, the odd CTA's have landed (one barrier)
+    auto landed = [&](uint64_t* bar, uint32_t ph) {
+      return warp_wait<kCl>(bar, ph, abort, status, kSiteKmMma);
     };
-    bool ok = landed(&bars.v_full, &bars.peer_v, 0) &&
-              warp_wait<kCl>(&bars.k_ready, 0, abort, status, kSiteKmMma);
+    bool ok = landed(&bars.v_full, 0) && warp_wait<kCl>(&bars.k_ready, 0, abort, status, kSiteKmMma);
     const uint64_t desc0 = sdesc(smem_u32(smem), 16, 1024);
     const uint64_t av = desc0 + (uint64_t)(Cfg::OFF_V >> 4);
+    // S^T = K Q^T, dP^T = V dO^T of block n into TMEM stage n & 1, with its commits
+    auto sdp = [&](int n) {
+      const int b = n & 1, bs = n % Cfg::NSQ;
+      const uint64_t bq = desc0 + (uint64_t)(Cfg::off_q(bs) >> 4);
+      const uint64_t bdo = desc0 + (uint64_t)(Cfg::off_do(bs) >> 4);
+      mma_ts_g<C>(tmem + Cfg::t_s(b), tmem + Cfg::T_K, bq, id_s, 0u);
+      mma_ss_g<C>(tmem + Cfg::t_dp(b), av, bdo, id_s, 0u);
+#pragma unroll
+      for (int ks = 1; ks < D / 8; ++ks) {
+        const uint64_t ob = desc_off(ks, Cfg::BLK_PANEL_BYTES);
+        mma_ts_acc_g<C>(tmem + Cfg::t_s(b), tmem + Cfg::T_K + 8 * ks, bq + ob, id_s);
+        mma_ss_acc_g<C>(tmem + Cfg::t_dp(b), av + desc_off(ks, Cfg::V_PANEL_BYTES), bdo + ob, id_s);
+      }
+      mma_commit_g<C>(&bars.s_full[b]);
+      mma_commit_g<C>(&bars.qdo_empty[bs]);
+    };
     // dV += P^T dO, dK += dS^T Q for block m (TMEM stage m & 1, Q^T / dO^T stage m % NST)
-    auto grad_mma = [&](int m) -> bool {
+    auto grad = [&](int m) {
       const int b = m & 1, bt = m % Cfg::NST;
-      if (!warp_wait<kCl>(&bars.p_ready[b], (m >> 1) & 1, abort, status, kSiteKmMma) ||
-          !landed(&bars.t_full[bt], &bars.peer_t[bt], (m / Cfg::NST) & 1))
-        return false;
       const uint64_t bqt = desc0 + (uint64_t)(Cfg::off_qt(bt) >> 4);
       const uint64_t bdot = desc0 + (uint64_t)(Cfg::off_dot(bt) >> 4);
       const uint32_t a_p = tmem + Cfg::t_s(b), a_ds = tmem + Cfg::t_dp(b);
       const uint32_t acc0 = (m > 0) ? 1u : 0u;
-      if (elect_one()) {
-        tc_fence_after();
-        mma_ts_g<C>(tmem + Cfg::T_DV, a_p, bdot, id_g, acc0);
-        mma_ts_g<C>(tmem + Cfg::T_DK, a_ds, bqt, id_g, acc0);
+      mma_ts_g<C>(tmem + Cfg::T_DV, a_p, bdot, id_g, acc0);
+      mma_ts_g<C>(tmem + Cfg::T_DK, a_ds, bqt, id_g, acc0);
 #pragma unroll
-        for (int kk = 1; kk < NQ / 8; ++kk) {
-          const uint64_t ot = desc_off(kk, Cfg::T_PANEL_BYTES);
-          mma_ts_acc_g<C>(tmem + Cfg::T_DV, a_p + 8 * kk, bdot + ot, id_g);
-          mma_ts_acc_g<C>(tmem + Cfg::T_DK, a_ds + 8 * kk, bqt + ot, id_g);
-        }
-        mma_commit_g<C>(&bars.t_empty[bt]);
+      for (int kk = 1; kk < NQ / 8; ++kk) {
+        const uint64_t ot = desc_off(kk, Cfg::T_PANEL_BYTES);
+        mma_ts_acc_g<C>(tmem + Cfg::T_DV, a_p + 8 * kk, bdot + ot, id_g);
+        mma_ts_acc_g<C>(tmem + Cfg::T_DK, a_ds + 8 * kk, bqt + ot, id_g);
       }
-      __syncwarp();
-      return true;
+      mma_commit_g<C>(&bars.t_empty[bt]);
     };
-    int n = 0;
-    for (int qb = walk.next(); ok && qb >= 0; qb = walk.next()) {
-      const int b = n & 1, bs = n % Cfg::NSQ;
-      if (!landed(&bars.qdo_full[bs], &bars.peer_qdo[bs], (n / Cfg::NSQ) & 1)) { ok = false; break; }
-      // TMEM stage b was last read by dV / dK of block n-2, issued earlier
-      // (MMAs run in issue order) after its softmax released it
-      const uint64_t bq = desc0 + (uint64_t)(Cfg::off_q(bs) >> 4);
-      const uint64_t bdo = desc0 + (uint64_t)(Cfg::off_do(bs) >> 4);
+    // Blocks are pulled from the walk one ahead of their use: exists(n) tells
+    // whether the tile (pair) has an n-th visible block.
+    int fetched = 0;
+    bool done = false;
+    auto exists = [&](int n) {
+      while (!done && fetched <= n) {
+        if (walk.next() < 0) done = true;
+        else ++fetched;
+      }
+      return n < fetched;
+    };
+    // S^T / dP^T of blocks 0 and 1, then per block m one burst: dV / dK of
+    // block m and S^T / dP^T of block m + 2 (the same TMEM stage: MMAs run in
+    // issue order, so it is rewritten only after dV / dK have read it). The
+    // tensor core's order is S(0) S(1) G(0) S(2) G(1) S(3) ..., with one wait
+    // on the softmax and one burst per block on the issuing warp.
+    for (int n = 0; ok && n < 2 && exists(n); ++n) {
+      if (!landed(&bars.qdo_full[n % Cfg::NSQ], (n / Cfg::NSQ) & 1)) { ok = false; break; }
       if (elect_one()) {
         tc_fence_after();
-        mma_ts_g<C>(tmem + Cfg::t_s(b), tmem + Cfg::T_K, bq, id_s, 0u);
-        mma_ss_g<C>(tmem + Cfg::t_dp(b), av, bdo, id_s, 0u);
-#pragma unroll
-        for (int ks = 1; ks < D / 8; ++ks) {
-          const uint64_t ob = desc_off(ks, Cfg::BLK_PANEL_BYTES);
-          mma_ts_acc_g<C>(tmem + Cfg::t_s(b), tmem + Cfg::T_K + 8 * ks, bq + ob, id_s);
-          mma_ss_acc_g<C>(tmem + Cfg::t_dp(b), av + desc_off(ks, Cfg::V_PANEL_BYTES), bdo + ob, id_s);
-        }
-        mma_commit_g<C>(&bars.s_full[b]);
-        mma_commit_g<C>(&bars.qdo_empty[bs]);
+        sdp(n);
       }
       __syncwarp();
-      if (n >= 1 && !grad_mma(n - 1)) { ok = false; break; }
-      ++n;
     }
-    if (ok && n >= 1) ok = grad_mma(n - 1);
+    for (int m = 0; ok && exists(m); ++m) {
+      const int n2 = m + 2;
+      const bool more = exists(n2);
+      if (!warp_wait<kCl>(&bars.p_ready[m & 1], (m >> 1) & 1, abort, status, kSiteKmMma) ||
+          !landed(&bars.t_full[m % Cfg::NST], (m / Cfg::NST) & 1) ||
+          (more && !landed(&bars.qdo_full[n2 % Cfg::NSQ], (n2 / Cfg::NSQ) & 1))) {
+        ok = false;
+        break;
+      }
+      if (elect_one()) {
+        tc_fence_after();
+        grad(m);
+        if (more) sdp(n2);
+      }
+      __syncwarp();
+    }
     if (elect_one()) mma_commit_g<C>(&bars.acc_done);   // also drains every MMA issued above
     __syncwarp();
     // no MMA of the group may still run when the CTAs leave

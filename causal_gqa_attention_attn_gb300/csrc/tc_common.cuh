@@ -376,12 +376,20 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool a_mn_major,
          ((uint32_t)(M >> 4) << 24);
 }
 
-// Round-to-nearest TF32 (low 13 mantissa bits cleared), for operands this
-// code writes itself (P, dS, the TMEM copies of Q and dO).
+// Round to TF32 (10 mantissa bits; the low 13 bits of the fp32 pattern
+// cleared), to nearest with ties away from zero, for operands this code
+// writes itself (P, dS, the TMEM copies of Q, dO and K). On the sign-magnitude
+// bit pattern, adding half a TF32 unit in the last place (bit 12) and then
+// truncating rounds the magnitude to nearest, ties up; a mantissa carry moves
+// into the exponent, which is the correctly rounded next binade. Two integer
+// operations on the ALU pipe, where a conversion instruction per element
+// would queue behind the softmax's exponentials. (Finite inputs; the
+// softmax never produces an infinity or NaN operand.)
+__host__ __device__ __forceinline__ uint32_t tf32_rna_bits(uint32_t u) {
+  return (u + 0x1000u) & 0xffffe000u;
+}
 __device__ __forceinline__ float to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
+  return __uint_as_float(tf32_rna_bits(__float_as_uint(x)));
 }
 
 __device__ __forceinline__ float ex2(float x) {
