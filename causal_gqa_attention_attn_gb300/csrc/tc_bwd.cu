@@ -281,7 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- pass 1: chunk c in stage c & 1 ----
     for (int c = 0; ok && !GD && c < nk; ++c) {
       const int st = c & 1;
-      if (!unit_wait(2 * c) || !unit_wait(2 * c + 1) || !stage_free(st)) { ok = false; break; }
+      const int ust = st ? use1 : use0;   // the stage's earlier uses (its release to wait for)
+      if (!warp_wait4<kCl>(ust > 0 ? 3 : 2, &bars.full[(2 * c) % NU], ((2 * c) / NU) & 1,
+                           &bars.full[(2 * c + 1) % NU], ((2 * c + 1) / NU) & 1,
+                           &bars.s_free[st], (ust - 1) & 1, nullptr, 0u, abort, status, kSiteQmMma)) {
+        ok = false;
+        break;
+      }
       if (elect_one()) {
         issue_sdp(tmem + Cfg::p1_stage(st), Cfg::BK1, id_s1, unit_desc(2 * c), unit_desc(2 * c + 1));
         mma_commit_g<C>(&bars.s_full[st]);
@@ -325,10 +331,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = s & 1, j = s / Cfg::NSUB, h = s % Cfg::NSUB, s2 = s + 2;
       const int ikt = p2_base + 3 * j + 2;
       const int u = (st ? use1 : use0) + (s >> 1);      // this sub-chunk's use of stage st
-      if (!warp_wait<kCl>(&bars.s_free[st], u & 1, abort, status, kSiteQmMma) ||
-          (h == 0 && !unit_wait(ikt)) || (s2 < n_sub && !kv_wait(s2))) {
-        ok = false;
-        break;
+      // dS(s) handed back, K^T of s's chunk (first sub-chunk) and K, V of
+      // s2's chunk (its first sub-chunk), waited for side by side
+      {
+        const int ik2 = p2_base + 3 * (s2 / Cfg::NSUB);
+        uint64_t* w1 = nullptr; uint64_t* w2 = nullptr; uint64_t* w3 = nullptr;
+        uint32_t p1 = 0, p2 = 0, p3 = 0;
+        int nw = 1;
+        auto add = [&](int unit) {
+          uint64_t* b = &bars.full[unit % NU];
+          const uint32_t p = (unit / NU) & 1;
+          if (nw == 1) { w1 = b; p1 = p; } else if (nw == 2) { w2 = b; p2 = p; } else { w3 = b; p3 = p; }
+          ++nw;
+        };
+        if (h == 0) add(ikt);
+        if (s2 < n_sub && s2 % Cfg::NSUB == 0) { add(ik2); add(ik2 + 1); }
+        if (!warp_wait4<kCl>(nw, &bars.s_free[st], u & 1, w1, p1, w2, p2, w3, p3, abort, status,
+                             kSiteQmMma)) {
+          ok = false;
+          break;
+        }
       }
       const uint32_t a_ds = tmem + Cfg::p2_stage(st), d_q = tmem + Cfg::T_DQ;
       const uint64_t bkt = unit_desc(ikt);
@@ -867,9 +889,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int m = 0; ok && exists(m); ++m) {
       const int n2 = m + 2;
       const bool more = exists(n2);
-      if (!warp_wait<kCl>(&bars.p_ready[m & 1], (m >> 1) & 1, abort, status, kSiteKmMma) ||
-          !landed(&bars.t_full[m % Cfg::NST], (m / Cfg::NST) & 1) ||
-          (more && !landed(&bars.qdo_full[n2 % Cfg::NSQ], (n2 / Cfg::NSQ) & 1))) {
+      // block m's softmax, its Q^T / dO^T tiles and block m+2's Q / dO tiles, side by side
+      if (!warp_wait4<kCl>(more ? 3 : 2, &bars.p_ready[m & 1], (m >> 1) & 1,
+                           &bars.t_full[m % Cfg::NST], (m / Cfg::NST) & 1,
+                           &bars.qdo_full[n2 % Cfg::NSQ], (n2 / Cfg::NSQ) & 1, nullptr, 0u,
+                           abort, status, kSiteKmMma)) {
         ok = false;
         break;
       }
