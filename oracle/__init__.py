@@ -44,7 +44,22 @@ query rows at a time (keys 0 .. last row of the block), which bounds memory;
 every row is computed from its own definition, so the block size changes
 nothing but rounding order inside the library matrix products.
 
-Pins: every function here is checked by ``tests/test_oracle_pins.py`` against
+Decode-style backward from saved probabilities (rullama ``training.rs``,
+``attention_backward_dq_chained`` / ``attention_backward_dkv_chained``; the
+page gives their buffer bindings and launch shapes, not the kernel bodies):
+one query per head against history_len cached keys, with the softmax
+probabilities of the forward stored instead of an LSE. Reading taken: the
+probabilities are softmax_j(sigma q_h . k_j), ``d_scores`` is the gradient
+with respect to those scores, and sigma is an argument (the page's parameter
+block has none; 1/sqrt(d) is the usual value):
+    dP_hj = d_out_h . v_j,   D_h = sum_j probs_hj dP_hj
+    d_scores_hj = probs_hj (dP_hj - D_h)
+    d_q_h  += sigma sum_j d_scores_hj k_j
+    d_k_j  += sigma sum_{h in group} d_scores_hj q_h
+    d_v_j  += sum_{h in group} probs_hj d_out_h
+
+Pins: every function here is checked by ``tests/test_oracle_pins.py`` (and
+``tests/test_oracle_decode.py`` for the decode backward) against
 central finite differences, closed forms (K = 0, S = 1, position 0), exact
 invariants (sum_j dS_ij = 0, no cross-document flow, GQA group sums) and an
 independent float64 autograd of the forward definition.
@@ -60,7 +75,7 @@ if "numpy" not in sys.modules:      # the pool below supplies the parallelism
 import numpy as np  # noqa: E402
 
 __all__ = ["fwd", "bwd", "bwd_rows", "bwd_dkdv_keys", "row_terms", "rope_bwd",
-           "allowed"]
+           "allowed", "decode_bwd"]
 
 _ROW_BLOCK = 256
 
@@ -299,3 +314,46 @@ def rope_bwd(dX, n_heads, head_dim, pos_offset=0, base=10000.0):
     X[..., 0] = x0 * c + x1 * s
     X[..., 1] = -x0 * s + x1 * c
     return X.reshape(S, n_heads * d)
+
+
+def decode_bwd(q, k_hist, v_hist, probs, d_out, n_heads, n_kv_heads, head_dim, scale):
+    """Decode-style attention backward from saved probabilities, in fp64.
+
+    rullama ``training.rs``, ``attention_backward_dq_chained`` (pass 1: d_q and
+    the staged d_scores [n_heads, history_len] from k_hist, v_hist, probs,
+    d_out) and ``attention_backward_dkv_chained`` (pass 2: d_k_hist, d_v_hist
+    from q, probs, d_out, d_scores). Layouts: q, d_out [H*d]; k_hist, v_hist
+    [L, Hk*d] (row-major, kv head g in columns g*d .. g*d+d-1); probs [H, L].
+    Per query head h with kv head g = h // (H/Hk), written out from the softmax
+    backward (module docstring):
+        dP = V_g d_out_h;  D = probs_h . dP;  d_scores_h = probs_h * (dP - D)
+        d_q_h = sigma K_g^T d_scores_h
+        d_k[:, g] += sigma outer(d_scores_h, q_h);  d_v[:, g] += outer(probs_h, d_out_h)
+    Returns (d_scores [H, L], d_q [H*d], d_k [L, Hk*d], d_v [L, Hk*d]) as new
+    fp64 arrays (the gradients' contributions, to be added by the caller).
+    """
+    H, Hk, d = n_heads, n_kv_heads, head_dim
+    if H % Hk:
+        raise ValueError("n_heads must be a multiple of n_kv_heads")
+    G = H // Hk
+    q, d_out = _f64(q).reshape(H * d), _f64(d_out).reshape(H * d)
+    K, V, P = _f64(k_hist), _f64(v_hist), _f64(probs)
+    L = K.shape[0]
+    if K.shape != (L, Hk * d) or V.shape != (L, Hk * d) or P.shape != (H, L):
+        raise ValueError("shape mismatch")
+    d_scores = np.zeros((H, L))
+    d_q = np.zeros(H * d)
+    d_k = np.zeros((L, Hk * d))
+    d_v = np.zeros((L, Hk * d))
+    for h in range(H):
+        g = h // G
+        Kg, Vg = K[:, _head_cols(g, d)], V[:, _head_cols(g, d)]
+        qh, oh = q[_head_cols(h, d)], d_out[_head_cols(h, d)]
+        dP = Vg @ oh
+        D = P[h] @ dP
+        ds = P[h] * (dP - D)
+        d_scores[h] = ds
+        d_q[_head_cols(h, d)] = scale * (Kg.T @ ds)
+        d_k[:, _head_cols(g, d)] += scale * np.outer(ds, qh)
+        d_v[:, _head_cols(g, d)] += np.outer(P[h], oh)
+    return d_scores, d_q, d_k, d_v
