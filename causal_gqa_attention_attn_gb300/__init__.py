@@ -16,7 +16,8 @@ import os
 
 __all__ = ["GqaError", "lib", "lib_path", "attn_fwd_lse", "attn_bwd", "attn_bwd_simt",
            "rope_bwd_inplace", "workspace_bytes", "read_device_status", "n_pairs_from_seg",
-           "profile_events", "profile_stage_name", "launch_count", "attn_bwd_noalloc"]
+           "profile_events", "profile_stage_name", "launch_count", "attn_bwd_noalloc",
+           "attn_fwd", "attn_bwd_rope", "attn_bwd_o", "attn_decode_bwd"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libgqa_attn.so")
@@ -50,6 +51,9 @@ def lib() -> ctypes.CDLL:
     L.attn_fwd.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
     L.attn_fwd_workspace_bytes.argtypes = [I, I, I, I]
     L.attn_fwd_workspace_bytes.restype = Z
+    L.attn_decode_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
+    L.attn_decode_bwd_workspace_bytes.argtypes = [I, I, I, I]
+    L.attn_decode_bwd_workspace_bytes.restype = Z
     bwd_args = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
     L.attn_bwd.argtypes = bwd_args
     L.attn_bwd_simt.argtypes = bwd_args
@@ -74,7 +78,7 @@ def lib() -> ctypes.CDLL:
     L.gqa_last_error.argtypes = []
     L.gqa_last_error.restype = ctypes.c_char_p
     for name in ("attn_fwd_lse", "attn_fwd", "attn_bwd", "attn_bwd_simt", "attn_bwd_rope", "attn_bwd_o",
-                 "rope_bwd_inplace", "attn_read_device_status"):
+                 "attn_decode_bwd", "rope_bwd_inplace", "attn_read_device_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -156,6 +160,38 @@ def attn_fwd(Q, K, V, seg, n_heads, n_kv_heads, head_dim, scale, O=None, LSE=Non
                           _ptr(workspace, "workspace", (torch.uint8,)), workspace.numel(),
                           _stream(stream)))
     return O, LSE
+
+
+def attn_decode_bwd(q, k_hist, v_hist, probs, d_out, n_heads, n_kv_heads, head_dim, scale,
+                    d_q=None, d_k_hist=None, d_v_hist=None, d_scores=None, workspace=None,
+                    stream=None):
+    """Decode-style backward from saved probabilities (one query per head vs the
+    key history): returns (d_scores, d_q, d_k_hist, d_v_hist). d_q, d_k_hist,
+    d_v_hist accumulate into the tensors passed (zeros when omitted); d_scores
+    is overwritten. q, d_out [n_heads*head_dim]; k_hist, v_hist
+    [history_len, n_kv_heads*head_dim]; probs [n_heads, history_len]."""
+    torch = _torch()
+    L = k_hist.shape[0]
+    dev = k_hist.device
+    if d_q is None:
+        d_q = torch.zeros(n_heads * head_dim, device=dev, dtype=torch.float32)
+    if d_k_hist is None:
+        d_k_hist = torch.zeros(L, n_kv_heads * head_dim, device=dev, dtype=torch.float32)
+    if d_v_hist is None:
+        d_v_hist = torch.zeros(L, n_kv_heads * head_dim, device=dev, dtype=torch.float32)
+    if d_scores is None:
+        d_scores = torch.empty(n_heads, L, device=dev, dtype=torch.float32)
+    need = int(lib().attn_decode_bwd_workspace_bytes(L, n_heads, n_kv_heads, head_dim))
+    if workspace is None:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    _check(lib().attn_decode_bwd(_f32(q, "q"), _f32(k_hist, "k_hist"), _f32(v_hist, "v_hist"),
+                                 _f32(probs, "probs"), _f32(d_out, "d_out"),
+                                 _f32(d_scores, "d_scores"), _f32(d_q, "d_q"),
+                                 _f32(d_k_hist, "d_k_hist"), _f32(d_v_hist, "d_v_hist"), L,
+                                 n_heads, n_kv_heads, head_dim, float(scale),
+                                 _ptr(workspace, "workspace", (torch.uint8,)), workspace.numel(),
+                                 _stream(stream)))
+    return d_scores, d_q, d_k_hist, d_v_hist
 
 
 def _bwd(fn, Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_dim, scale,

@@ -155,6 +155,34 @@ gqa_status attn_fwd(const float* Q, const float* K, const float* V, const uint32
   return tc_fwd(Q, K, V, seg, O, LSE, sh, (char*)workspace, st);
 }
 
+size_t attn_decode_bwd_workspace_bytes(int history_len, int n_heads, int n_kv_heads, int head_dim) {
+  if (history_len <= 0 || n_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0) return kWsHeader;
+  return decode_ws_bytes(history_len, n_heads, head_dim);
+}
+
+gqa_status attn_decode_bwd(const float* q, const float* k_hist, const float* v_hist,
+                           const float* probs, const float* d_out, float* d_scores, float* d_q,
+                           float* d_k_hist, float* d_v_hist, int history_len, int n_heads,
+                           int n_kv_heads, int head_dim, float scale, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  gqa_status r = check_attn_args(history_len, n_heads, n_kv_heads, head_dim, scale, 128);
+  if (r != GQA_OK) return r;
+  if (head_dim % 32 != 0)
+    return set_error(GQA_ERR_UNSUPPORTED, "decode backward: head_dim %d not in {32, 64, 96, 128}", head_dim);
+  if (n_kv_heads > 65535)
+    return set_error(GQA_ERR_UNSUPPORTED, "decode backward: n_kv_heads %d > 65535", n_kv_heads);
+  if (history_len == 0) return GQA_OK;
+  const void* p[] = {q, k_hist, v_hist, probs, d_out, d_scores, d_q, d_k_hist, d_v_hist, workspace};
+  const char* nm[] = {"q", "k_hist", "v_hist", "probs", "d_out", "d_scores", "d_q", "d_k_hist",
+                      "d_v_hist", "workspace"};
+  if ((r = check_ptrs(p, nm, 10)) != GQA_OK) return r;
+  const size_t need = attn_decode_bwd_workspace_bytes(history_len, n_heads, n_kv_heads, head_dim);
+  if (workspace_bytes < need)
+    return set_error(GQA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  return decode_bwd(q, k_hist, v_hist, probs, d_out, d_scores, d_q, d_k_hist, d_v_hist, history_len,
+                    n_heads, n_kv_heads, head_dim, scale, (char*)workspace, (cudaStream_t)stream);
+}
+
 gqa_status attn_bwd_simt(const float* Q, const float* K, const float* V, const float* dO,
                          const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
                          int seq_len, int n_heads, int n_kv_heads, int head_dim, float scale,

@@ -130,6 +130,11 @@ gqa_status tc_fwd(const float* Q, const float* K, const float* V, const uint32_t
                   float* LSE, const Shape& sh, char* ws, cudaStream_t st);
 
 // RoPE backward, rope_bwd.cu
+size_t decode_ws_bytes(int L, int H, int d);
+gqa_status decode_bwd(const float* q, const float* k_hist, const float* v_hist, const float* probs,
+                      const float* d_out, float* d_scores, float* d_q, float* d_k, float* d_v,
+                      int L, int H, int Hk, int d, float scale, char* ws, cudaStream_t st);
+
 gqa_status rope_bwd_launch(float* X, int S, int H, int d, int pos_offset, float base,
                            cudaStream_t st);
 

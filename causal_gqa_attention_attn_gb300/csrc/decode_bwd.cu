@@ -1,0 +1,285 @@
+// Decode-style attention backward from saved probabilities: one query per
+// head against history_len cached keys (rullama training.rs,
+// attention_backward_dq_chained: d_q and the staged d_scores [n_heads,
+// history_len] from k_hist, v_hist, probs, d_out; attention_backward_dkv_chained:
+// d_k_hist, d_v_hist from q, probs, d_out, d_scores). With G = H / Hk query
+// heads per kv head g and scale sigma:
+//   dP_hj = d_out_h . v_j,   D_h = sum_j probs_hj dP_hj
+//   d_scores_hj = probs_hj (dP_hj - D_h)         (gradient of the scores sigma q.k)
+//   d_q_h += sigma sum_j d_scores_hj k_j
+//   d_k_j += sigma sum_{h in g} d_scores_hj q_h,   d_v_j += sum_{h in g} probs_hj d_out_h
+//
+// The work is a few passes over the key history, so HBM decides the time:
+// every key row is read once per pass for all G heads of its group. CTA =
+// (block of 32 or 64 keys, kv head); a warp holds 4 or 8 key rows in
+// registers, each lane d/32 columns of them.
+//  decode_dp:   dP for the block's keys and the group's heads, staged in
+//               d_scores; per-CTA partial sums of probs * dP.
+//  decode_dsum: D_h = the partial sums added in a fixed order.
+//  decode_dkv:  d_scores from the staged dP; one owned += of the block's
+//               d_k / d_v rows; per-CTA partial d_q.
+//  decode_dq:   d_q += the partials added in a fixed order.
+// No atomics: results do not depend on scheduling.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kDecWarps = 8;
+constexpr int kDecThreads = 32 * kDecWarps;
+// key rows per warp: 8, or 4 for head_dim >= 96, so that the key rows and the
+// dK / dV accumulators of decode_dkv leave registers for two CTAs per SM
+__host__ __device__ constexpr int dec_kpw(int E) { return E >= 3 ? 4 : 8; }
+__host__ __device__ constexpr int dec_keys(int E) { return kDecWarps * dec_kpw(E); }
+
+struct DecWs {
+  int nblk;
+  size_t dpart, dsum, qpart, total;
+};
+
+DecWs dec_ws(int L, int H, int d) {
+  DecWs w;
+  const int keys = dec_keys(d / 32);
+  w.nblk = (L + keys - 1) / keys;
+  w.dpart = kWsHeader;
+  w.dsum = w.dpart + align256((size_t)w.nblk * H * sizeof(float));
+  w.qpart = w.dsum + align256((size_t)H * sizeof(float));
+  w.total = w.qpart + align256((size_t)w.nblk * H * d * sizeof(float));
+  return w;
+}
+
+// this lane's E consecutive columns of a row (16-byte aligned when E = 4)
+template <int E>
+__device__ __forceinline__ void load_cols(const float* p, float* v) {
+  if constexpr (E == 4) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  } else if constexpr (E == 2) {
+    const float2 x = __ldg(reinterpret_cast<const float2*>(p));
+    v[0] = x.x; v[1] = x.y;
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = __ldg(p + e);
+  }
+}
+
+// p[0 .. E) += v[0 .. E) (one vector access per lane when E = 2 or 4)
+template <int E>
+__device__ __forceinline__ void add_cols(float* p, const float* v) {
+  if constexpr (E == 4) {
+    float4* q = reinterpret_cast<float4*>(p);
+    float4 x = *q;
+    x.x += v[0]; x.y += v[1]; x.z += v[2]; x.w += v[3];
+    *q = x;
+  } else if constexpr (E == 2) {
+    float2* q = reinterpret_cast<float2*>(p);
+    float2 x = *q;
+    x.x += v[0]; x.y += v[1];
+    *q = x;
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) p[e] += v[e];
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+template <int E>
+__global__ void __launch_bounds__(kDecThreads) decode_dp(const float* __restrict__ V,
+                                                         const float* __restrict__ probs,
+                                                         const float* __restrict__ d_out,
+                                                         float* __restrict__ dsc,
+                                                         float* __restrict__ dpart, int L, int H,
+                                                         int Hk, int G) {
+  constexpr int D = 32 * E, KPW = dec_kpw(E);
+  extern __shared__ float red[];                  // [kDecWarps][G] per-warp partial sums
+  const int g = blockIdx.y, blk = blockIdx.x;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int j0 = blk * dec_keys(E) + warp * KPW;
+  float v[KPW][E];
+#pragma unroll
+  for (int k = 0; k < KPW; ++k) {
+    const int j = j0 + k;
+    if (j < L) load_cols<E>(V + ((long long)j * Hk + g) * D + lane * E, v[k]);
+    else
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[k][e] = 0.f;
+  }
+  for (int hh = 0; hh < G; ++hh) {
+    const int h = g * G + hh;
+    float o[E];
+    load_cols<E>(d_out + (long long)h * D + lane * E, o);
+    float mine = 0.f, psum = 0.f;                 // lane k keeps dP of key k
+#pragma unroll
+    for (int k = 0; k < KPW; ++k) {
+      float x = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) x = fmaf(o[e], v[k][e], x);
+      x = warp_sum(x);
+      const int j = j0 + k;
+      if (lane == k) mine = x;
+      if (j < L) psum = fmaf(__ldg(probs + (long long)h * L + j), x, psum);
+    }
+    if (lane < KPW && j0 + lane < L) dsc[(long long)h * L + j0 + lane] = mine;
+    if (lane == 0) red[warp * G + hh] = psum;
+  }
+  __syncthreads();
+  for (int hh = threadIdx.x; hh < G; hh += kDecThreads) {
+    float s = 0.f;
+    for (int w = 0; w < kDecWarps; ++w) s += red[w * G + hh];
+    dpart[(long long)blk * H + g * G + hh] = s;
+  }
+}
+
+__global__ void __launch_bounds__(256) decode_dsum(const float* __restrict__ dpart,
+                                                   float* __restrict__ dsum, int nblk, int H) {
+  __shared__ float part[256];
+  const int h = blockIdx.x;
+  float s = 0.f;
+  for (int b = threadIdx.x; b < nblk; b += 256) s += dpart[(long long)b * H + h];
+  part[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = 128; w >= 1; w >>= 1) {
+    if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) dsum[h] = part[0];
+}
+
+template <int E>
+__global__ void __launch_bounds__(kDecThreads) decode_dkv(
+    const float* __restrict__ q, const float* __restrict__ K, const float* __restrict__ probs,
+    const float* __restrict__ d_out, float* __restrict__ dsc, const float* __restrict__ dsum,
+    float* __restrict__ dK, float* __restrict__ dV, float* __restrict__ qpart, int L, int H,
+    int Hk, int G, float scale) {
+  constexpr int D = 32 * E, KPW = dec_kpw(E);
+  __shared__ float qred[kDecWarps][D];
+  const int g = blockIdx.y, blk = blockIdx.x;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int j0 = blk * dec_keys(E) + warp * KPW;
+  float kr[KPW][E], dk[KPW][E], dv[KPW][E];
+#pragma unroll
+  for (int k = 0; k < KPW; ++k) {
+    const int j = j0 + k;
+    if (j < L) load_cols<E>(K + ((long long)j * Hk + g) * D + lane * E, kr[k]);
+    else
+#pragma unroll
+      for (int e = 0; e < E; ++e) kr[k][e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) dk[k][e] = dv[k][e] = 0.f;
+  }
+  for (int hh = 0; hh < G; ++hh) {
+    const int h = g * G + hh;
+    float qh[E], oh[E], qa[E];
+    load_cols<E>(q + (long long)h * D + lane * E, qh);
+    load_cols<E>(d_out + (long long)h * D + lane * E, oh);
+#pragma unroll
+    for (int e = 0; e < E; ++e) qa[e] = 0.f;
+    const float Dh = __ldg(dsum + h);
+    float mine = 0.f;                             // lane k keeps d_scores of key k
+#pragma unroll
+    for (int k = 0; k < KPW; ++k) {
+      const int j = j0 + k;
+      const bool ok = j < L;
+      const float p = ok ? __ldg(probs + (long long)h * L + j) : 0.f;
+      const float dp = ok ? dsc[(long long)h * L + j] : 0.f;   // staged by decode_dp
+      const float ds = p * (dp - Dh);
+      if (lane == k) mine = ds;
+      const float sds = scale * ds;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        dk[k][e] = fmaf(sds, qh[e], dk[k][e]);
+        dv[k][e] = fmaf(p, oh[e], dv[k][e]);
+        qa[e] = fmaf(sds, kr[k][e], qa[e]);
+      }
+    }
+    __syncwarp();                                 // every lane has read the staged dP
+    if (lane < KPW && j0 + lane < L) dsc[(long long)h * L + j0 + lane] = mine;
+#pragma unroll
+    for (int e = 0; e < E; ++e) qred[warp][lane * E + e] = qa[e];
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += kDecThreads) {
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) s += qred[w][c];
+      qpart[((long long)blk * H + h) * D + c] = s;
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int k = 0; k < KPW; ++k) {
+    const int j = j0 + k;
+    if (j >= L) continue;
+    const long long off = ((long long)j * Hk + g) * D + lane * E;
+    add_cols<E>(dK + off, dk[k]);
+    add_cols<E>(dV + off, dv[k]);
+  }
+}
+
+__global__ void __launch_bounds__(128) decode_dq(const float* __restrict__ qpart,
+                                                 float* __restrict__ dq, int nblk, int H, int D) {
+  const int h = blockIdx.x;
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    float s = 0.f;
+    for (int b = 0; b < nblk; ++b) s += qpart[((long long)b * H + h) * D + c];
+    dq[(long long)h * D + c] += s;
+  }
+}
+
+template <int E>
+gqa_status decode_launch(const float* q, const float* k_hist, const float* v_hist,
+                         const float* probs, const float* d_out, float* d_scores, float* d_q,
+                         float* d_k, float* d_v, int L, int H, int Hk, float scale, char* ws,
+                         cudaStream_t st) {
+  constexpr int D = 32 * E;
+  const DecWs w = dec_ws(L, H, D);
+  const int G = H / Hk;
+  float* dpart = reinterpret_cast<float*>(ws + w.dpart);
+  float* dsum = reinterpret_cast<float*>(ws + w.dsum);
+  float* qpart = reinterpret_cast<float*>(ws + w.qpart);
+  const dim3 grid((unsigned)w.nblk, (unsigned)Hk);
+  const size_t red_bytes = (size_t)kDecWarps * G * sizeof(float);
+  if (red_bytes > 48 * 1024 &&
+      cudaFuncSetAttribute(decode_dp<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)red_bytes) != cudaSuccess)
+    return check_launch("decode dP smem attribute");
+  decode_dp<E><<<grid, kDecThreads, red_bytes, st>>>(v_hist, probs, d_out, d_scores, dpart, L, H,
+                                                     Hk, G);
+  note_launch();
+  gqa_status r;
+  if ((r = check_launch("decode dP")) != GQA_OK) return r;
+  decode_dsum<<<H, 256, 0, st>>>(dpart, dsum, w.nblk, H);
+  note_launch();
+  if ((r = check_launch("decode D")) != GQA_OK) return r;
+  decode_dkv<E><<<grid, kDecThreads, 0, st>>>(q, k_hist, probs, d_out, d_scores, dsum, d_k, d_v,
+                                              qpart, L, H, Hk, G, scale);
+  note_launch();
+  if ((r = check_launch("decode dK dV")) != GQA_OK) return r;
+  decode_dq<<<H, 128, 0, st>>>(qpart, d_q, w.nblk, H, D);
+  note_launch();
+  return check_launch("decode dQ");
+}
+
+}  // namespace
+
+size_t decode_ws_bytes(int L, int H, int d) { return dec_ws(L, H, d).total; }
+
+gqa_status decode_bwd(const float* q, const float* k_hist, const float* v_hist, const float* probs,
+                      const float* d_out, float* d_scores, float* d_q, float* d_k, float* d_v,
+                      int L, int H, int Hk, int d, float scale, char* ws, cudaStream_t st) {
+  switch (d) {
+    case 32: return decode_launch<1>(q, k_hist, v_hist, probs, d_out, d_scores, d_q, d_k, d_v, L, H, Hk, scale, ws, st);
+    case 64: return decode_launch<2>(q, k_hist, v_hist, probs, d_out, d_scores, d_q, d_k, d_v, L, H, Hk, scale, ws, st);
+    case 96: return decode_launch<3>(q, k_hist, v_hist, probs, d_out, d_scores, d_q, d_k, d_v, L, H, Hk, scale, ws, st);
+    case 128: return decode_launch<4>(q, k_hist, v_hist, probs, d_out, d_scores, d_q, d_k, d_v, L, H, Hk, scale, ws, st);
+    default: return set_error(GQA_ERR_UNSUPPORTED, "decode backward: head_dim %d not in {32, 64, 96, 128}", d);
+  }
+}
+
+}  // namespace gqa

@@ -78,6 +78,37 @@ gqa_status attn_fwd(const float* Q, const float* K, const float* V, const uint32
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_decode_bwd_workspace_bytes / attn_decode_bwd — decode-style attention
+ * backward from saved probabilities: one query per head against history_len
+ * cached keys (rullama training.rs, attention_backward_dq_chained: d_q and the
+ * staged d_scores from k_hist, v_hist, probs, d_out; attention_backward_dkv_chained:
+ * d_k_hist, d_v_hist from q, probs, d_out, d_scores). The page gives the
+ * bindings and launch shapes only; the arithmetic is the softmax backward of
+ * probs = softmax_j(scale * q_h . k_j), kv head g(h) = h / (n_heads / n_kv_heads):
+ *   dP[h, j]       = d_out_h . v_j,   D_h = sum_j probs[h, j] dP[h, j]
+ *   d_scores[h, j] = probs[h, j] (dP[h, j] - D_h)      (gradient of the scores)
+ *   d_q_h      += scale * sum_j d_scores[h, j] k_j
+ *   d_k_hist_j += scale * sum_{h in g} d_scores[h, j] q_h
+ *   d_v_hist_j += sum_{h in g} probs[h, j] d_out_h
+ * Layouts (row-major fp32, device memory, caller-owned): q, d_out, d_q
+ * [n_heads * head_dim]; k_hist, v_hist, d_k_hist, d_v_hist
+ * [history_len, n_kv_heads * head_dim]; probs, d_scores [n_heads, history_len].
+ * d_q, d_k_hist, d_v_hist accumulate (+=); d_scores is overwritten (it also
+ * stages dP between the passes). probs is used as given (its rows need not
+ * sum to one). head_dim in {32, 64, 96, 128} (else GQA_ERR_UNSUPPORTED);
+ * n_kv_heads <= 65535; every pointer non-NULL and 16-byte aligned;
+ * workspace >= attn_decode_bwd_workspace_bytes(...) bytes, any contents.
+ * history_len == 0 is a no-op. Deterministic (no atomics); CUDA cores,
+ * bound by HBM bandwidth. Errors are returned before any launch.
+ */
+size_t attn_decode_bwd_workspace_bytes(int history_len, int n_heads, int n_kv_heads, int head_dim);
+gqa_status attn_decode_bwd(const float* q, const float* k_hist, const float* v_hist,
+                           const float* probs, const float* d_out, float* d_scores, float* d_q,
+                           float* d_k_hist, float* d_v_hist, int history_len, int n_heads,
+                           int n_kv_heads, int head_dim, float scale, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
  * attn_bwd_workspace_bytes — bytes of device workspace attn_bwd needs for this
  * shape (a multiple of 256). The caller allocates it (any contents) and may
  * reuse it across calls that do not overlap on the GPU.

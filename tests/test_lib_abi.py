@@ -145,6 +145,26 @@ def test_tensor_core_forward_rejects_bad_arguments(L):
     assert L.attn_fwd_workspace_bytes(4096, 32, 8, 100) == 256
 
 
+def test_decode_backward_rejects_bad_arguments(L):
+    def call(Lh=64, H=4, Hk=2, d=32, s=0.2, ptrs=None, ws_bytes=None):
+        p = [FAKE] * 10 if ptrs is None else ptrs
+        if ws_bytes is None:
+            ws_bytes = L.attn_decode_bwd_workspace_bytes(Lh, H, Hk, d)
+        return L.attn_decode_bwd(*p[:9], Lh, H, Hk, d, s, p[9], ws_bytes, None)
+    assert call(H=5) == 1 and call(Hk=0) == 1 and call(Lh=-1) == 1 and call(Lh=0) == 0
+    assert call(d=30) == 1 and call(d=36) == 2 and call(d=160) == 2 and call(s=float("nan")) == 1
+    assert call(ws_bytes=16) == 1
+    for k in range(10):
+        p = [FAKE] * 10
+        p[k] = None
+        assert call(ptrs=p) == 1
+    p = [FAKE] * 10
+    p[3] = FAKE + 4                                   # probs not 16-byte aligned
+    assert call(ptrs=p) == 1
+    # per-block partial sums of D and of d_q, after the status header
+    assert L.attn_decode_bwd_workspace_bytes(16384, 32, 8, 128) >= 256 + 512 * 32 * 128 * 4
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ga, "_lib", None)
     monkeypatch.setattr(ga, "_LIB_PATH", str(tmp_path / "missing.so"))
