@@ -50,37 +50,32 @@ DecWs dec_ws(int L, int H, int d) {
   return w;
 }
 
-// this lane's E consecutive columns of a row (16-byte aligned when E = 4)
-template <int E>
+// this lane's E consecutive columns of a row (16-byte aligned when E = 4),
+// through the read-only path (RO) for data no kernel of the call writes
+template <int E, bool RO = true>
 __device__ __forceinline__ void load_cols(const float* p, float* v) {
   if constexpr (E == 4) {
-    const float4 x = __ldg(reinterpret_cast<const float4*>(p));
+    const float4 x = RO ? __ldg(reinterpret_cast<const float4*>(p)) : *reinterpret_cast<const float4*>(p);
     v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
   } else if constexpr (E == 2) {
-    const float2 x = __ldg(reinterpret_cast<const float2*>(p));
+    const float2 x = RO ? __ldg(reinterpret_cast<const float2*>(p)) : *reinterpret_cast<const float2*>(p);
     v[0] = x.x; v[1] = x.y;
   } else {
 #pragma unroll
-    for (int e = 0; e < E; ++e) v[e] = __ldg(p + e);
+    for (int e = 0; e < E; ++e) v[e] = RO ? __ldg(p + e) : p[e];
   }
 }
 
-// p[0 .. E) += v[0 .. E) (one vector access per lane when E = 2 or 4)
+// p[0 .. E) = v[0 .. E) (one vector store per lane when E = 2 or 4)
 template <int E>
-__device__ __forceinline__ void add_cols(float* p, const float* v) {
+__device__ __forceinline__ void store_cols(float* p, const float* v) {
   if constexpr (E == 4) {
-    float4* q = reinterpret_cast<float4*>(p);
-    float4 x = *q;
-    x.x += v[0]; x.y += v[1]; x.z += v[2]; x.w += v[3];
-    *q = x;
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
   } else if constexpr (E == 2) {
-    float2* q = reinterpret_cast<float2*>(p);
-    float2 x = *q;
-    x.x += v[0]; x.y += v[1];
-    *q = x;
+    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
   } else {
 #pragma unroll
-    for (int e = 0; e < E; ++e) p[e] += v[e];
+    for (int e = 0; e < E; ++e) p[e] = v[e];
   }
 }
 
@@ -111,23 +106,28 @@ __global__ void __launch_bounds__(kDecThreads) decode_dp(const float* __restrict
 #pragma unroll
       for (int e = 0; e < E; ++e) v[k][e] = 0.f;
   }
-  for (int hh = 0; hh < G; ++hh) {
-    const int h = g * G + hh;
-    float o[E];
-    load_cols<E>(d_out + (long long)h * D + lane * E, o);
-    float mine = 0.f, psum = 0.f;                 // lane k keeps dP of key k
+  constexpr int HC = 32 / KPW;                    // heads per chunk: one probs value per lane
+  for (int c0 = 0; c0 < G; c0 += HC) {
+    // lane l: probs of head c0 + l / KPW, key j0 + l % KPW (0 past the ends)
+    const int lh = c0 + lane / KPW, lj = j0 + lane % KPW;
+    const float pl = (lh < G && lj < L) ? __ldg(probs + (long long)(g * G + lh) * L + lj) : 0.f;
+    for (int hh = c0; hh < G && hh < c0 + HC; ++hh) {
+      const int h = g * G + hh;
+      float o[E];
+      load_cols<E>(d_out + (long long)h * D + lane * E, o);
+      float mine = 0.f, psum = 0.f;               // lane k keeps dP of key k
 #pragma unroll
-    for (int k = 0; k < KPW; ++k) {
-      float x = 0.f;
+      for (int k = 0; k < KPW; ++k) {
+        float x = 0.f;
 #pragma unroll
-      for (int e = 0; e < E; ++e) x = fmaf(o[e], v[k][e], x);
-      x = warp_sum(x);
-      const int j = j0 + k;
-      if (lane == k) mine = x;
-      if (j < L) psum = fmaf(__ldg(probs + (long long)h * L + j), x, psum);
+        for (int e = 0; e < E; ++e) x = fmaf(o[e], v[k][e], x);
+        x = warp_sum(x);
+        if (lane == k) mine = x;
+        psum = fmaf(__shfl_sync(0xffffffffu, pl, (hh - c0) * KPW + k), x, psum);
+      }
+      if (lane < KPW && j0 + lane < L) dsc[(long long)h * L + j0 + lane] = mine;
+      if (lane == 0) red[warp * G + hh] = psum;
     }
-    if (lane < KPW && j0 + lane < L) dsc[(long long)h * L + j0 + lane] = mine;
-    if (lane == 0) red[warp * G + hh] = psum;
   }
   __syncthreads();
   for (int hh = threadIdx.x; hh < G; hh += kDecThreads) {
@@ -159,56 +159,73 @@ __global__ void __launch_bounds__(kDecThreads) decode_dkv(
     float* __restrict__ dK, float* __restrict__ dV, float* __restrict__ qpart, int L, int H,
     int Hk, int G, float scale) {
   constexpr int D = 32 * E, KPW = dec_kpw(E);
-  __shared__ float qred[kDecWarps][D];
+  constexpr int HC = 32 / KPW;                    // heads per chunk: one value per lane
+  __shared__ float qred[HC][kDecWarps][D];        // per-warp partial d_q of a chunk's heads
   const int g = blockIdx.y, blk = blockIdx.x;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int j0 = blk * dec_keys(E) + warp * KPW;
+  // the warp's key rows and their d_k / d_v rows, all loaded up front; the
+  // gradients accumulate onto the loaded rows and are stored once at the end
   float kr[KPW][E], dk[KPW][E], dv[KPW][E];
 #pragma unroll
   for (int k = 0; k < KPW; ++k) {
     const int j = j0 + k;
-    if (j < L) load_cols<E>(K + ((long long)j * Hk + g) * D + lane * E, kr[k]);
-    else
+    const long long off = ((long long)j * Hk + g) * D + lane * E;
+    if (j < L) {
+      load_cols<E>(K + off, kr[k]);
+      load_cols<E, false>(dK + off, dk[k]);   // rows this thread writes back below
+      load_cols<E, false>(dV + off, dv[k]);
+    } else {
 #pragma unroll
-      for (int e = 0; e < E; ++e) kr[k][e] = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) dk[k][e] = dv[k][e] = 0.f;
-  }
-  for (int hh = 0; hh < G; ++hh) {
-    const int h = g * G + hh;
-    float qh[E], oh[E], qa[E];
-    load_cols<E>(q + (long long)h * D + lane * E, qh);
-    load_cols<E>(d_out + (long long)h * D + lane * E, oh);
-#pragma unroll
-    for (int e = 0; e < E; ++e) qa[e] = 0.f;
-    const float Dh = __ldg(dsum + h);
-    float mine = 0.f;                             // lane k keeps d_scores of key k
-#pragma unroll
-    for (int k = 0; k < KPW; ++k) {
-      const int j = j0 + k;
-      const bool ok = j < L;
-      const float p = ok ? __ldg(probs + (long long)h * L + j) : 0.f;
-      const float dp = ok ? dsc[(long long)h * L + j] : 0.f;   // staged by decode_dp
-      const float ds = p * (dp - Dh);
-      if (lane == k) mine = ds;
-      const float sds = scale * ds;
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        dk[k][e] = fmaf(sds, qh[e], dk[k][e]);
-        dv[k][e] = fmaf(p, oh[e], dv[k][e]);
-        qa[e] = fmaf(sds, kr[k][e], qa[e]);
-      }
+      for (int e = 0; e < E; ++e) kr[k][e] = dk[k][e] = dv[k][e] = 0.f;
     }
-    __syncwarp();                                 // every lane has read the staged dP
-    if (lane < KPW && j0 + lane < L) dsc[(long long)h * L + j0 + lane] = mine;
+  }
+  for (int c0 = 0; c0 < G; c0 += HC) {
+    // lane l: probs and the staged dP (decode_dp) of head c0 + l / KPW, key
+    // j0 + l % KPW (0 past the ends), loaded before this chunk's d_scores
+    // overwrite the staged values
+    const int lh = c0 + lane / KPW, lj = j0 + lane % KPW;
+    const bool lok = lh < G && lj < L;
+    const float pl = lok ? __ldg(probs + (long long)(g * G + lh) * L + lj) : 0.f;
+    const float dl = lok ? dsc[(long long)(g * G + lh) * L + lj] : 0.f;
+    __syncwarp();
+    for (int hh = c0; hh < G && hh < c0 + HC; ++hh) {
+      const int h = g * G + hh;
+      float qh[E], oh[E], qa[E];
+      load_cols<E>(q + (long long)h * D + lane * E, qh);
+      load_cols<E>(d_out + (long long)h * D + lane * E, oh);
 #pragma unroll
-    for (int e = 0; e < E; ++e) qred[warp][lane * E + e] = qa[e];
+      for (int e = 0; e < E; ++e) qa[e] = 0.f;
+      const float Dh = __ldg(dsum + h);
+      float mine = 0.f;                           // lane k keeps d_scores of key k
+#pragma unroll
+      for (int k = 0; k < KPW; ++k) {
+        const int src = (hh - c0) * KPW + k;
+        const float p = __shfl_sync(0xffffffffu, pl, src);
+        const float dp = __shfl_sync(0xffffffffu, dl, src);
+        const float ds = p * (dp - Dh);
+        if (lane == k) mine = ds;
+        const float sds = scale * ds;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          dk[k][e] = fmaf(sds, qh[e], dk[k][e]);
+          dv[k][e] = fmaf(p, oh[e], dv[k][e]);
+          qa[e] = fmaf(sds, kr[k][e], qa[e]);
+        }
+      }
+      if (lane < KPW && j0 + lane < L) dsc[(long long)h * L + j0 + lane] = mine;
+#pragma unroll
+      for (int e = 0; e < E; ++e) qred[hh - c0][warp][lane * E + e] = qa[e];
+    }
+    // the chunk's partial d_q: warps added in a fixed order
     __syncthreads();
-    for (int c = threadIdx.x; c < D; c += kDecThreads) {
-      float s = 0.f;
+    const int nh = min(HC, G - c0);
+    for (int t = threadIdx.x; t < nh * D; t += kDecThreads) {
+      const int i = t / D, c = t % D;
+      float sum = 0.f;
 #pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) s += qred[w][c];
-      qpart[((long long)blk * H + h) * D + c] = s;
+      for (int w = 0; w < kDecWarps; ++w) sum += qred[i][w][c];
+      qpart[((long long)blk * H + g * G + c0 + i) * D + c] = sum;
     }
     __syncthreads();
   }
@@ -217,18 +234,30 @@ __global__ void __launch_bounds__(kDecThreads) decode_dkv(
     const int j = j0 + k;
     if (j >= L) continue;
     const long long off = ((long long)j * Hk + g) * D + lane * E;
-    add_cols<E>(dK + off, dk[k]);
-    add_cols<E>(dV + off, dv[k]);
+    store_cols<E>(dK + off, dk[k]);
+    store_cols<E>(dV + off, dv[k]);
   }
 }
 
-__global__ void __launch_bounds__(128) decode_dq(const float* __restrict__ qpart,
+// d_q[h, c] += sum over blocks of qpart[b, h, c]: grid (H, D / 32), warp w of
+// 8 adds blocks b = w, w + 8, ... of its lane's column, then the 8 warp sums
+// are added in warp order (a fixed order: the result does not depend on
+// scheduling).
+__global__ void __launch_bounds__(256) decode_dq(const float* __restrict__ qpart,
                                                  float* __restrict__ dq, int nblk, int H, int D) {
-  const int h = blockIdx.x;
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    float s = 0.f;
-    for (int b = 0; b < nblk; ++b) s += qpart[((long long)b * H + h) * D + c];
-    dq[(long long)h * D + c] += s;
+  __shared__ float part[8][32];
+  const int h = blockIdx.x, lane = threadIdx.x % 32, w = threadIdx.x / 32;
+  const int c = blockIdx.y * 32 + lane;
+  float s = 0.f;
+#pragma unroll 8
+  for (int b = w; b < nblk; b += 8) s += __ldg(qpart + ((long long)b * H + h) * D + c);
+  part[w][lane] = s;
+  __syncthreads();
+  if (w == 0) {
+    float t = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t += part[i][lane];
+    dq[(long long)h * D + c] += t;
   }
 }
 
@@ -261,7 +290,7 @@ gqa_status decode_launch(const float* q, const float* k_hist, const float* v_his
                                               qpart, L, H, Hk, G, scale);
   note_launch();
   if ((r = check_launch("decode dK dV")) != GQA_OK) return r;
-  decode_dq<<<H, 128, 0, st>>>(qpart, d_q, w.nblk, H, D);
+  decode_dq<<<dim3((unsigned)H, D / 32), 256, 0, st>>>(qpart, d_q, w.nblk, H, D);
   note_launch();
   return check_launch("decode dQ");
 }
