@@ -416,6 +416,142 @@ def run_gpu(args) -> dict | None:
 
 
 # ---------------------------------------------------------------------------
+# --decode: the decode-style backward from saved probabilities (one query per
+# head against a key history), an HBM-bound path measured in GB/s
+# ---------------------------------------------------------------------------
+DECODE = {"name": "decode16k", "history_len": 16384, "n_heads": 32, "n_kv_heads": 8,
+          "head_dim": 128, "seed": 606}
+
+
+def decode_bytes(L: int, H: int, Hk: int, d: int) -> int:
+    """Algorithmic bytes of one attn_decode_bwd call: K and V read, d_k and d_v
+    read and written, probs read and d_scores written."""
+    return 6 * L * Hk * d * 4 + 2 * H * L * 4
+
+
+def decode_inputs(cfg: dict, seed_offset: int = 0) -> dict:
+    """Seeded q, K, V, d_out (N(0,1), fp32) of the decode workload."""
+    L, H, Hk, d = cfg["history_len"], cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    rng = np.random.default_rng(cfg["seed"] + seed_offset)
+    return {"q": rng.standard_normal(H * d, dtype=np.float32),
+            "K": rng.standard_normal((L, Hk * d), dtype=np.float32),
+            "V": rng.standard_normal((L, Hk * d), dtype=np.float32),
+            "d_out": rng.standard_normal(H * d, dtype=np.float32)}
+
+
+def run_decode(args) -> dict | None:
+    import torch
+    import causal_gqa_attention_attn_gb300 as ga
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cfg = DECODE
+    L, H, Hk, d = cfg["history_len"], cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    G, sc = H // Hk, 1.0 / math.sqrt(d)
+    x = decode_inputs(cfg, rank)
+    host = {k: torch.from_numpy(v).pin_memory() for k, v in x.items()}
+    t = {k: v.to(dev) for k, v in host.items()}
+    # the forward's probabilities of this query (setup, untimed)
+    Kg = t["K"].view(L, Hk, d).repeat_interleave(G, dim=1)          # [L, H, d]
+    t["probs"] = torch.softmax(sc * torch.einsum("lhd,hd->hl", Kg, t["q"].view(H, d)), dim=1).contiguous()
+    host["probs"] = t["probs"].cpu().pin_memory()
+    dq = torch.zeros(H * d, device=dev)
+    dk = torch.zeros(L, Hk * d, device=dev)
+    dv = torch.zeros(L, Hk * d, device=dev)
+    ds = torch.empty(H, L, device=dev)
+    ws = torch.empty(int(ga.lib().attn_decode_bwd_workspace_bytes(L, H, Hk, d)), dtype=torch.uint8,
+                     device=dev)
+
+    def step(src):
+        ga.attn_decode_bwd(src["q"], src["K"], src["V"], src["probs"], src["d_out"], H, Hk, d, sc,
+                           d_q=dq, d_k_hist=dk, d_v_hist=dv, d_scores=ds, workspace=ws)
+
+    for _ in range(args.warmup):
+        step(t)
+    torch.cuda.synchronize()
+    K = args.steps
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = ga.launch_count()
+    with ClockSampler(_gpu_uuid(torch, dev)) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        start.record()
+        for _ in range(K):
+            step(t)
+        end.record()
+        torch.cuda.synchronize()
+        barrier()
+    launches = ga.launch_count() - launches0
+    ms_max = max_over_ranks(start.elapsed_time(end), dev)
+    nbytes = decode_bytes(L, H, Hk, d)
+    value = world * nbytes / (ms_max / K / 1e3) / 1e9
+
+    # end to end with host buffers: each step uploads q, K, V, probs, d_out and
+    # reads back d_scores, d_q, d_k_hist, d_v_hist (no overlap)
+    outs = {n: torch.empty(g.shape, pin_memory=True) for n, g in
+            (("d_scores", ds), ("d_q", dq), ("d_k_hist", dk), ("d_v_hist", dv))}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+    dbuf = {k: torch.empty_like(v) for k, v in t.items()}
+
+    def e2e_step():
+        for k_, v_ in host.items():
+            dbuf[k_].copy_(v_, non_blocking=True)
+        step(dbuf)
+        for (n, o), g in zip(outs.items(), (ds, dq, dk, dv)):
+            o.copy_(g, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record()
+    for _ in range(K):
+        e2e_step()
+    e2.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2), dev)
+
+    peaks = load_peaks()
+    hbm = float(peaks.get("hbm_gbs") or 6800.0)
+    per_call_gbs = nbytes / (ms_max / K / 1e3) / 1e9
+    result = {
+        "metric": "decode attn-backward HBM GB/s (algorithmic bytes)", "value": value,
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) q, K, V, d_out; probs = softmax(scale q.K) of this query)",
+        "config": {"workload": cfg["name"], "history_len": L, "n_heads": H, "n_kv_heads": Hk,
+                   "head_dim": d, "bytes_per_step": nbytes,
+                   "step": "attn_decode_bwd (+= into d_q, d_k_hist, d_v_hist)",
+                   "l2": "working set (0.4 GB) larger than L2 (129 MB)"},
+        "e2e": {"value": world * nbytes / (e2e_ms / K / 1e3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "overlap": "none: copies and kernels in order on one stream"},
+        "gpu_launches": launches,
+        "roofline": {"bound": "hbm", "unit": "GB/s", "achieved": per_call_gbs, "peak": hbm,
+                     "frac": per_call_gbs / hbm, "traffic": None,
+                     "peak_source": "measured HBM copy rate (MEASURED_PEAKS.json hbm_gbs)"},
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        t0 = time.perf_counter()
+        oracle.decode_bwd(x["q"], x["K"], x["V"], host["probs"].numpy(), x["d_out"], H, Hk, d, sc)
+        secs = time.perf_counter() - t0
+        result["cpu_baseline"] = {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1,
+                                  "kind": "oracle", "seconds": secs,
+                                  "sample": f"oracle.decode_bwd (fp64, numpy) on the whole {cfg['name']} call"}
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+# ---------------------------------------------------------------------------
 # the fp64 oracle on the host cores: CPU baseline and the reference arm
 # ---------------------------------------------------------------------------
 def oracle_sample(w, x, lse32, n_rows: int) -> tuple[float, float, str, int]:
@@ -498,9 +634,18 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--given-o", action="store_true",
                     help="time attn_bwd_o (D = rowsum(dO*O) from the forward's O) instead of the LSE-only call")
+    ap.add_argument("--decode", action="store_true",
+                    help="time attn_decode_bwd (one query per head against a 16384-key history) in GB/s")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.decode:
+        if args.impl == "reference":
+            ap.error("--decode times this library's kernels only")
+        res = run_decode(args)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
     if args.impl == "reference":
         res = run_reference(args)
     else:

@@ -68,3 +68,14 @@ def test_max_over_ranks_gloo_two_ranks():
         assert p.exitcode == 0
     assert dict(out) == {0: 15.0, 1: 15.0}
     assert bench.max_over_ranks(3.0) == 3.0      # no process group: identity
+
+
+def test_decode_bytes_and_inputs():
+    import numpy as np
+    import bench
+    # K, V read; d_k, d_v read and written; probs read, d_scores written
+    assert bench.decode_bytes(16384, 32, 8, 128) == 6 * 16384 * 8 * 128 * 4 + 2 * 32 * 16384 * 4
+    cfg = dict(bench.DECODE, history_len=5, n_heads=4, n_kv_heads=2, head_dim=8)
+    a, b = bench.decode_inputs(cfg), bench.decode_inputs(cfg)
+    assert a["K"].shape == (5, 16) and a["q"].shape == (32,) and a["K"].dtype == np.float32
+    assert all(np.array_equal(a[k], b[k]) for k in a)          # seeded
