@@ -214,7 +214,10 @@ def run_gpu(args) -> dict | None:
     S, H, Hk, d, sc = w.seq_len, w.n_heads, w.n_kv_heads, w.head_dim, w.scale
     pairs = workloads.n_pairs(x["seg"])
     flops = counted_flops(d, H, pairs)
-    impl_fn = ga.attn_bwd if args.path == "auto" else ga.attn_bwd_simt
+    impl_fn = ga.attn_bwd_simt if args.path == "simt" else ga.attn_bwd
+    # "tc": the short path (one cooperative launch for short sequences) off,
+    # so that short workloads run the tensor-core kernels too
+    ga.set_short_path(args.path == "auto")
 
     host = {k: torch.from_numpy(np.ascontiguousarray(x[k])).pin_memory()
             for k in ("Q", "K", "V", "dO")}
@@ -228,7 +231,7 @@ def run_gpu(args) -> dict | None:
     dV = torch.zeros(S, Hk * d, device=dev)
     ws = torch.empty(ga.workspace_bytes(S, H, Hk, d), dtype=torch.uint8, device=dev)
 
-    fused_rope = w.rope and args.path == "auto" and not args.given_o
+    fused_rope = w.rope and args.path != "simt" and not args.given_o
     O_dev = None
     if args.given_o:       # the forward output O, as a training step keeps it (setup, untimed)
         O_dev, _ = ga.attn_fwd(t["Q"], t["K"], t["V"], t["seg"], H, Hk, d, sc)
@@ -629,8 +632,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default="causal16k")
-    ap.add_argument("--path", choices=["auto", "simt"], default="auto",
-                    help="auto: attn_bwd (tensor cores where built); simt: attn_bwd_simt")
+    ap.add_argument("--path", choices=["auto", "tc", "simt"], default="auto",
+                    help="auto: attn_bwd (the single-launch short path for short sequences, "
+                         "else tensor cores where built); tc: attn_bwd with the short path off; "
+                         "simt: attn_bwd_simt")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--given-o", action="store_true",
                     help="time attn_bwd_o (D = rowsum(dO*O) from the forward's O) instead of the LSE-only call")

@@ -17,7 +17,8 @@ import os
 __all__ = ["GqaError", "lib", "lib_path", "attn_fwd_lse", "attn_bwd", "attn_bwd_simt",
            "rope_bwd_inplace", "workspace_bytes", "read_device_status", "n_pairs_from_seg",
            "profile_events", "profile_stage_name", "launch_count", "attn_bwd_noalloc",
-           "attn_fwd", "attn_bwd_rope", "attn_bwd_o", "attn_decode_bwd"]
+           "attn_fwd", "attn_bwd_rope", "attn_bwd_o", "attn_decode_bwd", "attn_bwd_short",
+           "set_short_path"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libgqa_attn.so")
@@ -57,6 +58,9 @@ def lib() -> ctypes.CDLL:
     bwd_args = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
     L.attn_bwd.argtypes = bwd_args
     L.attn_bwd_simt.argtypes = bwd_args
+    L.attn_bwd_short.argtypes = bwd_args
+    L.gqa_set_short_path.argtypes = [I]
+    L.gqa_set_short_path.restype = ctypes.c_int
     L.attn_bwd_rope.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, F, P, Z, P]
     L.attn_bwd_o.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
     L.attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P]
@@ -73,11 +77,14 @@ def lib() -> ctypes.CDLL:
     L.gqa_profile_stage_name.restype = ctypes.c_char_p
     L.gqa_wait_selftest.argtypes = [P, Z, ctypes.c_longlong, P]
     L.gqa_wait_selftest.restype = ctypes.c_int
+    L.gqa_grid_barrier_selftest.argtypes = [P, Z, ctypes.c_longlong, P]
+    L.gqa_grid_barrier_selftest.restype = ctypes.c_int
     L.gqa_launch_count.argtypes = []
     L.gqa_launch_count.restype = ctypes.c_ulonglong
     L.gqa_last_error.argtypes = []
     L.gqa_last_error.restype = ctypes.c_char_p
-    for name in ("attn_fwd_lse", "attn_fwd", "attn_bwd", "attn_bwd_simt", "attn_bwd_rope", "attn_bwd_o",
+    for name in ("attn_fwd_lse", "attn_fwd", "attn_bwd", "attn_bwd_simt", "attn_bwd_short",
+                 "attn_bwd_rope", "attn_bwd_o",
                  "attn_decode_bwd", "rope_bwd_inplace", "attn_read_device_status"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
@@ -256,6 +263,22 @@ def attn_bwd_simt(Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_d
     """Same as :func:`attn_bwd`, on CUDA cores only (exact fp32 products)."""
     return _bwd(lib().attn_bwd_simt, Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads,
                 head_dim, scale, workspace, stream)
+
+
+def attn_bwd_short(Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_dim, scale,
+                   workspace=None, stream=None):
+    """Same as :func:`attn_bwd`, as one cooperative launch on CUDA cores for
+    short sequences (seq_len <= 2048 and bounded tile work; GqaError with
+    GQA_ERR_UNSUPPORTED beyond). Returns the workspace used."""
+    return _bwd(lib().attn_bwd_short, Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads,
+                head_dim, scale, workspace, stream)
+
+
+def set_short_path(enable: bool) -> bool:
+    """Process-wide: let attn_bwd / attn_bwd_o / attn_bwd_rope use the
+    single-launch short path for the shapes it accepts (default True).
+    Returns the previous setting."""
+    return bool(lib().gqa_set_short_path(1 if enable else 0))
 
 
 def attn_bwd_noalloc(Q, K, V, dO, LSE, seg, dQ, dK, dV, n_heads, n_kv_heads, head_dim, scale,

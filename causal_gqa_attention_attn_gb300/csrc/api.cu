@@ -16,6 +16,7 @@ static thread_local char g_last_error[512] = "";
 static thread_local ProfileHook g_hook;
 
 static std::atomic<unsigned long long> g_launches{0};
+static std::atomic<int> g_short_path{1};
 
 ProfileHook& profile_hook() { return g_hook; }
 void note_launch(int n) { g_launches.fetch_add((unsigned long long)n); }
@@ -113,9 +114,16 @@ unsigned long long gqa_launch_count(void) { return g_launches.load(); }
 size_t attn_bwd_workspace_bytes(int seq_len, int n_heads, int n_kv_heads, int head_dim) {
   if (seq_len <= 0 || n_heads <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads) return kWsHeader;
   const Shape sh{seq_len, n_heads, n_kv_heads, head_dim, n_heads / n_kv_heads, 1.f};
-  if (tc_supported(sh)) return tc_ws_layout(seq_len, n_heads, n_kv_heads, head_dim).total;
-  return ws_layout(seq_len, n_heads).total;
+  size_t need = tc_supported(sh) ? tc_ws_layout(seq_len, n_heads, n_kv_heads, head_dim).total
+                                 : ws_layout(seq_len, n_heads).total;
+  if (head_dim > 0 && head_dim <= 128 && short_supported(sh)) {
+    const size_t s = short_ws_bytes(seq_len, n_heads, head_dim);
+    if (s > need) need = s;
+  }
+  return need;
 }
+
+int gqa_set_short_path(int enable) { return g_short_path.exchange(enable != 0 ? 1 : 0); }
 
 gqa_status attn_fwd_lse(const float* Q, const float* K, const float* V, const uint32_t* seg,
                         float* O, float* LSE, int seq_len, int n_heads, int n_kv_heads,
@@ -211,6 +219,14 @@ static gqa_status bwd_dispatch(const float* Q, const float* K, const float* V, c
   if (r != GQA_OK || seq_len == 0) return r;
   const Shape sh{seq_len, n_heads, n_kv_heads, head_dim, n_heads / n_kv_heads, scale};
   cudaStream_t st = (cudaStream_t)stream;
+  if (g_short_path.load() != 0 && short_supported(sh)) {
+    const size_t need = short_ws_bytes(seq_len, n_heads, head_dim);
+    if (workspace_bytes < need)
+      return set_error(GQA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+    if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
+      return check_launch("workspace header reset");
+    return short_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st, rope);
+  }
   if (!tc_supported(sh)) {
     if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
       return check_launch("workspace header reset");
@@ -242,6 +258,29 @@ gqa_status attn_bwd(const float* Q, const float* K, const float* V, const float*
                     void* workspace, size_t workspace_bytes, void* stream) {
   return bwd_dispatch(Q, K, V, dO, LSE, seg, dQ, dK, dV, seq_len, n_heads, n_kv_heads, head_dim,
                       scale, workspace, workspace_bytes, stream, no_rope());
+}
+
+gqa_status attn_bwd_short(const float* Q, const float* K, const float* V, const float* dO,
+                          const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
+                          int seq_len, int n_heads, int n_kv_heads, int head_dim, float scale,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  gqa_status r = check_attn_args(seq_len, n_heads, n_kv_heads, head_dim, scale, 128);
+  if (r != GQA_OK || seq_len == 0) return r;
+  const Shape sh{seq_len, n_heads, n_kv_heads, head_dim, n_heads / n_kv_heads, scale};
+  if (!short_supported(sh))
+    return set_error(GQA_ERR_UNSUPPORTED,
+                     "short path: seq_len %d, n_heads %d, head_dim %d exceed its limits "
+                     "(seq_len <= 2048, tile work <= 2^26)", seq_len, n_heads, head_dim);
+  const void* p[] = {Q, K, V, dO, LSE, seg, dQ, dK, dV, workspace};
+  const char* nm[] = {"Q", "K", "V", "dO", "LSE", "seg", "dQ", "dK", "dV", "workspace"};
+  if ((r = check_ptrs(p, nm, 10)) != GQA_OK) return r;
+  const size_t need = short_ws_bytes(seq_len, n_heads, head_dim);
+  if (workspace_bytes < need)
+    return set_error(GQA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
+    return check_launch("workspace header reset");
+  return short_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st, no_rope());
 }
 
 gqa_status attn_bwd_o(const float* Q, const float* K, const float* V, const float* dO,
@@ -295,6 +334,18 @@ gqa_status gqa_wait_selftest(void* workspace, size_t workspace_bytes, long long 
   if (limit_cycles <= 0 || limit_cycles > 100000000LL)
     return set_error(GQA_ERR_INVALID_ARG, "limit_cycles must be in (0, 1e8]");
   return wait_selftest(workspace, limit_cycles, (cudaStream_t)stream);
+}
+
+gqa_status gqa_grid_barrier_selftest(void* workspace, size_t workspace_bytes,
+                                     long long limit_cycles, void* stream) {
+  if (workspace == nullptr || !aligned16(workspace))
+    return set_error(GQA_ERR_INVALID_ARG, "workspace is NULL or not 16-byte aligned");
+  if (workspace_bytes < kWsHeader)
+    return set_error(GQA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes,
+                     kWsHeader);
+  if (limit_cycles <= 0 || limit_cycles > 100000000LL)
+    return set_error(GQA_ERR_INVALID_ARG, "limit_cycles must be in (0, 1e8]");
+  return grid_barrier_selftest(workspace, limit_cycles, (cudaStream_t)stream);
 }
 
 gqa_status attn_read_device_status(const void* workspace, void* stream) {

@@ -113,6 +113,21 @@ gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* d
 
 gqa_status wait_selftest(void* workspace, long long limit_cycles, cudaStream_t st);
 
+// Single-launch backward for short sequences, short_bwd.cu: one cooperative
+// launch (three phases split by bounded grid barriers). Supported for
+// seq_len <= 2048 with at most kShortMaxWork multiply-adds per contraction,
+// counted over whole 32 x 32 (query, key) tiles:
+//   nt (nt + 1) / 2 * 32 * 32 * n_heads * padded head_dim <= kShortMaxWork,
+// nt = ceil(seq_len / 32). Above that the tensor-core kernels are faster.
+constexpr long long kShortMaxWork = 1LL << 26;
+bool short_supported(const Shape& sh);
+size_t short_ws_bytes(int S, int H, int d);
+// Test helper: the short path's bounded grid barrier, made to run out.
+gqa_status grid_barrier_selftest(void* workspace, long long limit_cycles, cudaStream_t st);
+gqa_status short_bwd(const float* Q, const float* K, const float* V, const float* dO,
+                     const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
+                     const Shape& sh, char* ws, cudaStream_t st, const RopeParams& rope);
+
 // Tensor-core host helpers (tc_bwd.cu): the 128-byte-swizzled panel view of a
 // row-major matrix (dims 32 floats x rows x panels; one box fills box_panels
 // panels of box_rows x 128 B) and the group transpose Xt [Hk*d][ld] of

@@ -125,15 +125,51 @@ size_t attn_bwd_workspace_bytes(int seq_len, int n_heads, int n_kv_heads, int he
  * In:  Q, K, V, dO, LSE, seg, scale. In/out: dQ, dK, dV are ACCUMULATED (+=),
  * as in the streaming kernel: zero them before the first call of a step.
  * workspace: >= attn_bwd_workspace_bytes(...) device bytes, caller-owned.
- * head_dim 32, 64 or 128 runs the tensor-core path where it is built; other
- * multiples of 4 up to 128 run the CUDA-core path (attn_bwd_simt).
- * The result is not bitwise deterministic (dQ partial sums may be reduced in
- * any order); it stays within fp32/TF32 rounding of the exact value.
+ * Path: short problems (those attn_bwd_short accepts) run its single
+ * cooperative launch on CUDA cores, unless gqa_set_short_path(0) turned that
+ * off; otherwise head_dim 32, 64 or 128 runs the tensor-core path where it is
+ * built, and other multiples of 4 up to 128 the CUDA-core path
+ * (attn_bwd_simt). The result stays within fp32/TF32 rounding of the exact
+ * value; which path ran decides the rounding.
  */
 gqa_status attn_bwd(const float* Q, const float* K, const float* V, const float* dO,
                     const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
                     int seq_len, int n_heads, int n_kv_heads, int head_dim, float scale,
                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_bwd_short — attn_bwd for short sequences in ONE kernel launch (the
+ * analogue of backward_attention.wgsl's attention_backward_short /
+ * attention_backward_short_dKdV, which serve short sequences with one
+ * dispatch each and keep P and dS for every (query, key, head) in an
+ * O(seq_len^2 * n_heads) scratch buffer; none of that is kept here). Work is
+ * cut into cells of 32 query rows x 32 keys x one query head; a cooperative
+ * launch runs three phases split by grid-wide barriers: (A) per cell, the
+ * partial row sums of P * dP; (B) per cell, D_i = the row's partials summed,
+ * dS = scale * P * (dP - D) and the cell's partial dQ = dS K, dK = dS^T Q,
+ * dV = P^T dO; (C) per output tile, the partials summed in a fixed order
+ * (dK, dV over the GQA group's query heads and the query tiles) and added
+ * once to dQ, dK, dV. fp32 FFMA on CUDA cores, deterministic.
+ * Limits: seq_len <= 2048 and nt*(nt+1)/2 * 1024 * n_heads * hp <= 2^26, where
+ * nt = ceil(seq_len / 32) and hp = head_dim rounded up to 32, 64 or 128;
+ * beyond them GQA_ERR_UNSUPPORTED (attn_bwd then runs its other paths).
+ * Same arguments, semantics (+=), workspace query (attn_bwd_workspace_bytes
+ * covers it) and errors as attn_bwd. Every grid-barrier wait is bounded
+ * (~1 s); one that gives up sets the status word that
+ * attn_read_device_status reports as GQA_ERR_DEVICE_TIMEOUT.
+ */
+gqa_status attn_bwd_short(const float* Q, const float* K, const float* V, const float* dO,
+                          const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
+                          int seq_len, int n_heads, int n_kv_heads, int head_dim, float scale,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * gqa_set_short_path — process-wide switch: whether attn_bwd, attn_bwd_o and
+ * attn_bwd_rope send the shapes attn_bwd_short accepts to it (1, the
+ * default) or to their tensor-core / CUDA-core kernels (0). Returns the
+ * previous setting. Not tied to a stream: change it only between calls.
+ */
+int gqa_set_short_path(int enable);
 
 /*
  * attn_bwd_o — attn_bwd for callers that kept the forward output O [seq_len,
@@ -255,6 +291,19 @@ unsigned long long gqa_launch_count(void);
  */
 gqa_status gqa_wait_selftest(void* workspace, size_t workspace_bytes, long long limit_cycles,
                              void* stream);
+
+/*
+ * gqa_grid_barrier_selftest — the same check for attn_bwd_short's grid-wide
+ * barrier (no counterpart on the pages): a cooperative launch of two CTAs
+ * waits, through that bounded barrier, for one arrival more than the grid
+ * makes, with a limit of limit_cycles SM cycles (at most 1e8). The wait gives
+ * up, sets the status word in `workspace` (>= 256 bytes, header cleared
+ * first; bit 0x400 marks this site), both CTAs return, and
+ * attn_read_device_status() reports GQA_ERR_DEVICE_TIMEOUT. Nothing hangs or
+ * faults, and the context stays usable.
+ */
+gqa_status gqa_grid_barrier_selftest(void* workspace, size_t workspace_bytes,
+                                     long long limit_cycles, void* stream);
 
 /* Static string naming a status code. */
 const char* gqa_status_str(gqa_status status);

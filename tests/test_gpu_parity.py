@@ -51,7 +51,33 @@ def assert_parity(name, got, ref, scale_ref=None):
     return err / mag if mag else 0.0
 
 
+class short_path_off:
+    """attn_bwd and its variants with the single-launch short path switched
+    off: shapes it would take run the tensor-core (or CUDA-core) kernels."""
+
+    def __init__(self, ga, off=True):
+        self.ga, self.off = ga, off
+
+    def __enter__(self):
+        self.prev = self.ga.set_short_path(not self.off)
+
+    def __exit__(self, *exc):
+        self.ga.set_short_path(self.prev)
+
+
+def short_ok(S, H, d):
+    """The shapes attn_bwd_short accepts (its documented limits)."""
+    nt = (S + 31) // 32
+    hp = 32 if d <= 32 else (64 if d <= 64 else 128)
+    return 1 <= S <= 2048 and nt * (nt + 1) // 2 * 1024 * H * hp <= 1 << 26
+
+
 def gpu_bwd(ga, fn, x, lse32, init=None, calls=1):
+    """fn: an entry point of the binding, or "attn_bwd_tc" = attn_bwd with the
+    short path switched off."""
+    if fn == "attn_bwd_tc":
+        with short_path_off(ga):
+            return gpu_bwd(ga, "attn_bwd", x, lse32, init, calls)
     S, H, Hk, d = x["seq_len"], x["n_heads"], x["n_kv_heads"], x["head_dim"]
     t = {k: _dev(x[k]) for k in ("Q", "K", "V", "dO")}
     if init is None:
@@ -87,9 +113,15 @@ def reference(name):
     return _REF[name]
 
 
-@pytest.mark.parametrize("fn", ["attn_bwd", "attn_bwd_simt"])
+BWD_FNS = ["attn_bwd", "attn_bwd_tc", "attn_bwd_simt", "attn_bwd_short"]
+
+
+@pytest.mark.parametrize("fn", BWD_FNS)
 @pytest.mark.parametrize("name", ["tiny", "causal512", "docs2k", "docs4k"])
 def test_backward_matches_oracle(ga, name, fn):
+    w = workloads.WORKLOADS[name]
+    if fn == "attn_bwd_short" and not short_ok(w.seq_len, w.n_heads, w.head_dim):
+        pytest.skip("beyond the short path's limits")
     x, _, _, lse32, (rq, rk, rv) = reference(name)
     dQ, dK, dV = gpu_bwd(ga, fn, x, lse32)
     assert_parity("dQ", dQ, rq)
@@ -159,9 +191,11 @@ EDGE = [
 ]
 
 
-@pytest.mark.parametrize("fn", ["attn_bwd", "attn_bwd_simt"])
+@pytest.mark.parametrize("fn", BWD_FNS)
 @pytest.mark.parametrize("S,H,Hk,d,seg_kind", EDGE)
 def test_edge_shapes(ga, S, H, Hk, d, seg_kind, fn):
+    if fn == "attn_bwd_short" and not short_ok(S, H, d):
+        pytest.skip("beyond the short path's limits")
     x = _edge_inputs(S, H, Hk, d, seg_kind, seed=S * 31 + d)
     _, lse = oracle.fwd(x["Q"], x["K"], x["V"], x["seg"], H, Hk, d, x["scale"])
     lse32 = lse.astype(np.float32)
@@ -172,7 +206,7 @@ def test_edge_shapes(ga, S, H, Hk, d, seg_kind, fn):
     assert_parity("dV", dV, rv)
 
 
-@pytest.mark.parametrize("fn", ["attn_bwd", "attn_bwd_simt"])
+@pytest.mark.parametrize("fn", BWD_FNS)
 def test_gradients_accumulate(ga, fn):
     """+= semantics: two calls on non-zero initial gradients give init + 2 * grad."""
     x, _, _, lse32, (rq, rk, rv) = reference("causal512")
@@ -184,10 +218,11 @@ def test_gradients_accumulate(ga, fn):
     assert_parity("dV", dV, init[2].astype(np.float32) + 2 * rv)
 
 
-def test_seq_len_one(ga):
+@pytest.mark.parametrize("fn", BWD_FNS)
+def test_seq_len_one(ga, fn):
     x = _edge_inputs(1, 8, 2, 64, "causal", seed=1)
     _, lse = oracle.fwd(x["Q"], x["K"], x["V"], x["seg"], 8, 2, 64, x["scale"])
-    dQ, dK, dV = gpu_bwd(ga, "attn_bwd", x, lse.astype(np.float32))
+    dQ, dK, dV = gpu_bwd(ga, fn, x, lse.astype(np.float32))
     want_v = np.stack([x["dO"][0].reshape(8, 64)[4 * g:4 * g + 4].sum(0) for g in range(2)]).reshape(1, -1)
     assert_parity("dV", dV, want_v)
     assert_parity("dQ", dQ, np.zeros_like(dQ), scale_ref=want_v)
@@ -213,11 +248,18 @@ FUSED_ROPE = [
 ]
 
 
+@pytest.mark.parametrize("short", [True, False])
 @pytest.mark.parametrize("S,H,Hk,d,seg_kind,pos", FUSED_ROPE)
-def test_fused_rope_backward_matches_oracle(ga, S, H, Hk, d, seg_kind, pos):
+def test_fused_rope_backward_matches_oracle(ga, S, H, Hk, d, seg_kind, pos, short):
     """attn_bwd_rope: dQ += R^T(attention dQ), dK += R^T(attention dK), dV += dV
     on non-zero initial gradients (only the new contribution is rotated);
-    tensor-core shapes and a CUDA-core one (d = 100), both angle paths."""
+    tensor-core shapes and a CUDA-core one (d = 100), both angle paths, with
+    the short path allowed (it takes these shapes) and switched off."""
+    with short_path_off(ga, off=not short):
+        _fused_rope_case(ga, S, H, Hk, d, seg_kind, pos)
+
+
+def _fused_rope_case(ga, S, H, Hk, d, seg_kind, pos):
     x = _edge_inputs(S, H, Hk, d, seg_kind, seed=S * 7 + d + pos)
     _, lse = oracle.fwd(x["Q"], x["K"], x["V"], x["seg"], H, Hk, d, x["scale"])
     lse32 = lse.astype(np.float32)
@@ -245,19 +287,27 @@ def test_backward_given_o_matches_oracle(ga, name):
     S, H, Hk, d = x["seq_len"], x["n_heads"], x["n_kv_heads"], x["head_dim"]
     t = {k: _dev(x[k]) for k in ("Q", "K", "V", "dO")}
     out = [torch.zeros(S, n * d, device="cuda") for n in (H, Hk, Hk)]
-    ws = ga.attn_bwd_o(t["Q"], t["K"], t["V"], t["dO"], _dev(O_ref.astype(np.float32)), _dev(lse32),
-                       _seg_dev(x["seg"]), *out, H, Hk, d, x["scale"])
+    with short_path_off(ga):   # the tensor-core kernels' given-O path at every size
+        ws = ga.attn_bwd_o(t["Q"], t["K"], t["V"], t["dO"], _dev(O_ref.astype(np.float32)),
+                           _dev(lse32), _seg_dev(x["seg"]), *out, H, Hk, d, x["scale"])
     ga.read_device_status(ws)
     torch.cuda.synchronize()
     for nm, g, r in (("dQ", out[0], rq), ("dK", out[1], rk), ("dV", out[2], rv)):
         assert_parity(nm, g.cpu().numpy(), r)
 
 
+@pytest.mark.parametrize("short", [True, False])
 @pytest.mark.parametrize("S,H,Hk,d,seg_kind", [(300, 8, 2, 128, "docs"), (129, 4, 2, 32, "nonmonotone"),
                                                (97, 4, 2, 100, "docs"), (200, 16, 4, 64, "causal")])
-def test_backward_given_o_from_gpu_forward(ga, S, H, Hk, d, seg_kind):
+def test_backward_given_o_from_gpu_forward(ga, S, H, Hk, d, seg_kind, short):
     """attn_bwd_o fed this library's own forward (O, LSE), on non-zero initial
-    gradients, against the oracle backward with the same fp32 LSE."""
+    gradients, against the oracle backward with the same fp32 LSE (with the
+    short path allowed, which forms D itself, and switched off)."""
+    with short_path_off(ga, off=not short):
+        _given_o_case(ga, S, H, Hk, d, seg_kind)
+
+
+def _given_o_case(ga, S, H, Hk, d, seg_kind):
     x = _edge_inputs(S, H, Hk, d, seg_kind, seed=S * 13 + d)
     t = {k: _dev(x[k]) for k in ("Q", "K", "V", "dO")}
     seg = _seg_dev(x["seg"])

@@ -62,7 +62,7 @@ def _bwd(L, S=128, H=4, Hk=2, d=32, scale=0.17, ws_bytes=None, ptrs=None, fn="at
     return getattr(L, fn)(*p[:9], S, H, Hk, d, scale, p[9], ws_bytes, None)
 
 
-@pytest.mark.parametrize("fn", ["attn_bwd", "attn_bwd_simt"])
+@pytest.mark.parametrize("fn", ["attn_bwd", "attn_bwd_simt", "attn_bwd_short"])
 def test_bwd_rejects_bad_arguments(L, fn):
     assert _bwd(L, H=6, Hk=4, fn=fn) == 1                       # heads not a multiple
     assert _bwd(L, Hk=0, fn=fn) == 1
@@ -80,6 +80,23 @@ def test_bwd_rejects_bad_arguments(L, fn):
         assert _bwd(L, ptrs=p, fn=fn) == 1
     assert _bwd(L, S=1 << 20, H=64, Hk=8, d=128, fn=fn) == 2   # 2^33 elements
     assert _bwd(L, S=0, fn=fn) == 0                             # empty: no-op
+
+
+def test_short_path_limits_and_switch(L):
+    """attn_bwd_short takes seq_len <= 2048 with bounded tile work and refuses
+    the rest before any launch; the workspace query covers its partial sums;
+    gqa_set_short_path returns the previous setting."""
+    assert _bwd(L, S=4096, H=4, Hk=2, d=32, fn="attn_bwd_short") == 2
+    assert _bwd(L, S=1024, H=32, Hk=8, d=128, fn="attn_bwd_short") == 2
+    assert "short path" in L.gqa_last_error().decode()
+    # 16 x 17 / 2 tiles x 1024 x 4 heads x 32: partial dQ, dK, dV of every cell
+    cells = 16 * 17 // 2 * 4
+    assert L.attn_bwd_workspace_bytes(512, 4, 2, 32) >= 3 * cells * 32 * 32 * 4 + cells * 32 * 4
+    # head_dim 100 is padded to 128 (8 x 9 / 2 tiles x 4 heads)
+    assert L.attn_bwd_workspace_bytes(256, 4, 2, 100) >= 3 * 144 * 32 * 128 * 4
+    assert L.gqa_set_short_path(0) == 1
+    assert L.gqa_set_short_path(1) == 0
+    assert L.gqa_set_short_path(1) == 1
 
 
 def test_fwd_and_rope_reject_bad_arguments(L):
