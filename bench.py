@@ -167,14 +167,22 @@ def summarize_clocks(lines: list[str]) -> dict:
             "samples": len(sm)}
 
 
-def _source_hash() -> str:
+# The sources each measured stage's kernels are compiled from (device code and
+# the headers it includes); a traffic record holds only while they are unchanged.
+STAGE_SOURCES = {
+    "tc_query_major+tc_key_major": ["tc_bwd.cu", "tc_common.cuh", "common.cuh", "rope_common.cuh"],
+    "short_bwd": ["short_bwd.cu", "common.cuh", "rope_common.cuh"],
+    "decode": ["decode_bwd.cu", "common.cuh"],
+}
+
+
+def _source_hash(stage: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "causal_gqa_attention_attn_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for f in sorted(STAGE_SOURCES.get(stage, [])):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -182,11 +190,11 @@ def _traffic(stage: str, workload: str):
     """DRAM bytes per launch of the dominant stage from the committed ncu
     summary, when it was taken on the current kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or stage not in STAGE_SOURCES:
         return None
     with open(path) as f:
         rec = json.load(f).get(f"{workload}:{stage}")
-    if not rec or rec.get("source_hash") != _source_hash():
+    if not rec or rec.get("source_hash") != _source_hash(stage):
         return None
     return rec.get("bytes_per_launch")
 
@@ -536,7 +544,7 @@ def run_decode(args) -> dict | None:
                 "overlap": "none: copies and kernels in order on one stream"},
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "unit": "GB/s", "achieved": per_call_gbs, "peak": hbm,
-                     "frac": per_call_gbs / hbm, "traffic": None,
+                     "frac": per_call_gbs / hbm, "traffic": _traffic("decode", "decode16k"),
                      "peak_source": "measured HBM copy rate (MEASURED_PEAKS.json hbm_gbs)"},
         "clocks": clk.summary(),
     }

@@ -206,6 +206,29 @@ def test_edge_shapes(ga, S, H, Hk, d, seg_kind, fn):
     assert_parity("dV", dV, rv)
 
 
+@pytest.mark.parametrize("S,H,Hk,d,seg_kind", [
+    (2000, 1, 1, 32, "docs"),            # 63 tiles: the short path's largest tile triangle
+    (900, 2, 1, 64, "nonmonotone"), (33, 8, 4, 128, "causal"), (31, 3, 1, 8, "docs")])
+def test_short_path_limits(ga, S, H, Hk, d, seg_kind):
+    """attn_bwd_short near its work limit (2^26 multiply-adds per contraction)
+    and at odd sizes, against the oracle; just past the limit it refuses."""
+    assert short_ok(S, H, d)
+    x = _edge_inputs(S, H, Hk, d, seg_kind, seed=S * 3 + d)
+    _, lse = oracle.fwd(x["Q"], x["K"], x["V"], x["seg"], H, Hk, d, x["scale"])
+    lse32 = lse.astype(np.float32)
+    rq, rk, rv = oracle.bwd(x["Q"], x["K"], x["V"], x["dO"], lse32, x["seg"], H, Hk, d, x["scale"])
+    dQ, dK, dV = gpu_bwd(ga, "attn_bwd_short", x, lse32)
+    assert_parity("dQ", dQ, rq, scale_ref=rv)
+    assert_parity("dK", dK, rk, scale_ref=rv)
+    assert_parity("dV", dV, rv)
+    S2 = S + 32 * 8 if S < 2000 else 2049
+    if not short_ok(S2, H, d):
+        y = _edge_inputs(S2, H, Hk, d, seg_kind, seed=1)
+        with pytest.raises(ga.GqaError) as e:
+            gpu_bwd(ga, "attn_bwd_short", y, np.zeros((S2, H), np.float32))
+        assert e.value.status == 2
+
+
 @pytest.mark.parametrize("fn", BWD_FNS)
 def test_gradients_accumulate(ga, fn):
     """+= semantics: two calls on non-zero initial gradients give init + 2 * grad."""
