@@ -180,8 +180,8 @@ int gqa_set_short_path(int enable);
  * pass and its two contractions (S and dP). The pages have no separate
  * entry point for this; it is this library's addition. Same arguments,
  * workspace, semantics (+=) and errors as attn_bwd, plus O (non-NULL, 16-byte
- * aligned). Where the CUDA-core path runs (head_dim not 32/64/128), O is not
- * read and D is formed as in attn_bwd.
+ * aligned). Where the short path (attn_bwd_short) or the CUDA-core path
+ * (head_dim not 32/64/128) runs, O is not read and D is formed as in attn_bwd.
  */
 gqa_status attn_bwd_o(const float* Q, const float* K, const float* V, const float* dO,
                       const float* O, const float* LSE, const uint32_t* seg, float* dQ, float* dK,
@@ -270,8 +270,9 @@ gqa_status attn_read_device_status(const void* workspace, void* stream);
  * call on this host thread records `before` on its stream immediately before
  * its dominant kernel stage and `after` immediately after it, then clears the
  * hook. The events are owned by the caller. Stage: the whole two-kernel
- * backward on the CUDA-core path; the main key-tile kernel on the
- * tensor-core path. gqa_profile_stage_name() names it.
+ * backward on the CUDA-core path; both tensor-core kernels (query-major and
+ * key-major) on the tensor-core path; the one cooperative launch on the short
+ * path. gqa_profile_stage_name() names it.
  */
 void gqa_profile_events(void* before, void* after);
 const char* gqa_profile_stage_name(void);
