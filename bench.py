@@ -171,6 +171,7 @@ def summarize_clocks(lines: list[str]) -> dict:
 # the headers it includes); a traffic record holds only while they are unchanged.
 STAGE_SOURCES = {
     "tc_query_major+tc_key_major": ["tc_bwd.cu", "tc_common.cuh", "common.cuh", "rope_common.cuh"],
+    "tc_forward": ["tc_fwd.cu", "tc_common.cuh", "common.cuh"],
     "short_bwd": ["short_bwd.cu", "common.cuh", "rope_common.cuh"],
     "decode": ["decode_bwd.cu", "common.cuh"],
 }
@@ -563,6 +564,153 @@ def run_decode(args) -> dict | None:
 
 
 # ---------------------------------------------------------------------------
+# the tensor-core forward (attn_fwd: O and LSE), the setup step of the
+# backward, measured on its own
+# ---------------------------------------------------------------------------
+def forward_counted_flops(head_dim: int, n_heads: int, pairs: int) -> float:
+    """Two d-deep contractions (Q K^T, P V) per unmasked pair and head."""
+    return 4.0 * head_dim * n_heads * pairs
+
+
+def run_forward(args) -> dict | None:
+    import torch
+    import causal_gqa_attention_attn_gb300 as ga
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = workloads.WORKLOADS[args.workload]
+    x = workloads.make_inputs(w, seed=w.seed + rank)
+    S, H, Hk, d, sc = w.seq_len, w.n_heads, w.n_kv_heads, w.head_dim, w.scale
+    pairs = workloads.n_pairs(x["seg"])
+    flops = forward_counted_flops(d, H, pairs)
+    host = {k: torch.from_numpy(np.ascontiguousarray(x[k])).pin_memory() for k in ("Q", "K", "V")}
+    host["seg"] = torch.from_numpy(x["seg"].astype(np.int32)).pin_memory()
+    t = {k: v.to(dev) for k, v in host.items()}
+    O = torch.empty(S, H * d, device=dev)
+    LSE = torch.empty(S, H, device=dev)
+    ws = torch.empty(int(ga.lib().attn_fwd_workspace_bytes(S, H, Hk, d)), dtype=torch.uint8,
+                     device=dev)
+
+    def step(src):
+        ga.attn_fwd(src["Q"], src["K"], src["V"], src["seg"], H, Hk, d, sc, O=O, LSE=LSE,
+                    workspace=ws)
+
+    for _ in range(args.warmup):
+        step(t)
+    ga.read_device_status(ws)
+    torch.cuda.synchronize()
+    K = args.steps
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in ev_a + ev_b:
+        e.record()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    launches0 = ga.launch_count()
+    with ClockSampler(_gpu_uuid(torch, dev)) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        start.record()
+        for k in range(K):
+            ga.profile_events(ev_a[k], ev_b[k])
+            step(t)
+        end.record()
+        torch.cuda.synchronize()
+        barrier()
+    launches = ga.launch_count() - launches0
+    stage = ga.profile_stage_name()
+    ga.read_device_status(ws)
+    ms_max = max_over_ranks(start.elapsed_time(end), dev)
+    stage_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / K
+    value = world * flops / (ms_max / K / 1e3) / 1e12
+
+    # end to end with host buffers: each step uploads Q, K, V, seg and reads
+    # back O and LSE (in order on one stream)
+    outs = {"O": torch.empty(O.shape, pin_memory=True), "LSE": torch.empty(LSE.shape, pin_memory=True)}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
+    dbuf = {k: torch.empty_like(v) for k, v in t.items()}
+
+    def e2e_step():
+        for k_, v_ in host.items():
+            dbuf[k_].copy_(v_, non_blocking=True)
+        step(dbuf)
+        outs["O"].copy_(O, non_blocking=True)
+        outs["LSE"].copy_(LSE, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record()
+    for _ in range(K):
+        e2e_step()
+    e2.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2), dev)
+
+    peaks = load_peaks()
+    tensor_path = stage == "tc_forward"
+    if tensor_path:
+        peak = tf32_peak(peaks, sustained=False)
+        roof = {"bound": "tensor", "unit": UNIT, "peak_source":
+                f"{peaks['source']} bf16 burst x nominal tf32/bf16 ratio {TF32_PER_BF16:.4f}"}
+    else:   # CUDA-core forward (head dims without a tensor-core kernel): no stage events
+        props = torch.cuda.get_device_properties(dev)
+        peak = fp32_simt_peak_tflops(props.multi_processor_count, peaks.get("sm_max_mhz", 2070.0))
+        roof = {"bound": "alu", "unit": UNIT, "peak_source":
+                f"{props.multi_processor_count} SMs x 128 fp32 FMA/clk x 2 x max SM clock"}
+        stage, stage_ms = "fwd_kernel (whole call)", ms_max / K
+    achieved = flops / (stage_ms / 1e3) / 1e12
+    roof.update({"kernel": stage, "achieved": achieved, "peak": peak, "frac": achieved / peak,
+                 "traffic": _traffic(stage, w.name), "stage_ms": stage_ms,
+                 "flops_per_launch": flops})
+    if tensor_path:   # LSE pass (S) + output pass (S again, P V): three contractions
+        ex = 6.0 * d * H * pairs
+        roof.update({"executed_flops_per_launch": ex,
+                     "executed_tflops": ex / (stage_ms / 1e3) / 1e12,
+                     "executed_frac": ex / (stage_ms / 1e3) / 1e12 / peak})
+    result = {
+        "metric": "attn-forward TFLOP/s (unmasked pairs)", "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_max / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "tf32" if tensor_path else "f32",
+        "data": "synthetic (seeded N(0,sigma^2) Q, K, V)",
+        "config": {"workload": w.name, "shape": w.describe.split(" +")[0], "seq_len": S,
+                   "n_heads": H, "n_kv_heads": Hk, "head_dim": d, "n_pairs": pairs,
+                   "counted_flop_per_step": flops, "step": "attn_fwd (O, LSE overwritten)",
+                   "l2": "inputs larger than L2 (129 MB)" if 4 * S * (H + 2 * Hk) * d > 129e6
+                   else "inputs smaller than L2: steps run back to back (warm L2)"},
+        "e2e": {"value": world * flops / (e2e_ms / K / 1e3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "overlap": "none: copies and kernels in order on one stream"},
+        "gpu_launches": launches,
+        "roofline": roof,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        n = CPU_SAMPLE_ROWS.get(w.name, 256)
+        rows = np.arange(max(0, S - n), S)
+        sp = int(np.sum(rows - x["seg"][rows].astype(np.int64) + 1))
+        t0 = time.perf_counter()
+        oracle.fwd(x["Q"], x["K"], x["V"], x["seg"], H, Hk, d, sc, rows=rows)
+        secs = time.perf_counter() - t0
+        result["cpu_baseline"] = {
+            "value": forward_counted_flops(d, H, sp) / secs / 1e12, "unit": UNIT,
+            "cores": oracle._workers(), "kind": "oracle", "seconds": secs,
+            "sample": f"oracle.fwd (fp64, numpy) on query rows [{rows[0]}, {S}) of all {H} heads "
+                      f"({sp} unmasked pairs per head) of workload {w.name}"}
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+# ---------------------------------------------------------------------------
 # the fp64 oracle on the host cores: CPU baseline and the reference arm
 # ---------------------------------------------------------------------------
 def oracle_sample(w, x, lse32, n_rows: int) -> tuple[float, float, str, int]:
@@ -647,11 +795,20 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--given-o", action="store_true",
                     help="time attn_bwd_o (D = rowsum(dO*O) from the forward's O) instead of the LSE-only call")
+    ap.add_argument("--forward", action="store_true",
+                    help="time attn_fwd (the tensor-core forward producing O and LSE) on the workload")
     ap.add_argument("--decode", action="store_true",
                     help="time attn_decode_bwd (one query per head against a 16384-key history) in GB/s")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.forward:
+        if args.impl == "reference" or args.decode or args.given_o:
+            ap.error("--forward times this library's attn_fwd alone")
+        res = run_forward(args)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
     if args.decode:
         if args.impl == "reference":
             ap.error("--decode times this library's kernels only")

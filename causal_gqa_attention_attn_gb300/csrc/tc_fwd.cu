@@ -353,8 +353,10 @@ gqa_status fwd_launch(const float* Q, const float* K, const float* Vt, long long
     return check_launch("forward smem attribute");
   const int QR = 128 / sh.G;
   dim3 grid((sh.S + QR - 1) / QR, sh.Hk);
+  profile_before(st, "tc_forward");
   tc_forward<D><<<grid, kFwdThreads, Cfg::SMEM_BYTES, st>>>(mk, mvt, Q, seg, O, LSE, status, sh);
   note_launch();
+  profile_after(st);
   return check_launch("tensor-core forward");
 }
 

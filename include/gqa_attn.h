@@ -266,13 +266,14 @@ gqa_status attn_read_device_status(const void* workspace, void* stream);
 
 /*
  * gqa_profile_events — measurement hook (no counterpart on the pages). When
- * both are non-NULL cudaEvent_t handles, the next attn_bwd / attn_bwd_simt
- * call on this host thread records `before` on its stream immediately before
+ * both are non-NULL cudaEvent_t handles, the next backward (attn_bwd and its
+ * variants) or tensor-core forward (attn_fwd) call on this host thread
+ * records `before` on its stream immediately before
  * its dominant kernel stage and `after` immediately after it, then clears the
  * hook. The events are owned by the caller. Stage: the whole two-kernel
  * backward on the CUDA-core path; both tensor-core kernels (query-major and
  * key-major) on the tensor-core path; the one cooperative launch on the short
- * path. gqa_profile_stage_name() names it.
+ * path; the tensor-core kernel of attn_fwd. gqa_profile_stage_name() names it.
  */
 void gqa_profile_events(void* before, void* after);
 const char* gqa_profile_stage_name(void);
