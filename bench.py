@@ -668,8 +668,8 @@ def run_forward(args) -> dict | None:
     roof.update({"kernel": stage, "achieved": achieved, "peak": peak, "frac": achieved / peak,
                  "traffic": _traffic(stage, w.name), "stage_ms": stage_ms,
                  "flops_per_launch": flops})
-    if tensor_path:   # LSE pass (S) + output pass (S again, P V): three contractions
-        ex = 6.0 * d * H * pairs
+    if tensor_path:   # one pass, online softmax: Q K^T and P V, the counted two
+        ex = 4.0 * d * H * pairs
         roof.update({"executed_flops_per_launch": ex,
                      "executed_tflops": ex / (stage_ms / 1e3) / 1e12,
                      "executed_frac": ex / (stage_ms / 1e3) / 1e12 / peak})

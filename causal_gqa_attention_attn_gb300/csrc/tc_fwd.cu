@@ -6,16 +6,23 @@
 //
 // One CTA per (slab of 128/G queries, kv head), M = 128 rows = the slab's
 // queries x the G heads of the group, the same layout as the backward's
-// query-major kernel. Q sits in TMEM (A operand). Two passes over the slab's
-// visible keys, in chunks of 64 keys streamed by TMA through a ring of units:
-//  pass 1: S = Q K^T per chunk; the row max m and sum l of 2^(s log2e
-//          scale - m) run online in registers, giving LSE = (m + log2 l) ln 2;
-//  pass 2: S again, P = exp(scale s - LSE) written back to TMEM (A operand)
-//          and O += P V (B = the chunk of V^T, a transposed copy in the
-//          workspace: TF32 operands are read K-major only).
-// Computing the LSE first keeps O free of the running rescale an online
-// softmax needs; the price is a second Q K^T (three contractions per pair
-// and head). O and LSE are overwritten.
+// query-major kernel. Q sits in TMEM (A operand). One pass over the slab's
+// visible keys in chunks of 64, streamed by TMA through a ring of units (K
+// and V^T, a transposed copy in the workspace: TF32 operands are read K-major
+// only), with an online softmax:
+//   S = Q K^T of chunk c into TMEM stage c & 1;
+//   the softmax warpgroup c & 1 (one thread per row, all 64 columns) keeps
+//   its own running row max m and sum l, writes P = 2^(s scale log2e - m)
+//   back over S (A operand) and the MMA warp adds P V into that warpgroup's
+//   own O accumulator (O_0 for even chunks, O_1 for odd ones);
+//   at the end the two (m, l, O) are combined: O = (O_0 2^(m_0 - m) +
+//   O_1 2^(m_1 - m)) / (l_0 2^(m_0 - m) + l_1 2^(m_1 - m)), LSE = m + log2(...).
+// The running max is raised (and O rescaled in TMEM) only when a chunk's max
+// exceeds it by more than 2^8, so P stays below 256 and rescaling is rare.
+// When the softmax of chunk c starts, the P V product of its warpgroup's
+// previous chunk c - 2 has completed (issued before S(c), which has
+// completed), so the rescale needs no extra hand-off. Two contractions per
+// pair and head (Q K^T, P V). O and LSE are overwritten.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -33,6 +40,7 @@ constexpr int kFwdFirstCompute = kFwdProducers + 1;
 constexpr int kFwdComputeWarps = 8;
 constexpr int kFwdThreads = 32 * (kFwdFirstCompute + kFwdComputeWarps);
 constexpr uint32_t kTmemColsFwd = 512;   // allocations are powers of two; one CTA per SM
+constexpr float kRescaleLog2 = 8.f;      // raise the running max only past 2^8
 
 enum : uint32_t { kSiteFwdProducer = 1u << 8, kSiteFwdMma = 1u << 9, kSiteFwdCompute = 1u << 10 };
 
@@ -49,14 +57,15 @@ struct FwdCfg {
   static constexpr int NUNIT = (192 * 1024 / UNIT_BYTES < 12) ? 192 * 1024 / UNIT_BYTES : 12;
   static constexpr int SMEM_BYTES =
       (NUNIT * UNIT_BYTES + 1024 > 120 * 1024) ? NUNIT * UNIT_BYTES + 1024 : 120 * 1024;
-  // TMEM columns: Q | O | two S stages of BK columns
-  static constexpr uint32_t T_Q = 0, T_O = D, T_ST = 2 * D;
+  // TMEM columns: Q | O_0 | O_1 | two S stages of BK columns
+  static constexpr uint32_t T_Q = 0, T_ST = 3 * D;
+  static constexpr uint32_t t_o(int w) { return D + w * D; }
   static constexpr uint32_t stage(int st) { return T_ST + st * BK; }
   static_assert(T_ST + 2 * BK <= 512, "TMEM budget");
 };
 
 struct FwdBarriers {
-  uint64_t full[12], empty[12], s_full[2], s_free[2], q_ready, o_done;
+  uint64_t full[12], empty[12], s_full[2], p_ready[2], q_ready, o_done;
   uint32_t tmem_base;
   int abort;
   unsigned kmin;
@@ -70,7 +79,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                float* __restrict__ O, float* __restrict__ LSE, uint32_t* __restrict__ status,
                Shape sh) {
   using Cfg = FwdCfg<D>;
-  constexpr int NU = Cfg::NUNIT, BK = Cfg::BK, HB = BK / 2;
+  constexpr int NU = Cfg::NUNIT, BK = Cfg::BK;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -89,7 +98,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.s_free[i], kFwdComputeWarps);
+      mbar_init(&bars.p_ready[i], kFwdComputeWarps / 2);   // the four warps of warpgroup i
     }
     mbar_init(&bars.q_ready, kFwdComputeWarps);
     mbar_init(&bars.o_done, 1);
@@ -114,12 +123,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   const int q_last = min(q0 + QR, S) - 1;
   const int kc0 = (int)(min(bars.kmin, (unsigned)q_last) / BK);
-  const int nk = q_last / BK - kc0 + 1;                     // chunks per pass
-  const int n_units = 3 * nk;                               // K (pass 1); K, V^T (pass 2)
+  const int nk = q_last / BK - kc0 + 1;                     // chunks
+  const int n_units = 2 * nk;                               // unit 2c: K of chunk c, 2c + 1: its V^T
   volatile int* abort = &bars.abort;
 
   if (warp < kFwdProducers) {
-    // ---------------- TMA producers: warp pw loads the units i with i % 2 == pw ----------------
+    // ---------------- TMA producers: warp 0 loads the K units, warp 1 the V^T units ----------------
     const int pw = warp;
     if (elect_one()) {
       tma_prefetch_desc(&mapK);
@@ -130,14 +139,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int u = i % NU;
       if (i >= NU && !warp_wait(&bars.empty[u], ((i / NU) - 1) & 1, abort, status, kSiteFwdProducer))
         break;
-      const bool p1 = i < nk;
-      const int chunk = p1 ? i : (i - nk) / 2;
-      const bool vt = !p1 && ((i - nk) % 2 == 1);
-      const int key0 = (kc0 + chunk) * BK;
+      const int key0 = (kc0 + i / 2) * BK;
       unsigned char* dst = smem + u * Cfg::UNIT_BYTES;
       if (elect_one()) {
         mbar_arrive_expect_tx(&bars.full[u], Cfg::UNIT_BYTES);
-        if (vt) tma_load_3d(dst, &mapVt, 0, g * D, key0 / 32, &bars.full[u]);
+        if (pw == 1) tma_load_3d(dst, &mapVt, 0, g * D, key0 / 32, &bars.full[u]);
         else tma_load_3d(dst, &mapK, 0, key0, g * Cfg::PANELS, &bars.full[u]);
       }
       __syncwarp();
@@ -154,42 +160,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     auto unit_wait = [&](int i) {
       return warp_wait(&bars.full[i % NU], (i / NU) & 1, abort, status, kSiteFwdMma);
     };
-    int use0 = 0, use1 = 0;
-    auto stage_free = [&](int st) {
-      const int u = st ? use1 : use0;
-      return u == 0 || warp_wait(&bars.s_free[st], (u - 1) & 1, abort, status, kSiteFwdMma);
-    };
-    auto issue_s = [&](uint32_t ts, uint64_t bk) {
-      tc_fence_after();
-      mma_ts(ts, tmem + Cfg::T_Q, bk, id_s, 0u);
-#pragma unroll
-      for (int ks = 1; ks < D / 8; ++ks)
-        mma_ts_acc(ts, tmem + Cfg::T_Q + 8 * ks, bk + desc_off(ks, Cfg::K_PANEL_BYTES), id_s);
-    };
-    bool ok = warp_wait(&bars.q_ready, 0, abort, status, kSiteFwdMma);
-    // ---- pass 1: S of chunk c in stage c & 1 ----
-    for (int c = 0; ok && c < nk; ++c) {
-      const int st = c & 1;
-      if (!unit_wait(c) || !stage_free(st)) { ok = false; break; }
-      if (elect_one()) {
-        issue_s(tmem + Cfg::stage(st), unit_desc(c));
-        mma_commit(&bars.s_full[st]);
-        mma_commit(&bars.empty[c % NU]);
-      }
-      __syncwarp();
-      if (st) ++use1; else ++use0;
-    }
-    // ---- pass 2: S of chunk c, then O += P V for chunk c-1 ----
-    int o_use = 0;
+    // O_{c&1} += P(c) V(c): after the softmax of chunk c has written P
     auto issue_o = [&](int c) -> bool {
-      const int st = c & 1, ivt = nk + 2 * c + 1;
-      if (!warp_wait(&bars.s_free[st], o_use & 1, abort, status, kSiteFwdMma) || !unit_wait(ivt))
+      const int st = c & 1, ivt = 2 * c + 1;
+      if (!warp_wait(&bars.p_ready[st], (c >> 1) & 1, abort, status, kSiteFwdMma) || !unit_wait(ivt))
         return false;
-      const uint32_t a_p = tmem + Cfg::stage(st), d_o = tmem + Cfg::T_O;
+      const uint32_t a_p = tmem + Cfg::stage(st), d_o = tmem + Cfg::t_o(st);
       const uint64_t bvt = unit_desc(ivt);
       if (elect_one()) {
         tc_fence_after();
-        mma_ts(d_o, a_p, bvt, id_o, c > 0 ? 1u : 0u);
+        mma_ts(d_o, a_p, bvt, id_o, c >= 2 ? 1u : 0u);   // chunks 0 and 1 start their accumulators
 #pragma unroll
         for (int kk = 1; kk < BK / 8; ++kk)
           mma_ts_acc(d_o, a_p + 8 * kk, bvt + desc_off(kk, Cfg::VT_PANEL_BYTES), id_o);
@@ -198,28 +178,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       __syncwarp();
       return true;
     };
+    bool ok = warp_wait(&bars.q_ready, 0, abort, status, kSiteFwdMma);
+    // S(c) into stage c & 1 (its previous P was read by O(c-2), issued before),
+    // then O(c-1): the tensor core works on S(c) while the softmax of c-1 runs
     for (int c = 0; ok && c < nk; ++c) {
-      const int st = c & 1, ik = nk + 2 * c;
+      const int st = c & 1, ik = 2 * c;
       if (!unit_wait(ik)) { ok = false; break; }
-      // the stage's previous use: pass 1 for c < 2, else chunk c-2 of this
-      // pass, whose release issue_o(c-2) has already waited for
-      if (c < 2 && !stage_free(st)) { ok = false; break; }
       if (elect_one()) {
-        issue_s(tmem + Cfg::stage(st), unit_desc(ik));
+        tc_fence_after();
+        const uint32_t ts = tmem + Cfg::stage(st);
+        const uint64_t bk = unit_desc(ik);
+        mma_ts(ts, tmem + Cfg::T_Q, bk, id_s, 0u);
+#pragma unroll
+        for (int ks = 1; ks < D / 8; ++ks)
+          mma_ts_acc(ts, tmem + Cfg::T_Q + 8 * ks, bk + desc_off(ks, Cfg::K_PANEL_BYTES), id_s);
         mma_commit(&bars.s_full[st]);
         mma_commit(&bars.empty[ik % NU]);
       }
       __syncwarp();
-      const int this_use = st ? use1++ : use0++;
       if (c > 0 && !issue_o(c - 1)) { ok = false; break; }
-      o_use = this_use;
     }
     if (ok && nk > 0) ok = issue_o(nk - 1);
     if (elect_one()) mma_commit(&bars.o_done);   // also drains every MMA issued above
     __syncwarp();
   } else {
-    // ---------------- compute: one TMEM lane (= one row) per thread; both
-    // warpgroups take every chunk, warpgroup wg its columns [wg*BK/2, (wg+1)*BK/2) ----------------
+    // ---------------- compute: one TMEM lane (= one row) per thread; warpgroup
+    // wg takes the chunks c with c & 1 == wg, all BK columns of them ----------------
     const int wg = (warp - kFwdFirstCompute) >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int qi = r / G, q = q0 + qi;
@@ -246,88 +230,96 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     const float sl2 = sh.scale * kLog2e;
     const int segq = valid ? (int)__ldg(seg + q) : 0;
+    const uint32_t to = tl + Cfg::t_o(wg);
     float m = -1e30f, l = 0.f;     // running max (log2 units) and sum over this warpgroup's keys
-    bool ok = true;
-    // ---- pass 1: row max and sum, online ----
-    for (int c = 0; c < nk; ++c) {
-      const int st = c & 1;
-      if (!mbar_wait(&bars.s_full[st], (c >> 1) & 1, abort, status, kSiteFwdCompute)) { ok = false; break; }
+    bool ok = true, has_o = false;
+    for (int c = wg; c < nk; c += 2) {
+      if (!mbar_wait(&bars.s_full[wg], (c >> 1) & 1, abort, status, kSiteFwdCompute)) { ok = false; break; }
       tc_fence_after();
-      const int k0 = (kc0 + c) * BK + wg * HB;
-      const bool full = valid && k0 >= segq && k0 + HB - 1 <= q;
-      float sv[32];
-      tmem_ld32(tl + Cfg::stage(st) + wg * HB, sv);
+      const int k0 = (kc0 + c) * BK;
+      const bool full = valid && k0 >= segq && k0 + BK - 1 <= q;
+      const uint32_t ts = tl + Cfg::stage(wg);
+      float sv[BK];
+      tmem_ld32(ts, sv);
+      tmem_ld32(ts + 32, sv + 32);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.s_free[st]);
       float mx = -1e30f;
+      if (full) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int key = k0 + j;
-        const bool vis = full || (valid && key >= segq && key <= q);
-        sv[j] = vis ? sv[j] * sl2 : -1e30f;
-        mx = fmaxf(mx, sv[j]);
+        for (int j = 0; j < BK; ++j) {
+          sv[j] *= sl2;
+          mx = fmaxf(mx, sv[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < BK; ++j) {
+          const int key = k0 + j;
+          const bool vis = valid && key >= segq && key <= q;
+          sv[j] = vis ? sv[j] * sl2 : -1e30f;
+          mx = fmaxf(mx, sv[j]);
+        }
       }
-      if (mx > m) {
-        l *= ex2(m - mx);
+      // raise the running max past 2^8 growth only; O of this warpgroup is
+      // idle here (its last P V product completed before S(c) did)
+      const bool raise = mx > m + kRescaleLog2;
+      const float alpha = raise ? ex2(m - mx) : 1.f;
+      if (raise) {
+        l *= alpha;
         m = mx;
       }
+      if (has_o && __any_sync(0xffffffffu, raise)) {
+        for (int cc = 0; cc < D; cc += 32) {
+          float ov[32];
+          tmem_ld32(to + cc, ov);
+          tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) l += (sv[j] > -1e29f) ? ex2(sv[j] - m) : 0.f;
+          for (int j = 0; j < 32; ++j) ov[j] *= alpha;
+          tmem_st32(to + cc, ov);
+        }
+      }
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < BK; ++j) {
+        const float pj = (sv[j] > -1e29f) ? ex2(sv[j] - m) : 0.f;
+        sum += pj;
+        sv[j] = to_tf32(pj);
+      }
+      l += sum;
+      tmem_st32(ts, sv);
+      tmem_st32(ts + 32, sv + 32);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.p_ready[wg]);
+      has_o = true;
     }
-    // both warpgroups' (max, sum) pairs -> the row's LSE (log2 units)
+    // both warpgroups' (max, sum) of each row -> its LSE (log2 units) and the
+    // weights of the two O accumulators
     bars.part[wg][0][r] = m;
     bars.part[wg][1][r] = l;
     asm volatile("bar.sync 2, 256;" ::: "memory");
     const float m0 = bars.part[0][0][r], m1 = bars.part[1][0][r];
     const float mm = fmaxf(m0, m1);
-    const float ll = bars.part[0][1][r] * ex2(m0 - mm) + bars.part[1][1][r] * ex2(m1 - mm);
+    const float a0 = ex2(m0 - mm), a1 = ex2(m1 - mm);
+    const float ll = bars.part[0][1][r] * a0 + bars.part[1][1][r] * a1;
     const float lse2 = mm + __log2f(ll);
-    // ---- pass 2: P = 2^(s*scale*log2e - lse2) over S, for O += P V ----
-    for (int c = 0; ok && c < nk; ++c) {
-      const int st = c & 1;
-      const int uses_p1 = st ? nk / 2 : (nk + 1) / 2;
-      if (!mbar_wait(&bars.s_full[st], (uses_p1 + (c >> 1)) & 1, abort, status, kSiteFwdCompute)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int k0 = (kc0 + c) * BK + wg * HB;
-      const bool full = valid && k0 >= segq && k0 + HB - 1 <= q;
-      const uint32_t ts = tl + Cfg::stage(st) + wg * HB;
-      float sv[32];
-      tmem_ld32(ts, sv);
-      tmem_ld_wait();
-      if (full) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = to_tf32(ex2(fmaf(sv[j], sl2, -lse2)));
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int key = k0 + j;
-          const bool vis = valid && key >= segq && key <= q;
-          sv[j] = vis ? to_tf32(ex2(fmaf(sv[j], sl2, -lse2))) : 0.f;
-        }
-      }
-      tmem_st32(ts, sv);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.s_free[st]);
-    }
-    // epilogue: O (warpgroup wg: half wg of the columns) and LSE, overwritten
+    const float inv = 1.f / ll;
+    // epilogue: O (warpgroup wg: half wg of the columns of both accumulators) and LSE
     if (ok && mbar_wait(&bars.o_done, 0, abort, status, kSiteFwdCompute)) {
       tc_fence_after();
+      const bool has1 = nk >= 2;   // O_1 was written only if there is an odd chunk
       for (int cc = wg * (D / 2); cc < (wg + 1) * (D / 2); cc += 16) {
-        float v[16];
-        tmem_ld16(tl + Cfg::T_O + cc, v);
+        float v0[16], v1[16];
+        tmem_ld16(tl + Cfg::t_o(0) + cc, v0);
+        if (has1) tmem_ld16(tl + Cfg::t_o(1) + cc, v1);
         tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v0[i] = (v0[i] * a0 + (has1 ? v1[i] * a1 : 0.f)) * inv;
         if (valid) {
           float4* dst = reinterpret_cast<float4*>(O + row_off + cc);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            dst[i] = make_float4(v0[4 * i], v0[4 * i + 1], v0[4 * i + 2], v0[4 * i + 3]);
         }
       }
       if (valid && wg == 0) LSE[(long long)q * H + h] = lse2 / kLog2e;
