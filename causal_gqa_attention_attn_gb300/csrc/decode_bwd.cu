@@ -9,15 +9,18 @@
 //   d_q_h += sigma sum_j d_scores_hj k_j
 //   d_k_j += sigma sum_{h in g} d_scores_hj q_h,   d_v_j += sum_{h in g} probs_hj d_out_h
 //
-// The work is a few passes over the key history, so HBM decides the time:
+// The work is two passes over the key history, so HBM decides the time:
 // every key row is read once per pass for all G heads of its group. CTA =
 // (block of 32 or 64 keys, kv head); a warp holds 4 or 8 key rows in
 // registers, each lane d/32 columns of them.
 //  decode_dp:   dP for the block's keys and the group's heads, staged in
-//               d_scores; per-CTA partial sums of probs * dP.
+//               d_scores; per-CTA partial sums of probs * dP; one owned +=
+//               of the block's d_v rows (d_v needs no D). Reads V, d_v;
+//               writes d_v.
 //  decode_dsum: D_h = the partial sums added in a fixed order.
-//  decode_dkv:  d_scores from the staged dP; one owned += of the block's
-//               d_k / d_v rows; per-CTA partial d_q.
+//  decode_dkv:  d_scores from the staged dP; one owned += of the block's d_k
+//               rows; per-CTA partial d_q. Reads K, d_k; writes d_k (the two
+//               passes move about the same bytes).
 //  decode_dq:   d_q += the partials added in a fixed order.
 // No atomics: results do not depend on scheduling.
 #include <cuda_runtime.h>
@@ -90,21 +93,28 @@ __global__ void __launch_bounds__(kDecThreads) decode_dp(const float* __restrict
                                                          const float* __restrict__ probs,
                                                          const float* __restrict__ d_out,
                                                          float* __restrict__ dsc,
-                                                         float* __restrict__ dpart, int L, int H,
+                                                         float* __restrict__ dpart,
+                                                         float* __restrict__ dV, int L, int H,
                                                          int Hk, int G) {
   constexpr int D = 32 * E, KPW = dec_kpw(E);
   extern __shared__ float red[];                  // [kDecWarps][G] per-warp partial sums
   const int g = blockIdx.y, blk = blockIdx.x;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int j0 = blk * dec_keys(E) + warp * KPW;
-  float v[KPW][E];
+  // the warp's value rows and their d_v rows, loaded up front; d_v
+  // accumulates onto the loaded rows and is stored once at the end
+  float v[KPW][E], dv[KPW][E];
 #pragma unroll
   for (int k = 0; k < KPW; ++k) {
     const int j = j0 + k;
-    if (j < L) load_cols<E>(V + ((long long)j * Hk + g) * D + lane * E, v[k]);
-    else
+    const long long off = ((long long)j * Hk + g) * D + lane * E;
+    if (j < L) {
+      load_cols<E>(V + off, v[k]);
+      load_cols<E, false>(dV + off, dv[k]);    // rows this thread writes back below
+    } else {
 #pragma unroll
-      for (int e = 0; e < E; ++e) v[k][e] = 0.f;
+      for (int e = 0; e < E; ++e) v[k][e] = dv[k][e] = 0.f;
+    }
   }
   constexpr int HC = 32 / KPW;                    // heads per chunk: one probs value per lane
   for (int c0 = 0; c0 < G; c0 += HC) {
@@ -123,11 +133,19 @@ __global__ void __launch_bounds__(kDecThreads) decode_dp(const float* __restrict
         for (int e = 0; e < E; ++e) x = fmaf(o[e], v[k][e], x);
         x = warp_sum(x);
         if (lane == k) mine = x;
-        psum = fmaf(__shfl_sync(0xffffffffu, pl, (hh - c0) * KPW + k), x, psum);
+        const float p = __shfl_sync(0xffffffffu, pl, (hh - c0) * KPW + k);
+        psum = fmaf(p, x, psum);
+#pragma unroll
+        for (int e = 0; e < E; ++e) dv[k][e] = fmaf(p, o[e], dv[k][e]);
       }
       if (lane < KPW && j0 + lane < L) dsc[(long long)h * L + j0 + lane] = mine;
       if (lane == 0) red[warp * G + hh] = psum;
     }
+  }
+#pragma unroll
+  for (int k = 0; k < KPW; ++k) {
+    const int j = j0 + k;
+    if (j < L) store_cols<E>(dV + ((long long)j * Hk + g) * D + lane * E, dv[k]);
   }
   __syncthreads();
   for (int hh = threadIdx.x; hh < G; hh += kDecThreads) {
@@ -156,17 +174,16 @@ template <int E>
 __global__ void __launch_bounds__(kDecThreads) decode_dkv(
     const float* __restrict__ q, const float* __restrict__ K, const float* __restrict__ probs,
     const float* __restrict__ d_out, float* __restrict__ dsc, const float* __restrict__ dsum,
-    float* __restrict__ dK, float* __restrict__ dV, float* __restrict__ qpart, int L, int H,
-    int Hk, int G, float scale) {
+    float* __restrict__ dK, float* __restrict__ qpart, int L, int H, int Hk, int G, float scale) {
   constexpr int D = 32 * E, KPW = dec_kpw(E);
   constexpr int HC = 32 / KPW;                    // heads per chunk: one value per lane
   __shared__ float qred[HC][kDecWarps][D];        // per-warp partial d_q of a chunk's heads
   const int g = blockIdx.y, blk = blockIdx.x;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int j0 = blk * dec_keys(E) + warp * KPW;
-  // the warp's key rows and their d_k / d_v rows, all loaded up front; the
-  // gradients accumulate onto the loaded rows and are stored once at the end
-  float kr[KPW][E], dk[KPW][E], dv[KPW][E];
+  // the warp's key rows and their d_k rows, loaded up front; d_k accumulates
+  // onto the loaded rows and is stored once
+  float kr[KPW][E], dk[KPW][E];
 #pragma unroll
   for (int k = 0; k < KPW; ++k) {
     const int j = j0 + k;
@@ -174,10 +191,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_dkv(
     if (j < L) {
       load_cols<E>(K + off, kr[k]);
       load_cols<E, false>(dK + off, dk[k]);   // rows this thread writes back below
-      load_cols<E, false>(dV + off, dv[k]);
     } else {
 #pragma unroll
-      for (int e = 0; e < E; ++e) kr[k][e] = dk[k][e] = dv[k][e] = 0.f;
+      for (int e = 0; e < E; ++e) kr[k][e] = dk[k][e] = 0.f;
     }
   }
   for (int c0 = 0; c0 < G; c0 += HC) {
@@ -209,7 +225,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_dkv(
 #pragma unroll
         for (int e = 0; e < E; ++e) {
           dk[k][e] = fmaf(sds, qh[e], dk[k][e]);
-          dv[k][e] = fmaf(p, oh[e], dv[k][e]);
           qa[e] = fmaf(sds, kr[k][e], qa[e]);
         }
       }
@@ -233,9 +248,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_dkv(
   for (int k = 0; k < KPW; ++k) {
     const int j = j0 + k;
     if (j >= L) continue;
-    const long long off = ((long long)j * Hk + g) * D + lane * E;
-    store_cols<E>(dK + off, dk[k]);
-    store_cols<E>(dV + off, dv[k]);
+    store_cols<E>(dK + ((long long)j * Hk + g) * D + lane * E, dk[k]);
   }
 }
 
@@ -278,16 +291,16 @@ gqa_status decode_launch(const float* q, const float* k_hist, const float* v_his
       cudaFuncSetAttribute(decode_dp<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)red_bytes) != cudaSuccess)
     return check_launch("decode dP smem attribute");
-  decode_dp<E><<<grid, kDecThreads, red_bytes, st>>>(v_hist, probs, d_out, d_scores, dpart, L, H,
-                                                     Hk, G);
+  decode_dp<E><<<grid, kDecThreads, red_bytes, st>>>(v_hist, probs, d_out, d_scores, dpart, d_v,
+                                                     L, H, Hk, G);
   note_launch();
   gqa_status r;
   if ((r = check_launch("decode dP")) != GQA_OK) return r;
   decode_dsum<<<H, 256, 0, st>>>(dpart, dsum, w.nblk, H);
   note_launch();
   if ((r = check_launch("decode D")) != GQA_OK) return r;
-  decode_dkv<E><<<grid, kDecThreads, 0, st>>>(q, k_hist, probs, d_out, d_scores, dsum, d_k, d_v,
-                                              qpart, L, H, Hk, G, scale);
+  decode_dkv<E><<<grid, kDecThreads, 0, st>>>(q, k_hist, probs, d_out, d_scores, dsum, d_k, qpart,
+                                              L, H, Hk, G, scale);
   note_launch();
   if ((r = check_launch("decode dK dV")) != GQA_OK) return r;
   decode_dq<<<dim3((unsigned)H, D / 32), 256, 0, st>>>(qpart, d_q, w.nblk, H, D);
