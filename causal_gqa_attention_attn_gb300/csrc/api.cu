@@ -270,7 +270,7 @@ gqa_status attn_bwd_short(const float* Q, const float* K, const float* V, const 
   if (!short_supported(sh))
     return set_error(GQA_ERR_UNSUPPORTED,
                      "short path: seq_len %d, n_heads %d, head_dim %d exceed its limits "
-                     "(seq_len <= 2048, tile work <= 2^26)", seq_len, n_heads, head_dim);
+                     "(seq_len <= 2048, tile work <= 2^27)", seq_len, n_heads, head_dim);
   const void* p[] = {Q, K, V, dO, LSE, seg, dQ, dK, dV, workspace};
   const char* nm[] = {"Q", "K", "V", "dO", "LSE", "seg", "dQ", "dK", "dV", "workspace"};
   if ((r = check_ptrs(p, nm, 10)) != GQA_OK) return r;

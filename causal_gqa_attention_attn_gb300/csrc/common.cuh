@@ -119,7 +119,7 @@ gqa_status wait_selftest(void* workspace, long long limit_cycles, cudaStream_t s
 // counted over whole 32 x 32 (query, key) tiles:
 //   nt (nt + 1) / 2 * 32 * 32 * n_heads * padded head_dim <= kShortMaxWork,
 // nt = ceil(seq_len / 32). Above that the tensor-core kernels are faster.
-constexpr long long kShortMaxWork = 1LL << 26;
+constexpr long long kShortMaxWork = 1LL << 27;
 bool short_supported(const Shape& sh);
 size_t short_ws_bytes(int S, int H, int d);
 // Test helper: the short path's bounded grid barrier, made to run out.

@@ -248,6 +248,11 @@ __global__ void __launch_bounds__(kThr) short_bwd_kernel(const ShortArgs a, cons
   const int n_cells = sh.H * a.ntri;
 
   // ---- phase A: partial row sums of P * dP -----------------------------
+  // The CTA's last visible cell keeps its tiles in shared memory and its P
+  // and dP in registers: phase B, which walks the cells in reverse, starts
+  // with that cell and reuses them.
+  int kept = -1;
+  float kp[2][4], kdp[2][4];
   for (int cell = blockIdx.x; cell < n_cells; cell += gridDim.x) {
     const int h = cell / a.ntri;
     int qt, kt;
@@ -281,12 +286,15 @@ __global__ void __launch_bounds__(kThr) short_bwd_kernel(const ShortArgs a, cons
         const bool ok = row < S && key <= row && (uint32_t)key >= sm.seg[r];
         const float p = ok ? exp2f(s[i][j] * sl2 - sm.lse2[r]) : 0.f;
         part = fmaf(p, dp[i][j], part);
+        kp[i][j] = p;
+        kdp[i][j] = dp[i][j];
       }
       part += __shfl_xor_sync(0xffffffffu, part, 1);
       part += __shfl_xor_sync(0xffffffffu, part, 2);
       part += __shfl_xor_sync(0xffffffffu, part, 4);
       if (tc == 0) a.dpart[(size_t)cell * kT + r] = part;
     }
+    kept = cell;
   }
   if (!grid_barrier(a, gridDim.x, kSiteBarrier1, &sm.ok)) return;
 
@@ -294,18 +302,24 @@ __global__ void __launch_bounds__(kThr) short_bwd_kernel(const ShortArgs a, cons
   __syncthreads();
 
   // ---- phase B: dS and the cells' partial gradients ----------------------
-  for (int cell = blockIdx.x; cell < n_cells; cell += gridDim.x) {
+  const int last = (int)blockIdx.x < n_cells
+                       ? (int)blockIdx.x + ((n_cells - 1 - (int)blockIdx.x) / (int)gridDim.x) * (int)gridDim.x
+                       : -1;
+  for (int cell = last; cell >= (int)blockIdx.x; cell -= gridDim.x) {
     const int h = cell / a.ntri;
     int qt, kt;
     tri_decode(cell - h * a.ntri, qt, kt);
     const uint32_t tmin = sm.tmin[qt];
     if (!visible(qt, kt, tmin)) continue;
     const int q0 = qt * kT, k0 = kt * kT, g = h / G;
-    __syncthreads();
-    load_rows_async<DP>(sm.q, a.Q, ldq, h * d, q0, S - q0, d);
-    load_rows_async<DP>(sm.dout, a.dO, ldq, h * d, q0, S - q0, d);
-    load_rows_async<DP>(sm.k, a.K, ldk, g * d, k0, S - k0, d);
-    load_rows_async<DP>(sm.v, a.V, ldk, g * d, k0, S - k0, d);
+    const bool reuse = cell == kept;   // first cell of this walk: tiles, P, dP still here
+    if (!reuse) {
+      __syncthreads();
+      load_rows_async<DP>(sm.q, a.Q, ldq, h * d, q0, S - q0, d);
+      load_rows_async<DP>(sm.dout, a.dO, ldq, h * d, q0, S - q0, d);
+      load_rows_async<DP>(sm.k, a.K, ldk, g * d, k0, S - k0, d);
+      load_rows_async<DP>(sm.v, a.V, ldk, g * d, k0, S - k0, d);
+    }
     if (threadIdx.x < kT) {
       // D of row r: its partials over the visible key tiles k2 = tmin/32 .. qt
       // (consecutive cells), in order, eight loads in flight
@@ -323,14 +337,37 @@ __global__ void __launch_bounds__(kThr) short_bwd_kernel(const ShortArgs a, cons
         }
       }
       sm.dsum[r] = D;
-      sm.seg[r] = row < S ? __ldg(a.seg + row) : 0u;
-      sm.lse2[r] = row < S ? __ldg(a.LSE + (long long)row * sh.H + h) * kLog2e : 0.f;
+      if (!reuse) {
+        sm.seg[r] = row < S ? __ldg(a.seg + row) : 0u;
+        sm.lse2[r] = row < S ? __ldg(a.LSE + (long long)row * sh.H + h) * kLog2e : 0.f;
+      }
     }
-    cp_async_wait_all();
+    if (!reuse) cp_async_wait_all();
     __syncthreads();
-    float s[2][4], dp[2][4];
-    mm_abt<DP>(sm.q, sm.k, s);
-    mm_abt<DP>(sm.dout, sm.v, dp);
+    float pv[2][4], dp[2][4];
+    if (reuse) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          pv[i][j] = kp[i][j];
+          dp[i][j] = kdp[i][j];
+        }
+    } else {
+      float s[2][4];
+      mm_abt<DP>(sm.q, sm.k, s);
+      mm_abt<DP>(sm.dout, sm.v, dp);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int r = tr + 16 * i, row = q0 + r;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int key = k0 + tc + 8 * j;
+          const bool ok = row < S && key <= row && (uint32_t)key >= sm.seg[r];
+          pv[i][j] = ok ? exp2f(s[i][j] * sl2 - sm.lse2[r]) : 0.f;
+        }
+      }
+    }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int r = tr + 16 * i, row = q0 + r;
@@ -338,9 +375,8 @@ __global__ void __launch_bounds__(kThr) short_bwd_kernel(const ShortArgs a, cons
       for (int j = 0; j < 4; ++j) {
         const int c = tc + 8 * j, key = k0 + c;
         const bool ok = row < S && key <= row && (uint32_t)key >= sm.seg[r];
-        const float p = ok ? exp2f(s[i][j] * sl2 - sm.lse2[r]) : 0.f;
-        sm.p[r][c] = p;
-        sm.ds[r][c] = ok ? sh.scale * p * (dp[i][j] - sm.dsum[r]) : 0.f;
+        sm.p[r][c] = pv[i][j];
+        sm.ds[r][c] = ok ? sh.scale * pv[i][j] * (dp[i][j] - sm.dsum[r]) : 0.f;
       }
     }
     __syncthreads();

@@ -150,7 +150,7 @@ gqa_status attn_bwd(const float* Q, const float* K, const float* V, const float*
  * dV = P^T dO; (C) per output tile, the partials summed in a fixed order
  * (dK, dV over the GQA group's query heads and the query tiles) and added
  * once to dQ, dK, dV. fp32 FFMA on CUDA cores, deterministic.
- * Limits: seq_len <= 2048 and nt*(nt+1)/2 * 1024 * n_heads * hp <= 2^26, where
+ * Limits: seq_len <= 2048 and nt*(nt+1)/2 * 1024 * n_heads * hp <= 2^27, where
  * nt = ceil(seq_len / 32) and hp = head_dim rounded up to 32, 64 or 128;
  * beyond them GQA_ERR_UNSUPPORTED (attn_bwd then runs its other paths).
  * Same arguments, semantics (+=), workspace query (attn_bwd_workspace_bytes
