@@ -168,6 +168,22 @@ def test_forward_edge_shapes(ga, S, H, Hk, d, seg_kind):
     assert_parity("LSE", LSE, lse_ref)
 
 
+@pytest.mark.parametrize("S,H,Hk,d,seg_kind", [(1000, 8, 2, 128, "causal"), (700, 4, 1, 64, "docs"),
+                                               (513, 4, 4, 32, "causal")])
+def test_forward_growing_scores(ga, S, H, Hk, d, seg_kind):
+    """attn_fwd where a row's running max keeps growing past the first chunks:
+    key j is scaled by 0.1 + 4 j / S, so the scores of later keys exceed the
+    early maxima by far more than 2^8 (in log2 units) and the online softmax
+    raises its max and rescales its O accumulators mid-row, repeatedly."""
+    x = _edge_inputs(S, H, Hk, d, seg_kind, seed=S + d)
+    grow = (0.1 + 4.0 * np.arange(S) / S).astype(np.float32)[:, None]
+    x["K"] = (x["K"] * grow).astype(np.float32)
+    O_ref, lse_ref = oracle.fwd(x["Q"], x["K"], x["V"], x["seg"], H, Hk, d, x["scale"])
+    O, LSE = gpu_fwd(ga, "attn_fwd", x)
+    assert_parity("O", O, O_ref)
+    assert_parity("LSE", LSE, lse_ref)
+
+
 def _edge_inputs(S, H, Hk, d, seg_kind, seed):
     rng = np.random.default_rng(seed)
     if seg_kind == "causal":
