@@ -24,6 +24,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace gqa {
@@ -485,9 +487,10 @@ ShortLayout short_layout(int S, int H, int d) {
   return L;
 }
 
-// Per device and head-dim variant: CTAs per SM the cooperative launch may use.
+// Per device and head-dim variant: co-resident CTAs the cooperative launch
+// may use (0 = not yet known; threads that race here compute the same value).
 constexpr int kMaxDevices = 64;
-int g_capacity[kMaxDevices][3];
+std::atomic<int> g_capacity[kMaxDevices][3];
 
 template <int DP>
 gqa_status short_launch(const float* Q, const float* K, const float* V, const float* dO,
@@ -498,7 +501,7 @@ gqa_status short_launch(const float* Q, const float* K, const float* V, const fl
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return check_launch("short path: device");
   if (dev < 0 || dev >= kMaxDevices) return set_error(GQA_ERR_UNSUPPORTED, "device ordinal %d", dev);
-  int& cap = g_capacity[dev][vi];
+  int cap = g_capacity[dev][vi].load(std::memory_order_acquire);
   if (cap == 0) {
     if (cudaFuncSetAttribute(short_bwd_kernel<DP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
@@ -510,6 +513,7 @@ gqa_status short_launch(const float* Q, const float* K, const float* V, const fl
       return check_launch("short path: occupancy");
     if (per_sm <= 0) return set_error(GQA_ERR_CUDA, "short path: kernel cannot be resident");
     cap = per_sm * n_sm;
+    g_capacity[dev][vi].store(cap, std::memory_order_release);   // after the smem attribute is set
   }
   const ShortLayout L = short_layout(sh.S, sh.H, sh.d);
   ShortArgs a;
