@@ -275,23 +275,57 @@ def run_gpu(args) -> dict | None:
         e.record()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    graph = None
+    if args.graph:
+        # the whole step (gradient fills + the backward) captured once as a
+        # CUDA graph and replayed: one host call per step instead of the
+        # binding's and the library's per-launch host work. (Events recorded
+        # during capture become graph dependencies, not timestamps: the stage
+        # time is read from eager steps after the timed region.)
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        cap0 = ga.launch_count()
+        with torch.cuda.graph(graph):
+            step()
+        launches_per_step = ga.launch_count() - cap0
+        graph.replay()
+        torch.cuda.synchronize()
     launches0 = ga.launch_count()
     with ClockSampler(_gpu_uuid(torch, dev)) as clk:
         barrier()
         torch.cuda.synchronize()
         start.record()
         for k in range(K):
-            ga.profile_events(ev_a[k], ev_b[k])
-            step()
+            if graph is not None:
+                graph.replay()
+            else:
+                ga.profile_events(ev_a[k], ev_b[k])
+                step()
         end.record()
         torch.cuda.synchronize()
         barrier()
     launches = ga.launch_count() - launches0
+    if graph is not None:
+        launches = launches_per_step * K      # replays do not pass through the library's host code
     stage = ga.profile_stage_name()
     ga.read_device_status(ws)
     ms = start.elapsed_time(end)
     ms_max = max_over_ranks(ms, dev)
-    stage_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / K
+    if graph is not None:     # the same kernels, run eagerly: their stage time
+        n_eager = min(K, 10)
+        for k in range(n_eager):
+            ga.profile_events(ev_a[k], ev_b[k])
+            step()
+        torch.cuda.synchronize()
+        stage = ga.profile_stage_name()
+        stage_ms = sum(ev_a[k].elapsed_time(ev_b[k]) for k in range(n_eager)) / n_eager
+    else:
+        stage_ms = sum(a.elapsed_time(b) for a, b in zip(ev_a, ev_b)) / K
     value = world * flops / (ms_max / K / 1e3) / 1e12
 
     # End to end through the public API with host buffers (pinned) every step:
@@ -412,7 +446,8 @@ def run_gpu(args) -> dict | None:
                             (" + rope_bwd(dQ) + rope_bwd(dK)" if w.rope else "")),
                    "l2": "inputs larger than L2 (129 MB)" if 4 * S * H * d > 129e6 else
                          "inputs smaller than L2: steps run back to back (warm L2)",
-                   "path": stage},
+                   "path": stage,
+                   "launch": "CUDA graph replay of the step" if args.graph else "eager (Python-driven)"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "overlap": "two device buffer sets: step k+1's upload and step k-1's download "
@@ -795,6 +830,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--given-o", action="store_true",
                     help="time attn_bwd_o (D = rowsum(dO*O) from the forward's O) instead of the LSE-only call")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay the step as a captured CUDA graph (for launch-bound short workloads)")
     ap.add_argument("--forward", action="store_true",
                     help="time attn_fwd (the tensor-core forward producing O and LSE) on the workload")
     ap.add_argument("--decode", action="store_true",
