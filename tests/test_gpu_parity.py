@@ -362,3 +362,40 @@ def _given_o_case(ga, S, H, Hk, d, seg_kind):
     torch.cuda.synchronize()
     for nm, g, r, i0 in (("dQ", out[0], rq, init[0]), ("dK", out[1], rk, init[1]), ("dV", out[2], rv, init[2])):
         assert_parity(nm, g.cpu().numpy() - i0, r, scale_ref=rv)
+
+
+@pytest.mark.parametrize("short", [True, False])
+def test_backward_captured_in_cuda_graph(ga, short):
+    """attn_bwd captured in a CUDA graph (with the gradients' zeroing) and
+    replayed twice: the short path's cooperative launch and the tensor-core
+    kernels' cluster launches replay to the oracle's result each time."""
+    x, _, _, lse32, (rq, rk, rv) = reference("causal512")
+    S, H, Hk, d, sc = x["seq_len"], x["n_heads"], x["n_kv_heads"], x["head_dim"], x["scale"]
+    t = {k: _dev(x[k]) for k in ("Q", "K", "V", "dO")}
+    seg, LSE = _seg_dev(x["seg"]), _dev(lse32)
+    out = [torch.zeros(S, n * d, device="cuda") for n in (H, Hk, Hk)]
+    with short_path_off(ga, off=not short):
+        ws = torch.empty(ga.workspace_bytes(S, H, Hk, d), dtype=torch.uint8, device="cuda")
+
+        def step():
+            for o in out:
+                o.zero_()
+            ga.attn_bwd(t["Q"], t["K"], t["V"], t["dO"], LSE, seg, *out, H, Hk, d, sc, workspace=ws)
+
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()                       # first call outside capture (one-time set-up)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(2):
+            for o in out:
+                o.fill_(7.0)             # replays must overwrite this through their own zeroing
+            g.replay()
+            torch.cuda.synchronize()
+            ga.read_device_status(ws)
+            for nm, got, r in (("dQ", out[0], rq), ("dK", out[1], rk), ("dV", out[2], rv)):
+                assert_parity(nm, got.cpu().numpy(), r)
