@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const float* __restrict__ LSE, const uint32_t* __restrict__ seg,
                    float* __restrict__ dQ, float* __restrict__ Dws, float* __restrict__ Qt,
                    float* __restrict__ dOt, long long ld_qt, uint32_t* __restrict__ status,
-                   Shape sh, const RopeParams rope) {
+                   Shape sh, const RopeParams rope, int slab_major) {
   using Cfg = QmCfg<D, C>;
   constexpr int NU = Cfg::NUNIT;
   constexpr bool kCl = C > 1;
@@ -149,12 +149,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ QmBarriers bars;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int G = sh.G, QR = 128 / G;
-  const int n_pad = gridDim.x;                           // slabs, padded to a multiple of C
-  const int slab = n_pad - 1 - (int)blockIdx.x;          // longest rows first
+  // Dispatch order (CTAs start x-fastest), as for the key-major kernel:
+  // kv-head-major, grid (slab groups * C, Hk), when the grid is four or more
+  // waves deep (the CTAs running together stream one head's K / V chunks);
+  // slab-major, grid (C * Hk, slab groups), below that (the longest rows of
+  // every kv head first). Slab groups are counted from the end of the
+  // sequence: longest rows first.
+  const int sg = slab_major ? (int)blockIdx.y : (int)blockIdx.x / C;
+  const int g = slab_major ? (int)blockIdx.x / C : (int)blockIdx.y;
+  const int n_pad = (slab_major ? (int)gridDim.y : (int)gridDim.x / C) * C;   // slabs, padded to a multiple of C
   const uint32_t rank = (C > 1) ? cluster_ctarank() : 0u;
   const bool issuer = rank == 0;                         // issues the group's MMAs
-  const int top_slab = n_pad - 1 - ((int)blockIdx.x - (int)rank);   // the group's last slab
-  const int g = blockIdx.y;
+  const int top_slab = n_pad - 1 - sg * C;               // the group's last slab
+  const int slab = top_slab - (int)rank;
   const int q0 = slab * QR;
   const int S = sh.S, H = sh.H;
 
@@ -1298,10 +1305,13 @@ gqa_status qm_launch_c(const float* Q, const float* K, const float* V, const flo
     return check_launch("query-major smem attribute");
   const int QR = 128 / sh.G;
   const int n_slabs = (sh.S + QR - 1) / QR;
-  dim3 grid((n_slabs + C - 1) / C * C, sh.Hk);
+  const int n_sg = (n_slabs + C - 1) / C;
+  // one CTA per SM (the kernel holds all of TMEM): slab-major below four waves
+  const int slab_major = (long long)n_sg * C * sh.Hk < 4LL * sm_count() ? 1 : 0;
+  const dim3 grid = slab_major ? dim3(C * sh.Hk, n_sg) : dim3(n_sg * C, sh.Hk);
   return launch_clustered(tc_query_major<D, C, GD>, grid, C, Cfg::SMEM_BYTES, st,
                           "tensor-core query-major", mk, mv, mkt, Q, dO, LSE, seg, dQ, Dws, Qt, dOt,
-                          ld_qt, status, sh, rope);
+                          ld_qt, status, sh, rope, slab_major);
 }
 
 template <int D>
