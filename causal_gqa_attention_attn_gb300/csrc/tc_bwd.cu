@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const uint32_t* __restrict__ seg, const uint32_t* __restrict__ blk_minseg,
                  const uint32_t* __restrict__ blk_maxseg, float* __restrict__ dK,
                  float* __restrict__ dV, uint32_t* __restrict__ status, Shape sh,
-                 const RopeParams rope, int tile_major) {
+                 const RopeParams rope, int band) {
   using Cfg = KmCfg<D, C>;
   constexpr int NQ = Cfg::NQ;
   constexpr bool kCl = C > 1;
@@ -703,15 +703,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int S = sh.S, H = sh.H;
   const uint32_t rank = (C > 1) ? cluster_ctarank() : 0u;
   const bool issuer = rank == 0;          // issues the group's MMAs
-  // Dispatch order (CTAs start x-fastest). Kv-head-major, grid (tile groups
-  // * C, Hk): the CTAs running together share one kv head's Q / dO / Q^T /
-  // dO^T stream, which L2 then serves (16k causal: 2.2 GB of DRAM reads per
-  // launch; tile-major: 13.7 GB, at the same time). Tile-major, grid (C * Hk,
-  // tile groups): the heaviest tiles (the first keys, seen by every later
-  // query) of all kv heads start first, which matters when the grid is only
-  // a few waves deep (packed 4k documents: 1.12 -> 0.99 ms). The host picks.
-  const int tg = tile_major ? (int)blockIdx.y : (int)blockIdx.x / C;
-  const int g = tile_major ? (int)blockIdx.x / C : (int)blockIdx.y;
+  // Dispatch order: grid (C * band, Hk / band * n_tg), CTAs start x-fastest:
+  // kv heads in bands of `band`, and within a band the tile groups heaviest
+  // first (the first keys, seen by every later query), each tile group for
+  // all heads of the band. band = 1: head after head, so the CTAs running
+  // together share one head's Q / dO / Q^T / dO^T stream in L2 (16k causal:
+  // 2.0 GB of DRAM reads per launch); band = Hk: the heaviest tiles of every
+  // head first, which matters when the grid is only a few waves deep (packed
+  // 4k documents: 1.12 -> 0.99 ms; at 16k it read 13.7 GB). The host picks.
+  const int n_tg = ((S + 127) / 128 + C - 1) / C;
+  const int tg = (int)blockIdx.y % n_tg;
+  const int g = ((int)blockIdx.y / n_tg) * band + (int)blockIdx.x / C;
   const int kg0 = tg * C * 128;                            // the group's first key
   const int k0 = kg0 + (int)rank * 128;
   const int k_hi = min(kg0 + 128 * C, S) - 1;             // the group's last key
@@ -1244,12 +1246,14 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
     return check_launch("key-major smem attribute");
   const int n_tiles = (sh.S + 127) / 128;
   const int n_tg = (n_tiles + C - 1) / C;
-  // one CTA per SM (the kernel holds all of TMEM): tile-major below four waves
-  const int tile_major = (long long)n_tg * C * sh.Hk < 4LL * sm_count() ? 1 : 0;
-  const dim3 grid = tile_major ? dim3(C * sh.Hk, n_tg) : dim3(n_tg * C, sh.Hk);
+  // one CTA per SM (the kernel holds all of TMEM): all heads in one band
+  // below four waves, else bands of two heads (one when Hk is odd)
+  const bool few_waves = (long long)n_tg * C * sh.Hk < 4LL * sm_count();
+  const int band = few_waves ? sh.Hk : (sh.Hk % 2 == 0 ? 2 : 1);
+  const dim3 grid(C * band, (sh.Hk / band) * n_tg);
   return launch_clustered(tc_key_major<D, C>, grid, C, Cfg::SMEM_BYTES, st, "tensor-core key-major",
                           mv, mq, mdo, mqt, mdot, K, LSE, Dws, seg, blk_minseg, blk_maxseg, dK, dV,
-                          status, sh, rope, tile_major);
+                          status, sh, rope, band);
 }
 
 gqa_status transpose_launch(const float* X, float* Xt, int S, int Hk, int Gx, int d, long long ld,
