@@ -1075,28 +1075,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 // rows of a kv group out as the contiguous K dimension of a K-major operand.
 // ld is S*Gx rounded up to 32; the grid covers all ld columns.
 // ---------------------------------------------------------------------------
+constexpr int kTrRows = 64;   // rows r of X per CTA of the transpose
+
 __global__ void __launch_bounds__(256) group_transpose(const float* __restrict__ X,
                                                        float* __restrict__ Xt, int S, int Hk,
                                                        int Gx, int d, long long ld) {
-  __shared__ float tile[32][33];
+  __shared__ float tile[kTrRows][33];
+  constexpr int PER = kTrRows / 8;                        // rows per thread (blockDim.y = 8)
   const int g = blockIdx.z, e0 = blockIdx.y * 32;
-  const long long r0 = (long long)blockIdx.x * 32, nrows = (long long)S * Gx;
+  const int r0 = blockIdx.x * kTrRows, nrows = S * Gx;    // S * Gx < 2^31 (checked by the API)
   const long long row_stride = (long long)Hk * Gx * d;
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const long long r = r0 + i;
-    float v = 0.f;
+  // all of this thread's loads first (coalesced: 32 consecutive e per row)
+  float v[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int r = r0 + threadIdx.y + 8 * k;
+    v[k] = 0.f;
     if (r < nrows) {
-      const long long q = r / Gx, hh = r % Gx;
-      v = __ldg(X + q * row_stride + (g * Gx + hh) * d + e0 + threadIdx.x);
+      const int q = r / Gx, hh = r - q * Gx;
+      v[k] = __ldg(X + q * row_stride + (long long)(g * Gx + hh) * d + e0 + threadIdx.x);
     }
-    tile[i][threadIdx.x] = v;
   }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) tile[threadIdx.y + 8 * k][threadIdx.x] = v[k];
   __syncthreads();
   // columns nrows .. ld-1 are padding: written as zeros (the panel view of
   // the copy reads them as ordinary elements, masked to zero weight)
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const long long r = r0 + threadIdx.x;
-    if (r < ld) Xt[(long long)(g * d + e0 + i) * ld + r] = tile[threadIdx.x][i];
+#pragma unroll
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    float* dst = Xt + (long long)(g * d + e0 + i) * ld;
+#pragma unroll
+    for (int c = 0; c < kTrRows; c += 32) {
+      const long long r = (long long)r0 + c + threadIdx.x;
+      if (r < ld) dst[r] = tile[c + threadIdx.x][i];
+    }
   }
 }
 
@@ -1258,8 +1270,7 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
 
 gqa_status transpose_launch(const float* X, float* Xt, int S, int Hk, int Gx, int d, long long ld,
                             cudaStream_t st) {
-  const long long nrows = (long long)S * Gx;
-  dim3 grid((unsigned)((nrows + 31) / 32), d / 32, Hk);
+  dim3 grid((unsigned)((ld + kTrRows - 1) / kTrRows), d / 32, Hk);   // ld >= S * Gx
   group_transpose<<<grid, dim3(32, 8), 0, st>>>(X, Xt, S, Hk, Gx, d, ld);
   note_launch();
   return check_launch("group transpose");
