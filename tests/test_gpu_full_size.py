@@ -88,3 +88,36 @@ def test_causal16k_sampled_with_rope(ga):
     kidx = torch.from_numpy(keys1).cuda()
     _check("dK (last keys, all groups, after RoPE)", dK[kidx].cpu().numpy(), rk)
     _check("dV (last keys, all groups)", dV[kidx].cpu().numpy(), rv)
+
+
+@pytest.mark.parametrize("H,Hk,d,docs", [(5, 5, 32, True), (12, 6, 64, True)])
+def test_16k_dispatch_bands_sampled(ga, H, Hk, d, docs):
+    """16k tokens with grids four or more waves deep: the key-major kernel
+    runs kv heads in bands (of one head for an odd count, of two for an even
+    one); packed documents. LSE from this library's forward, consumed by both
+    sides; sampled dQ rows and dK / dV keys against the oracle."""
+    S = 16384
+    rng = np.random.default_rng(H * 100 + d)
+    seg = workloads.random_seg(S, rng) if docs else np.zeros(S, np.uint32)
+    f = lambda c: (0.5 * rng.standard_normal((S, c))).astype(np.float32)  # noqa: E731
+    Q, K, V, dO = f(H * d), f(Hk * d), f(Hk * d), f(H * d)
+    sc = 1.0 / np.sqrt(d)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    tQ, tK, tV, tdO, tseg = dev(Q), dev(K), dev(V), dev(dO), dev(seg.astype(np.int32))
+    _, LSE = ga.attn_fwd(tQ, tK, tV, tseg, H, Hk, d, sc)
+    torch.cuda.synchronize()
+    lse32 = LSE.cpu().numpy()
+    out = [torch.zeros(S, n * d, device="cuda") for n in (H, Hk, Hk)]
+    ws = ga.attn_bwd(tQ, tK, tV, tdO, LSE, tseg, *out, H, Hk, d, sc)
+    ga.read_device_status(ws)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([[0, 1, 127, 128], np.arange(700, S, 1531), [S - 129, S - 1]]))
+    rq = oracle.bwd_rows(Q, K, V, dO, lse32, seg, H, Hk, d, sc, rows)
+    _check("dQ (sampled rows)", out[0][torch.from_numpy(rows).cuda()].cpu().numpy(), rq)
+    keys = np.unique(np.concatenate([[0, 1, 127, 128, 255], np.arange(513, S, 2039), [S - 1]]))
+    g0 = Hk - 1                                    # one kv head (its group's query heads)
+    rk, rv = oracle.bwd_dkdv_keys(Q, K, V, dO, lse32, seg, H, Hk, d, sc, keys, kv_heads=[g0])
+    kidx = torch.from_numpy(keys).cuda()
+    cols = slice(g0 * d, (g0 + 1) * d)
+    _check("dK (sampled keys, one kv head)", out[1][kidx].cpu().numpy()[:, cols], rk[:, cols])
+    _check("dV (sampled keys, one kv head)", out[2][kidx].cpu().numpy()[:, cols], rv[:, cols])
