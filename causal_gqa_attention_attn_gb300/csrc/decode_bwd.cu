@@ -155,23 +155,28 @@ __global__ void __launch_bounds__(kDecThreads) decode_dp(const float* __restrict
   }
 }
 
+// D_h = the per-block partial sums added in a fixed order: thread t adds
+// blocks t, t + 256, ..., each warp its 32 threads by a shuffle tree, then
+// thread 0 the 8 warp sums in warp order.
 __global__ void __launch_bounds__(256) decode_dsum(const float* __restrict__ dpart,
                                                    float* __restrict__ dsum, int nblk, int H) {
-  __shared__ float part[256];
+  __shared__ float part[8];
   const int h = blockIdx.x;
   float s = 0.f;
   for (int b = threadIdx.x; b < nblk; b += 256) s += dpart[(long long)b * H + h];
-  part[threadIdx.x] = s;
+  s = warp_sum(s);
+  if (threadIdx.x % 32 == 0) part[threadIdx.x / 32] = s;
   __syncthreads();
-  for (int w = 128; w >= 1; w >>= 1) {
-    if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
-    __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += part[w];
+    dsum[h] = t;
   }
-  if (threadIdx.x == 0) dsum[h] = part[0];
 }
 
 template <int E>
-__global__ void __launch_bounds__(kDecThreads) decode_dkv(
+__global__ void __launch_bounds__(kDecThreads, E >= 3 ? 4 : 3) decode_dkv(
     const float* __restrict__ q, const float* __restrict__ K, const float* __restrict__ probs,
     const float* __restrict__ d_out, float* __restrict__ dsc, const float* __restrict__ dsum,
     float* __restrict__ dK, float* __restrict__ qpart, int L, int H, int Hk, int G, float scale) {
@@ -253,23 +258,33 @@ __global__ void __launch_bounds__(kDecThreads) decode_dkv(
 }
 
 // d_q[h, c] += sum over blocks of qpart[b, h, c]: grid (H, D / 32), warp w of
-// 8 adds blocks b = w, w + 8, ... of its lane's column, then the 8 warp sums
-// are added in warp order (a fixed order: the result does not depend on
-// scheduling).
-__global__ void __launch_bounds__(256) decode_dq(const float* __restrict__ qpart,
-                                                 float* __restrict__ dq, int nblk, int H, int D) {
-  __shared__ float part[8][32];
+// 32 adds blocks b = w, w + 32, ... of its lane's column (eight loads in
+// flight), then the 32 warp sums are added in warp order (a fixed order: the
+// result does not depend on scheduling).
+constexpr int kDqWarps = 32;
+__global__ void __launch_bounds__(32 * kDqWarps) decode_dq(const float* __restrict__ qpart,
+                                                           float* __restrict__ dq, int nblk, int H,
+                                                           int D) {
+  __shared__ float part[kDqWarps][33];
   const int h = blockIdx.x, lane = threadIdx.x % 32, w = threadIdx.x / 32;
   const int c = blockIdx.y * 32 + lane;
   float s = 0.f;
-#pragma unroll 8
-  for (int b = w; b < nblk; b += 8) s += __ldg(qpart + ((long long)b * H + h) * D + c);
+  for (int b0 = w; b0 < nblk; b0 += 8 * kDqWarps) {
+    float x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int b = b0 + u * kDqWarps;
+      x[u] = b < nblk ? __ldg(qpart + ((long long)b * H + h) * D + c) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) s += x[u];
+  }
   part[w][lane] = s;
   __syncthreads();
   if (w == 0) {
     float t = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) t += part[i][lane];
+#pragma unroll 8
+    for (int i = 0; i < kDqWarps; ++i) t += part[i][lane];
     dq[(long long)h * D + c] += t;
   }
 }
@@ -303,7 +318,7 @@ gqa_status decode_launch(const float* q, const float* k_hist, const float* v_his
                                               L, H, Hk, G, scale);
   note_launch();
   if ((r = check_launch("decode dK dV")) != GQA_OK) return r;
-  decode_dq<<<dim3((unsigned)H, D / 32), 256, 0, st>>>(qpart, d_q, w.nblk, H, D);
+  decode_dq<<<dim3((unsigned)H, D / 32), 32 * kDqWarps, 0, st>>>(qpart, d_q, w.nblk, H, D);
   note_launch();
   return check_launch("decode dQ");
 }
