@@ -49,7 +49,7 @@ inline WsLayout ws_layout(int S, int H) {
 // (128 or 64)/G queries.
 struct TcWsLayout {
   long long ld_kt, ld_qt;
-  size_t kt_off, qt_off, dot_off, blk_off, blkmax_off;
+  size_t kt_off, qt_off, dot_off, blk_off, blkmax_off, part_off;
   size_t total;
 };
 TcWsLayout tc_ws_layout(int S, int H, int Hk, int d);

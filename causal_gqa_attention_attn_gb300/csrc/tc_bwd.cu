@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const uint32_t* __restrict__ seg, const uint32_t* __restrict__ blk_minseg,
                  const uint32_t* __restrict__ blk_maxseg, float* __restrict__ dK,
                  float* __restrict__ dV, uint32_t* __restrict__ status, Shape sh,
-                 const RopeParams rope, int band) {
+                 const RopeParams rope, int band, int n_split, float* __restrict__ parts) {
   using Cfg = KmCfg<D, C>;
   constexpr int NQ = Cfg::NQ;
   constexpr bool kCl = C > 1;
@@ -711,9 +711,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 2.0 GB of DRAM reads per launch); band = Hk: the heaviest tiles of every
   // head first, which matters when the grid is only a few waves deep (packed
   // 4k documents: 1.12 -> 0.99 ms; at 16k it read 13.7 GB). The host picks.
+  // With n_split > 1 (a grid under four waves deep) y also carries the part
+  // of the tile pair's query walk this CTA takes (innermost).
   const int n_tg = ((S + 127) / 128 + C - 1) / C;
-  const int tg = (int)blockIdx.y % n_tg;
-  const int g = ((int)blockIdx.y / n_tg) * band + (int)blockIdx.x / C;
+  const int yy = (int)blockIdx.y / n_split, part = (int)blockIdx.y % n_split;
+  const int tg = yy % n_tg;
+  const int g = (yy / n_tg) * band + (int)blockIdx.x / C;
   const int kg0 = tg * C * 128;                            // the group's first key
   const int k0 = kg0 + (int)rank * 128;
   const int k_hi = min(kg0 + 128 * C, S) - 1;             // the group's last key
@@ -751,7 +754,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort = &bars.abort;
-  BlockWalk walk(blk_minseg, (unsigned)k_hi, qb0, nqb);
+  // this CTA's part of the query blocks [qb0, nqb) (all of them when n_split = 1)
+  const int pb0 = qb0 + (int)((long long)(nqb - qb0) * part / n_split);
+  const int pb1 = qb0 + (int)((long long)(nqb - qb0) * (part + 1) / n_split);
+  BlockWalk walk(blk_minseg, (unsigned)k_hi, pb0, pb1);
 
   if (warp < kProducerWarps) {
     // ---------------- TMA producers: warp 0 loads Q and dO, warp 1 Q^T, dO^T and V ----------------
@@ -1027,17 +1033,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++n;
     }
     // epilogue: warpgroup 0 adds dK (rotated by the RoPE backward of the key's
-    // position when rope.on), warpgroup 1 adds dV (owned rows, NaN-guarded)
+    // position when rope.on), warpgroup 1 adds dV (owned rows, NaN-guarded).
+    // With n_split > 1 each part stores its partial sums instead (zeros when
+    // it saw no block); km_split_reduce adds them up.
     if (ok && mbar_wait<kCl>(&bars.acc_done, 0, abort, status, kSiteKmCompute)) {
       tc_fence_after();
       const long long row = (long long)key * sh.Hk * D + (long long)g * D;
       float* dst_row = (wg == 0 ? dK : dV) + row;
       const uint32_t src = tl + (wg == 0 ? Cfg::T_DK : Cfg::T_DV);
+      float* part_row = parts + ((size_t)(wg * n_split + part) * S) * ((size_t)sh.Hk * D) + row;
       for (int cc = 0; cc < D; cc += 32) {
         float a[32];
         tmem_ld32(src + cc, a);
         tmem_ld_wait();
-        if (key < S && n > 0) {
+        if (n_split > 1) {
+          if (key < S) {
+            float4* pp = reinterpret_cast<float4*>(part_row + cc);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              pp[i] = n > 0 ? make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3])
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        } else if (key < S && n > 0) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) a[i] = (a[i] == a[i]) ? a[i] : 0.f;
           if (wg == 0 && rope.on) {
@@ -1110,6 +1127,43 @@ __global__ void __launch_bounds__(256) group_transpose(const float* __restrict__
       if (r < ld) dst[r] = tile[c + threadIdx.x][i];
     }
   }
+}
+
+// dK += R^T(sum of the key-major parts' dK), dV += sum of their dV: one
+// float4 per thread, parts added in order (a fixed order: deterministic),
+// NaN -> 0 on the sums as in the unsplit epilogue. parts holds [2][n_split]
+// planes of [S][Hk * d] (dK planes, then dV planes).
+__global__ void __launch_bounds__(256) km_split_reduce(const float* __restrict__ parts,
+                                                       float* __restrict__ dK,
+                                                       float* __restrict__ dV, int S, int hkd,
+                                                       int d, int n_split, const RopeParams rope) {
+  const long long n4 = (long long)S * hkd / 4;
+  const long long i4 = (long long)blockIdx.x * 256 + threadIdx.x;
+  if (i4 >= 2 * n4) return;
+  const bool is_v = i4 >= n4;
+  const long long e = (is_v ? i4 - n4 : i4) * 4;        // element index in [S][Hk * d]
+  const size_t plane = (size_t)S * hkd;
+  const float* src = parts + (is_v ? (size_t)n_split * plane : 0) + e;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int p = 0; p < n_split; ++p) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(src + (size_t)p * plane));
+    acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+  }
+  acc.x = (acc.x == acc.x) ? acc.x : 0.f;
+  acc.y = (acc.y == acc.y) ? acc.y : 0.f;
+  acc.z = (acc.z == acc.z) ? acc.z : 0.f;
+  acc.w = (acc.w == acc.w) ? acc.w : 0.f;
+  if (!is_v && rope.on) {
+    const long long key = e / hkd;
+    const int c = (int)(e % hkd) % d;                  // column in the head (even)
+    const long long tpos = key + rope.pos_offset;
+    rope_rotate(acc.x, acc.y, tpos, c / 2, rope);
+    rope_rotate(acc.z, acc.w, tpos, c / 2 + 1, rope);
+  }
+  float4* o = reinterpret_cast<float4*>((is_v ? dV : dK) + e);
+  float4 cur = *o;
+  cur.x += acc.x; cur.y += acc.y; cur.z += acc.z; cur.w += acc.w;
+  *o = cur;
 }
 
 // D[i, h] = sum_e dO[i, h, e] * O[i, h, e]: one warp per (query, head) row,
@@ -1242,7 +1296,7 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
                        const float* LSE, const uint32_t* seg, float* dK, float* dV, const float* Qt,
                        const float* dOt, long long ld_qt, const float* Dws, const uint32_t* blk_minseg,
                        const uint32_t* blk_maxseg, uint32_t* status, const Shape& sh,
-                       cudaStream_t st, const RopeParams& rope) {
+                       cudaStream_t st, const RopeParams& rope, int n_split, float* parts) {
   using Cfg = KmCfg<D, C>;
   const int QB = Cfg::NQ / sh.G;
   CUtensorMap mv, mq, mdo, mqt, mdot;
@@ -1262,10 +1316,17 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
   // below four waves, else bands of two heads (one when Hk is odd)
   const bool few_waves = (long long)n_tg * C * sh.Hk < 4LL * sm_count();
   const int band = few_waves ? sh.Hk : (sh.Hk % 2 == 0 ? 2 : 1);
-  const dim3 grid(C * band, (sh.Hk / band) * n_tg);
-  return launch_clustered(tc_key_major<D, C>, grid, C, Cfg::SMEM_BYTES, st, "tensor-core key-major",
-                          mv, mq, mdo, mqt, mdot, K, LSE, Dws, seg, blk_minseg, blk_maxseg, dK, dV,
-                          status, sh, rope, band);
+  const dim3 grid(C * band, (sh.Hk / band) * n_tg * n_split);
+  r = launch_clustered(tc_key_major<D, C>, grid, C, Cfg::SMEM_BYTES, st,
+                                  "tensor-core key-major", mv, mq, mdo, mqt, mdot, K, LSE, Dws, seg,
+                                  blk_minseg, blk_maxseg, dK, dV, status, sh, rope, band, n_split,
+                                  parts);
+  if (r != GQA_OK || n_split == 1) return r;
+  const long long n4 = (long long)sh.S * sh.Hk * D / 4;
+  km_split_reduce<<<(unsigned)((2 * n4 + 255) / 256), 256, 0, st>>>(parts, dK, dV, sh.S, sh.Hk * D,
+                                                                   D, n_split, rope);
+  note_launch();
+  return check_launch("key-major part sums");
 }
 
 gqa_status transpose_launch(const float* X, float* Xt, int S, int Hk, int Gx, int d, long long ld,
@@ -1289,17 +1350,35 @@ int cta_group() {
 
 // The key-major kernel runs on SM pairs when the pair's half block holds
 // whole queries (G divides NQ/2), else on one SM per key tile.
+int km_cta_group(const Shape& sh) {
+  const int nqh = (sh.d == 128) ? KmCfg<128, 2>::NQH : KmCfg<64, 2>::NQH;
+  return (cta_group() == 2 && nqh % sh.G == 0) ? 2 : 1;
+}
+
+// Parts the key-major kernel splits each tile (pair)'s query walk into: 1
+// when its grid is at least four waves deep (one CTA per SM), else enough
+// parts, at most four, to fill about four waves. Each part writes partial
+// dK / dV sums to the workspace; km_split_reduce adds them up.
+int km_split(const Shape& sh) {
+  const int C = km_cta_group(sh);
+  const long long ctas = (long long)(((sh.S + 127) / 128 + C - 1) / C) * C * sh.Hk;
+  const long long target = 4LL * sm_count();
+  if (ctas >= target) return 1;
+  const long long n = target / ctas;
+  return (int)(n < 1 ? 1 : (n > 4 ? 4 : n));
+}
 template <int D>
 gqa_status km_launch(const float* Q, const float* K, const float* V, const float* dO,
                      const float* LSE, const uint32_t* seg, float* dK, float* dV, const float* Qt,
                      const float* dOt, long long ld_qt, const float* Dws, const uint32_t* blk_minseg,
                      const uint32_t* blk_maxseg, uint32_t* status, const Shape& sh,
-                     cudaStream_t st, const RopeParams& rope) {
-  if (cta_group() == 2 && (KmCfg<D, 2>::NQH % sh.G) == 0)
+                     cudaStream_t st, const RopeParams& rope, float* parts) {
+  const int n_split = km_split(sh);
+  if (km_cta_group(sh) == 2)
     return km_launch_c<D, 2>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, ld_qt, Dws, blk_minseg,
-                             blk_maxseg, status, sh, st, rope);
+                             blk_maxseg, status, sh, st, rope, n_split, parts);
   return km_launch_c<D, 1>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, ld_qt, Dws, blk_minseg,
-                           blk_maxseg, status, sh, st, rope);
+                           blk_maxseg, status, sh, st, rope, n_split, parts);
 }
 
 template <int D, int C, bool GD>
@@ -1376,7 +1455,12 @@ TcWsLayout tc_ws_layout(int S, int H, int Hk, int d) {
   t.dot_off = t.qt_off + align256((size_t)Hk * d * t.ld_qt * sizeof(float));
   t.blk_off = t.dot_off + align256((size_t)Hk * d * t.ld_qt * sizeof(float));
   t.blkmax_off = t.blk_off + align256((size_t)S * sizeof(uint32_t));
-  t.total = t.blkmax_off + align256((size_t)S * sizeof(uint32_t));
+  t.part_off = t.blkmax_off + align256((size_t)S * sizeof(uint32_t));
+  // the key-major kernel's partial dK / dV when it splits its walk
+  const Shape sh{S, H, Hk, d, (int)G, 1.f};
+  const int n_split = tc_supported(sh) ? km_split(sh) : 1;
+  const size_t parts = n_split > 1 ? (size_t)2 * n_split * S * Hk * d * sizeof(float) : 0;
+  t.total = t.part_off + align256(parts);
   return t;
 }
 
@@ -1401,6 +1485,7 @@ gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* d
   float* dOt = reinterpret_cast<float*>(ws + T.dot_off);
   uint32_t* blk = reinterpret_cast<uint32_t*>(ws + T.blk_off);
   uint32_t* blk_max = reinterpret_cast<uint32_t*>(ws + T.blkmax_off);
+  float* parts = reinterpret_cast<float*>(ws + T.part_off);
   const int QB = ((sh.d == 128) ? KmCfg<128, 1>::NQ : KmCfg<64, 1>::NQ) / sh.G;
   gqa_status r;
   if ((r = tile_minseg(seg, sh.S, QB, blk, st, blk_max)) != GQA_OK) return r;
@@ -1420,19 +1505,22 @@ gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* d
       r = qm_launch<32>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope,
                         O != nullptr);
       if (r == GQA_OK)
-        r = km_launch<32>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope);
+        r = km_launch<32>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope,
+                           parts);
       break;
     case 64:
       r = qm_launch<64>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope,
                         O != nullptr);
       if (r == GQA_OK)
-        r = km_launch<64>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope);
+        r = km_launch<64>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope,
+                           parts);
       break;
     default:
       r = qm_launch<128>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope,
                         O != nullptr);
       if (r == GQA_OK)
-        r = km_launch<128>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope);
+        r = km_launch<128>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope,
+                           parts);
       break;
   }
   profile_after(st);
