@@ -79,3 +79,23 @@ def test_decode_bytes_and_inputs():
     a, b = bench.decode_inputs(cfg), bench.decode_inputs(cfg)
     assert a["K"].shape == (5, 16) and a["q"].shape == (32,) and a["K"].dtype == np.float32
     assert all(np.array_equal(a[k], b[k]) for k in a)          # seeded
+
+
+def test_traffic_records_name_known_stages():
+    """Every DRAM-traffic record in profiles/ names a stage whose source files
+    exist, so bench.py can tell whether the record still matches the kernels
+    (the hash itself changes with every kernel edit and is not pinned here)."""
+    import json
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    with open(os.path.join(root, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    csrc = os.path.join(root, "causal_gqa_attention_attn_gb300", "csrc")
+    assert rec
+    for key, r in rec.items():
+        workload, stage = key.split(":", 1)
+        assert stage in bench.STAGE_SOURCES, key
+        for src in bench.STAGE_SOURCES[stage]:
+            assert os.path.exists(os.path.join(csrc, src)), (key, src)
+        assert r["bytes_per_launch"] > 0 and len(r["source_hash"]) == 16
+        assert bench._source_hash(stage) and "ncu" in r["command"]
