@@ -9,7 +9,12 @@ contractions per pair and head), and the fraction of the dense TF32 tensor
 peak.
 
 Prints ONE JSON line (rank 0). ``--impl reference`` times the fp64 CPU
-oracle instead, on a bounded sample of the same workload.
+oracle instead, on a bounded sample of the same workload. Other lines for the
+rest of the path: ``--forward`` (the tensor-core forward, TFLOP/s),
+``--given-o`` (the backward given the forward's O), ``--decode`` (the
+decode-style backward, HBM GB/s); ``--workload`` picks one of the five
+synthetic workloads, ``--path tc|simt`` a kernel family and ``--graph``
+replays the step as a captured CUDA graph (launch-bound short workloads).
 
 Multi-GPU (torchrun): every rank runs its own copy of the workload (the kv-head
 groups, batches or documents of a training step are independent problems), so
