@@ -99,6 +99,21 @@ def test_short_path_limits_and_switch(L):
     assert L.gqa_set_short_path(1) == 1
 
 
+def test_workspace_reserves_key_major_parts(L):
+    """Where the key-major grid is under four waves (one CTA per SM; 148 SMs
+    assumed without a GPU) its walk is split into up to four parts whose
+    partial dK / dV live in the workspace: [2][parts][S][Hk*d] fp32. Deep
+    grids (the 16k workload) reserve nothing for them."""
+    S, H, Hk, d = 2048, 16, 4, 64           # 64 key-major CTAs: four parts
+    parts = 2 * 4 * S * Hk * d * 4
+    qt = Hk * d * (S * (H // Hk)) * 4       # Q^T (and dO^T) copies
+    assert L.attn_bwd_workspace_bytes(S, H, Hk, d) >= parts + 2 * qt
+    S, H, Hk, d = 16384, 32, 8, 128         # 1024 key-major CTAs: no split
+    copies = 2 * Hk * d * (S * (H // Hk)) * 4 + Hk * d * S * 4   # Q^T, dO^T, K^T
+    one_part = 2 * S * Hk * d * 4                                # what a single part would add
+    assert copies <= L.attn_bwd_workspace_bytes(S, H, Hk, d) < copies + one_part // 2
+
+
 def test_fwd_and_rope_reject_bad_arguments(L):
     fwd = lambda S=64, H=4, Hk=2, d=32, s=0.2: L.attn_fwd_lse(  # noqa: E731
         FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, S, H, Hk, d, s, None)
