@@ -224,6 +224,7 @@ def test_edge_shapes(ga, S, H, Hk, d, seg_kind, fn):
 
 @pytest.mark.parametrize("S,H,Hk,d,seg_kind", [
     (2000, 2, 1, 32, "docs"),            # 63 tiles, 2^26.98 multiply-adds per contraction
+    (2048, 1, 1, 32, "causal"),          # seq_len 2048: all 64 query tiles
     (900, 2, 1, 64, "nonmonotone"), (33, 8, 4, 128, "causal"), (31, 3, 1, 8, "docs")])
 def test_short_path_limits(ga, S, H, Hk, d, seg_kind):
     """attn_bwd_short near its work limit (2^27 multiply-adds per contraction)
