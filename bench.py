@@ -96,14 +96,76 @@ def load_peaks() -> dict:
             "source": "fallback"}
 
 
-# Nominal dense rates (TFLOP/s): bf16 2250, tf32 1100. A TF32 contraction is
-# measured against the measured bf16 peak times this ratio.
+# Nominal dense rates (TFLOP/s): bf16 2250, tf32 1100. The secondary TF32
+# figure: the measured bf16 peak times this ratio.
 TF32_PER_BF16 = 1100.0 / 2250.0
 
 
 def tf32_peak(peaks: dict, sustained: bool) -> float:
     key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
     return peaks[key] * TF32_PER_BF16
+
+
+_TF32_MEASURED: dict = {}
+
+
+def measure_tf32(torch, dev, n: int = 8192, best_of: int = 10, sustain_s: float = 4.0) -> dict:
+    """Dense TF32 rate of this GPU, measured in this run the way the bf16 peak
+    was: torch.matmul of fp32 n x n x n with TF32 allowed (cuBLAS, tcgen05
+    kind::tf32), 2 n^3 flop per call. burst = best of `best_of` single calls
+    timed by CUDA events; sustained = calls back to back for `sustain_s`
+    seconds under the power cap. Measured once per process, outside every
+    timed region (after it, so that the GEMM's heat does not touch it)."""
+    if _TF32_MEASURED:
+        return _TF32_MEASURED
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        g = torch.Generator(device=dev).manual_seed(1)
+        a = torch.randn(n, n, device=dev, generator=g)
+        b = torch.randn(n, n, device=dev, generator=g)
+        c = torch.empty(n, n, device=dev)
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        torch.cuda.synchronize()
+        flop = 2.0 * n ** 3
+        best = float("inf")
+        for _ in range(best_of):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        per = max(1, int(sustain_s * 1e3 / best))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(per):
+            torch.matmul(a, b, out=c)
+        e1.record()
+        torch.cuda.synchronize()
+        sus_ms = e0.elapsed_time(e1) / per
+        del a, b, c
+        _TF32_MEASURED.update({
+            "burst": flop / (best / 1e3) / 1e12, "sustained": flop / (sus_ms / 1e3) / 1e12,
+            "how": f"torch.matmul fp32 {n}^3 with allow_tf32 (cuBLAS): best of {best_of} "
+                   f"(burst) and {per} back to back (sustained), this run"})
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    return _TF32_MEASURED
+
+
+def tensor_roofline_peak(torch, dev, peaks: dict) -> tuple[float, dict]:
+    """The TF32 roofline denominator: the burst rate measured in this run
+    (measure_tf32), with the measured-bf16 x nominal-ratio figure kept as a
+    secondary field."""
+    m = measure_tf32(torch, dev)
+    return m["burst"], {"peak_source": f"measured tf32 ({m['how']})",
+                        "tf32_sustained": m["sustained"],
+                        "peak_bf16_ratio": tf32_peak(peaks, sustained=False),
+                        "peak_bf16_ratio_source":
+                            f"{peaks['source']} bf16 burst x nominal tf32/bf16 ratio "
+                            f"{TF32_PER_BF16:.4f}"}
 
 
 def fp32_simt_peak_tflops(n_sm: int, max_mhz: float) -> float:
@@ -419,10 +481,10 @@ def run_gpu(args) -> dict | None:
     props = torch.cuda.get_device_properties(dev)
     tensor_path = "tc" in stage
     clocks = clk.summary()
+    tf32, tf32_info = tensor_roofline_peak(torch, dev, peaks)
     if tensor_path:
-        peak = tf32_peak(peaks, sustained=False)
-        roof = {"bound": "tensor", "unit": UNIT, "peak_source":
-                f"{peaks['source']} bf16 burst x nominal tf32/bf16 ratio {TF32_PER_BF16:.4f}"}
+        peak = tf32
+        roof = {"bound": "tensor", "unit": UNIT, **tf32_info}
     else:
         peak = fp32_simt_peak_tflops(props.multi_processor_count, peaks.get("sm_max_mhz", 2070.0))
         roof = {"bound": "alu", "unit": UNIT, "peak_source":
@@ -435,8 +497,8 @@ def run_gpu(args) -> dict | None:
         ex = executed_flops(d, H, pairs, 7 if args.given_o else 9)
         roof.update({"executed_flops_per_launch": ex,
                      "executed_tflops": ex / (stage_ms / 1e3) / 1e12,
-                     "executed_frac": ex / (stage_ms / 1e3) / 1e12 / peak})
-    tf32 = tf32_peak(peaks, sustained=False)
+                     "executed_frac": ex / (stage_ms / 1e3) / 1e12 / peak,
+                     "frac_of_bf16_ratio_peak": achieved / tf32_info["peak_bf16_ratio"]})
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_max / K, "higher_is_better": True,
@@ -695,9 +757,8 @@ def run_forward(args) -> dict | None:
     peaks = load_peaks()
     tensor_path = stage == "tc_forward"
     if tensor_path:
-        peak = tf32_peak(peaks, sustained=False)
-        roof = {"bound": "tensor", "unit": UNIT, "peak_source":
-                f"{peaks['source']} bf16 burst x nominal tf32/bf16 ratio {TF32_PER_BF16:.4f}"}
+        peak, tf32_info = tensor_roofline_peak(torch, dev, peaks)
+        roof = {"bound": "tensor", "unit": UNIT, **tf32_info}
     else:   # CUDA-core forward (head dims without a tensor-core kernel): no stage events
         props = torch.cuda.get_device_properties(dev)
         peak = fp32_simt_peak_tflops(props.multi_processor_count, peaks.get("sm_max_mhz", 2070.0))

@@ -8,9 +8,15 @@ library's CUDA kernels. PyTorch provides device memory and streams.
 If the shared library has not been built, importing works but the first call
 raises :class:`GqaError`; build it with ``__graft_entry__.build()`` (or
 ``python -m causal_gqa_attention_attn_gb300.build``). There is no fallback.
+
+``checks_build()`` routes the calls made inside its ``with`` block through
+``libgqa_attn_checks.so``, the debug build of the same sources with
+device-side checks (seg precondition, kernel indices) that report through
+the workspace status word (``read_device_status`` raises GQA_ERR_DEVICE_CHECK).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -18,15 +24,17 @@ __all__ = ["GqaError", "lib", "lib_path", "attn_fwd_lse", "attn_bwd", "attn_bwd_
            "rope_bwd_inplace", "workspace_bytes", "read_device_status", "n_pairs_from_seg",
            "profile_events", "profile_stage_name", "launch_count", "attn_bwd_noalloc",
            "attn_fwd", "attn_bwd_rope", "attn_bwd_o", "attn_decode_bwd", "attn_bwd_short",
-           "set_short_path"]
+           "set_short_path", "checks_build"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libgqa_attn.so")
-_lib = None
+_LIB_PATHS = {"release": _LIB_PATH, "checks": os.path.join(_HERE, "libgqa_attn_checks.so")}
+_libs: dict = {}
+_active = "release"
 
 GQA_OK = 0
 _STATUS = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_UNSUPPORTED", 3: "GQA_ERR_CUDA",
-           4: "GQA_ERR_DEVICE_TIMEOUT"}
+           4: "GQA_ERR_DEVICE_TIMEOUT", 5: "GQA_ERR_DEVICE_CHECK"}
 
 
 class GqaError(RuntimeError):
@@ -39,14 +47,17 @@ def lib_path() -> str:
     return _LIB_PATH
 
 
-def lib() -> ctypes.CDLL:
-    """The loaded library (declares the argument types of every entry point)."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(_LIB_PATH):
-        raise GqaError(3, f"{_LIB_PATH} is missing: build it first (__graft_entry__.build())")
-    L = ctypes.CDLL(_LIB_PATH)
+def lib(variant: str | None = None) -> ctypes.CDLL:
+    """The loaded library (declares the argument types of every entry point):
+    the release build, or inside ``checks_build()`` the debug build; an
+    explicit ``variant`` ("release" or "checks") picks one."""
+    variant = _active if variant is None else variant
+    if variant in _libs:
+        return _libs[variant]
+    path = _LIB_PATHS[variant]
+    if not os.path.exists(path):
+        raise GqaError(3, f"{path} is missing: build it first (__graft_entry__.build())")
+    L = ctypes.CDLL(path)
     P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.attn_fwd_lse.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P]
     L.attn_fwd.argtypes = [P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
@@ -87,8 +98,23 @@ def lib() -> ctypes.CDLL:
                  "attn_bwd_rope", "attn_bwd_o",
                  "attn_decode_bwd", "rope_bwd_inplace", "attn_read_device_status"):
         getattr(L, name).restype = ctypes.c_int
-    _lib = L
+    _libs[variant] = L
     return L
+
+
+@contextlib.contextmanager
+def checks_build():
+    """Inside the block, this module's calls go to libgqa_attn_checks.so (the
+    -DGQA_CHECKS debug build); yields that library. Not thread-safe: switch
+    only between calls."""
+    global _active
+    prev = _active
+    L = lib("checks")
+    _active = "checks"
+    try:
+        yield L
+    finally:
+        _active = prev
 
 
 def _check(status: int):

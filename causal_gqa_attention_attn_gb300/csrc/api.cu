@@ -92,6 +92,7 @@ const char* gqa_status_str(gqa_status s) {
     case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED";
     case GQA_ERR_CUDA: return "GQA_ERR_CUDA";
     case GQA_ERR_DEVICE_TIMEOUT: return "GQA_ERR_DEVICE_TIMEOUT";
+    case GQA_ERR_DEVICE_CHECK: return "GQA_ERR_DEVICE_CHECK";
   }
   return "GQA_ERR_UNKNOWN";
 }
@@ -159,6 +160,7 @@ gqa_status attn_fwd(const float* Q, const float* K, const float* V, const uint32
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
     return check_launch("workspace header reset");
+  if ((r = debug_check_seg(seg, seq_len, workspace, st)) != GQA_OK) return r;
   if (!tc_fwd_supported(sh)) return simt_fwd_lse(Q, K, V, seg, O, LSE, sh, st);
   return tc_fwd(Q, K, V, seg, O, LSE, sh, (char*)workspace, st);
 }
@@ -201,6 +203,7 @@ gqa_status attn_bwd_simt(const float* Q, const float* K, const float* V, const f
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
     return check_launch("workspace header reset");
+  if ((r = debug_check_seg(seg, seq_len, workspace, st)) != GQA_OK) return r;
   Shape sh{seq_len, n_heads, n_kv_heads, head_dim, n_heads / n_kv_heads, scale};
   return simt_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st, no_rope());
 }
@@ -225,11 +228,13 @@ static gqa_status bwd_dispatch(const float* Q, const float* K, const float* V, c
       return set_error(GQA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
     if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
       return check_launch("workspace header reset");
+    if ((r = debug_check_seg(seg, seq_len, workspace, st)) != GQA_OK) return r;
     return short_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st, rope);
   }
   if (!tc_supported(sh)) {
     if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
       return check_launch("workspace header reset");
+    if ((r = debug_check_seg(seg, seq_len, workspace, st)) != GQA_OK) return r;
     return simt_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st, rope);
   }
   const size_t need = tc_ws_layout(seq_len, n_heads, n_kv_heads, head_dim).total;
@@ -237,6 +242,7 @@ static gqa_status bwd_dispatch(const float* Q, const float* K, const float* V, c
     return set_error(GQA_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
   if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
     return check_launch("workspace header reset");
+  if ((r = debug_check_seg(seg, seq_len, workspace, st)) != GQA_OK) return r;
   return tc_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st, rope, O);
 }
 
@@ -280,6 +286,7 @@ gqa_status attn_bwd_short(const float* Q, const float* K, const float* V, const 
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(workspace, 0, kWsHeader, st) != cudaSuccess)
     return check_launch("workspace header reset");
+  if ((r = debug_check_seg(seg, seq_len, workspace, st)) != GQA_OK) return r;
   return short_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)workspace, st, no_rope());
 }
 
@@ -355,8 +362,15 @@ gqa_status attn_read_device_status(const void* workspace, void* stream) {
   if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return check_launch("status read");
   if (cudaStreamSynchronize(st) != cudaSuccess) return check_launch("status read sync");
-  if (word != 0)
+  if (word & kStatusTimeout)
     return set_error(GQA_ERR_DEVICE_TIMEOUT, "device status word 0x%08x: a bounded wait gave up", word);
+  if (word & kStatusCheck)
+    return set_error(GQA_ERR_DEVICE_CHECK,
+                     "device status word 0x%08x: a device-side check of the debug build failed "
+                     "(0x1 seg[s] > s, 0x2/0x4 query-major store/load, 0x8/0x10 key-major "
+                     "store/load, 0x20 short path, 0x40 CUDA-core path, 0x80 forward)", word);
+  if (word != 0)
+    return set_error(GQA_ERR_DEVICE_TIMEOUT, "device status word 0x%08x", word);
   return GQA_OK;
 }
 

@@ -54,6 +54,38 @@ struct TcWsLayout {
 };
 TcWsLayout tc_ws_layout(int S, int H, int Hk, int d);
 
+// ---------------------------------------------------------------------------
+// Device status word (workspace byte 0, cleared by each call). A bounded wait
+// that gives up ORs kStatusTimeout | its site. In the debug build
+// (-DGQA_CHECKS, built as libgqa_attn_checks.so) a failed device-side check
+// ORs kStatusCheck | its site and the checked access is skipped (no trap, no
+// fault). attn_read_device_status reports GQA_ERR_DEVICE_TIMEOUT, else
+// GQA_ERR_DEVICE_CHECK. In the release build the checks compile to nothing.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kStatusTimeout = 0x80000000u, kStatusCheck = 0x40000000u;
+enum : uint32_t {
+  kChkSeg = 1u << 0,        // seg[s] > s somewhere (the documented precondition)
+  kChkTcQmStore = 1u << 1,  // query-major kernel: dQ / D / Q^T / dO^T store index
+  kChkTcQmLoad = 1u << 2,   // query-major kernel: Q / dO row or TMA coordinate
+  kChkTcKmStore = 1u << 3,  // key-major kernel: dK / dV / part-sum store index
+  kChkTcKmLoad = 1u << 4,   // key-major kernel: K row, column metadata or TMA coordinate
+  kChkShort = 1u << 5,      // short path: partial or final store index
+  kChkSimt = 1u << 6,       // CUDA-core path: dQ / dK / dV / D store index
+  kChkFwd = 1u << 7,        // tensor-core forward: O / LSE store index or TMA coordinate
+};
+#ifdef GQA_CHECKS
+__device__ __forceinline__ bool dcheck(uint32_t* status, bool ok, uint32_t site) {
+  if (!ok) atomicOr(status, kStatusCheck | site);
+  return ok;
+}
+#define GQA_DCHECK(status, cond, site) ::gqa::dcheck((status), (cond), (site))
+#else
+#define GQA_DCHECK(status, cond, site) true
+#endif
+// Debug build: one pass over seg that flags seg[s] > s (kChkSeg) in the
+// status word at `ws`; the release build launches nothing.
+gqa_status debug_check_seg(const uint32_t* seg, int S, void* ws, cudaStream_t st);
+
 // Problem description passed by value to kernels.
 struct Shape {
   int S, H, Hk, d, G;   // seq_len, n_heads, n_kv_heads, head_dim, H / Hk

@@ -17,12 +17,19 @@
 //  - every call shares the one array: calls whose GPU work overlaps (two
 //    streams, two host threads) race on it and give wrong results;
 //  - the first call on a device looks up the array's device address
-//    (cudaGetSymbolAddress, with that device current) and caches it; make that
-//    first call before any stream capture on the device.
+//    (cudaGetSymbolAddress, with that device current) and caches it together
+//    with the id of the device's current CUDA context; make that first call
+//    before any stream capture on the device. A later call that finds another
+//    context current (after cudaDeviceReset or a primary-context teardown the
+//    library's device code is loaded again and the array may move) looks the
+//    address up again instead of using the stale one.
 // The kernels are the CUDA-core backward (the same ones attn_bwd_simt runs).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 
@@ -38,6 +45,33 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};   // context id the address belongs to
+
+// Unique id of the calling thread's current CUDA context (driver entry
+// points looked up once through the runtime, as for the tensor maps).
+gqa_status current_context_id(unsigned long long* id) {
+  static const auto fns = [] {
+    std::pair<PFN_cuCtxGetCurrent_v4000, PFN_cuCtxGetId_v12000> f{nullptr, nullptr};
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      f.first = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      f.second = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    return f;
+  }();
+  if (fns.first == nullptr || fns.second == nullptr)
+    return set_error(GQA_ERR_CUDA, "cuCtxGetCurrent / cuCtxGetId unavailable");
+  CUcontext ctx = nullptr;
+  if (fns.first(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+    return set_error(GQA_ERR_CUDA, "no current CUDA context");
+  if (fns.second(ctx, id) != CUDA_SUCCESS)
+    return set_error(GQA_ERR_CUDA, "cuCtxGetId failed");
+  return GQA_OK;
+}
 
 gqa_status scratch_address(void** out) {
   int dev = 0;
@@ -46,13 +80,22 @@ gqa_status scratch_address(void** out) {
     return set_error(GQA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices)
     return set_error(GQA_ERR_UNSUPPORTED, "device ordinal %d is beyond %d", dev, kMaxDevices);
+  // cudaSetDevice initialises the device's primary context and makes it
+  // current (a no-op when it already is), so that the context id below is the
+  // one the launches will use; it allocates nothing
+  if ((e = cudaSetDevice(dev)) != cudaSuccess)
+    return set_error(GQA_ERR_CUDA, "cudaSetDevice(%d): %s", dev, cudaGetErrorString(e));
+  unsigned long long ctx = 0;
+  gqa_status r = current_context_id(&ctx);
+  if (r != GQA_OK) return r;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (g_scratch_addr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr)
       return set_error(GQA_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_addr[dev];
   return GQA_OK;
@@ -88,6 +131,7 @@ extern "C" gqa_status attn_bwd_noalloc(const float* Q, const float* K, const flo
   // at zero; D and the per-tile minima are fully rewritten before they are read.
   if (cudaMemsetAsync(ws, 0, kWsHeader, st) != cudaSuccess)
     return check_launch("attn_bwd_noalloc scratch header reset");
+  if ((r = debug_check_seg(seg, seq_len, ws, st)) != GQA_OK) return r;
   Shape sh{seq_len, n_heads, n_kv_heads, head_dim, n_heads / n_kv_heads, scale};
   return simt_bwd(Q, K, V, dO, LSE, seg, dQ, dK, dV, sh, (char*)ws, st, no_rope());
 }

@@ -383,13 +383,15 @@ __global__ void __launch_bounds__(kThr) short_bwd_kernel(const ShortArgs a, cons
     }
     __syncthreads();
     const size_t off = (size_t)cell * kT * DP;
+    // (debug build: the cell decodes to a tile pair of the triangle)
+    const bool cell_ok = GQA_DCHECK(a.status, qt < a.nt && kt <= qt && h < sh.H, kChkShort);
     float4 out[2][DP / 32];
     mm_score_rows<DP, false>(sm.ds, sm.k, out);    // dQ partial = dS K
-    store_partial<DP>(a.dqp + off, out);
+    if (cell_ok) store_partial<DP>(a.dqp + off, out);
     mm_score_rows<DP, true>(sm.ds, sm.q, out);     // dK partial = dS^T Q
-    store_partial<DP>(a.dkp + off, out);
+    if (cell_ok) store_partial<DP>(a.dkp + off, out);
     mm_score_rows<DP, true>(sm.p, sm.dout, out);   // dV partial = P^T dO
-    store_partial<DP>(a.dvp + off, out);
+    if (cell_ok) store_partial<DP>(a.dvp + off, out);
   }
   if (!grid_barrier(a, 2u * gridDim.x, kSiteBarrier2, &sm.ok)) return;
 
@@ -411,6 +413,7 @@ __global__ void __launch_bounds__(kThr) short_bwd_kernel(const ShortArgs a, cons
     const int tile = rem / NRG, r = (rem % NRG) * RPI + rr;
     const int pos = tile * kT + r;             // row (dQ) or key (dK, dV)
     if (pos >= S || 4 * qd >= d) continue;
+    if (!GQA_DCHECK(a.status, hh < (kind == 0 ? sh.H : sh.Hk) && tile < a.nt, kChkShort)) continue;
     float4 acc;
     if (kind == 0) {
       // dQ[pos, head hh]: partials over the visible key tiles (consecutive cells)

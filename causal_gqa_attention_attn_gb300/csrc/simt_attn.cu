@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(NT) bwd_query_major(
     const float* __restrict__ Q, const float* __restrict__ K, const float* __restrict__ V,
     const float* __restrict__ dO, const float* __restrict__ LSE, const uint32_t* __restrict__ seg,
     float* __restrict__ dQ, float* __restrict__ Dws, uint32_t* __restrict__ minseg64, Shape sh,
-    const RopeParams rope) {
+    const RopeParams rope, uint32_t* __restrict__ status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   QmSmem<DP>& sm = *reinterpret_cast<QmSmem<DP>*>(smem_raw);
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
@@ -288,7 +288,9 @@ __global__ void __launch_bounds__(NT) bwd_query_major(
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     D[i] = half_warp_sum(Dp[i]);
-    if (tx == 0 && row[i] < S) Dws[(long long)row[i] * sh.H + h] = D[i];
+    if (tx == 0 && row[i] < S &&
+        GQA_DCHECK(status, h < sh.H && (long long)row[i] * sh.H + h < (long long)S * sh.H, kChkSimt))
+      Dws[(long long)row[i] * sh.H + h] = D[i];
   }
 
   // Pass 2: dS = scale P (dP - D), dQ_i += sum_j dS_ij k_j
@@ -326,7 +328,9 @@ __global__ void __launch_bounds__(NT) bwd_query_major(
       float v = acc[i][n];
       v = (v == v) ? v : 0.f;   // NaN guard on the final write, as the pages do
       if (rope.on) rope_pair_shfl(v, c, (long long)row[i] + rope.pos_offset, tx, rope);
-      if (row[i] < S && c < d) dQ[(long long)row[i] * ldq + h * d + c] += v;
+      if (row[i] < S && c < d &&
+          GQA_DCHECK(status, (long long)row[i] * ldq + h * d + c < (long long)S * ldq, kChkSimt))
+        dQ[(long long)row[i] * ldq + h * d + c] += v;
     }
   }
 }
@@ -345,7 +349,7 @@ __global__ void __launch_bounds__(NT) bwd_key_major(
     const float* __restrict__ Q, const float* __restrict__ K, const float* __restrict__ V,
     const float* __restrict__ dO, const float* __restrict__ LSE, const uint32_t* __restrict__ seg,
     const float* __restrict__ Dws, const uint32_t* __restrict__ minseg64, float* __restrict__ dK,
-    float* __restrict__ dV, Shape sh, const RopeParams rope) {
+    float* __restrict__ dV, Shape sh, const RopeParams rope, uint32_t* __restrict__ status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   KmSmem<DP>& sm = *reinterpret_cast<KmSmem<DP>*>(smem_raw);
   const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
@@ -414,7 +418,9 @@ __global__ void __launch_bounds__(NT) bwd_key_major(
       const float b = dv[i][n];
       a = (a == a) ? a : 0.f;
       if (rope.on) rope_pair_shfl(a, c, (long long)key + rope.pos_offset, tx, rope);
-      if (key < S && c < d) {
+      if (key < S && c < d &&
+          GQA_DCHECK(status, g < sh.Hk && (long long)key * ldk + g * d + c < (long long)S * ldk,
+                     kChkSimt)) {
         const long long o = (long long)key * ldk + g * d + c;
         dK[o] += a;
         dV[o] += (b == b) ? b : 0.f;
@@ -451,11 +457,14 @@ gqa_status bwd_launch(const float* Q, const float* K, const float* V, const floa
   if (allow_smem(bwd_key_major<DP>, s2) != cudaSuccess) return check_launch("bwd smem attribute");
   const int nt = (sh.S + BT - 1) / BT;
   profile_before(st, "simt_bwd_query_major+key_major");
-  bwd_query_major<DP><<<dim3(nt, sh.H), NT, s1, st>>>(Q, K, V, dO, LSE, seg, dQ, Dws, minseg, sh, rope);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  bwd_query_major<DP><<<dim3(nt, sh.H), NT, s1, st>>>(Q, K, V, dO, LSE, seg, dQ, Dws, minseg, sh, rope,
+                                                      status);
   note_launch();
   gqa_status r = check_launch("simt backward (query-major)");
   if (r != GQA_OK) return r;
-  bwd_key_major<DP><<<dim3(nt, sh.Hk), NT, s2, st>>>(Q, K, V, dO, LSE, seg, Dws, minseg, dK, dV, sh, rope);
+  bwd_key_major<DP><<<dim3(nt, sh.Hk), NT, s2, st>>>(Q, K, V, dO, LSE, seg, Dws, minseg, dK, dV, sh, rope,
+                                                      status);
   note_launch();
   profile_after(st);
   return check_launch("simt backward (key-major)");
@@ -486,7 +495,28 @@ __global__ void tile_minseg_kernel(const uint32_t* __restrict__ seg, int S, int 
   }
 }
 
+#ifdef GQA_CHECKS
+// Debug build: flags seg[s] > s (the precondition every path relies on).
+__global__ void seg_check_kernel(const uint32_t* __restrict__ seg, int S, uint32_t* status) {
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < S; s += gridDim.x * blockDim.x)
+    if (__ldg(seg + s) > (uint32_t)s) atomicOr(status, kStatusCheck | kChkSeg);
+}
+#endif
+
 }  // namespace
+
+gqa_status debug_check_seg(const uint32_t* seg, int S, void* ws, cudaStream_t st) {
+#ifdef GQA_CHECKS
+  if (S <= 0) return GQA_OK;
+  const int blocks = (S + 255) / 256 < 1024 ? (S + 255) / 256 : 1024;
+  seg_check_kernel<<<blocks, 256, 0, st>>>(seg, S, reinterpret_cast<uint32_t*>(ws));
+  note_launch();
+  return check_launch("seg check (debug build)");
+#else
+  (void)seg; (void)S; (void)ws; (void)st;
+  return GQA_OK;
+#endif
+}
 
 gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cudaStream_t st,
                        uint32_t* out_max) {

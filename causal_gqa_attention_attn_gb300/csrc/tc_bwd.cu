@@ -1,21 +1,26 @@
 // Tensor-core backward (tcgen05, kind::tf32, fp32 accumulation in TMEM).
 //
-// Two kernels, both warp-specialised (TMA producer warp, MMA warp, four
-// compute warps that own the 128 TMEM lanes), with every operand resident on
-// chip:
+// Two kernels, both warp-specialised: two TMA producer warps, one MMA warp
+// (one elected lane issues every MMA and commit) and two compute warpgroups
+// (eight warps; a warp reads and writes the 32 TMEM lanes of its quadrant,
+// the two warpgroups split the columns of each tile), with every operand
+// resident on chip. By default both run on SM pairs (cta_group::2, M = 256).
 //
 //  tc_query_major (grid: query slabs x kv heads). A slab is 128 rows =
 //    (128 / G) queries x the G query heads of one kv group, so the whole group
 //    shares each K/V chunk. Q and dO of the slab sit in TMEM as the A operands;
-//    K/V chunks of BK keys stream through a TMA ring (128-byte swizzle).
+//    K/V chunks stream through a TMA ring (128-byte swizzle).
 //    Pass 1 over the visible chunks: S = Q K^T, dP = dO V^T, D += rowsum(P dP)
 //    (backward_attention.wgsl, attention_backward Pass A). Pass 2: the same
 //    S, dP, then dS = scale P (dP - D) written back to TMEM over S and
 //    dQ += dS K (Pass B), with B = the matching chunk of K^T (a transposed
 //    copy of K in the workspace: the TF32 MMA reads both operands K-major).
-//    dQ and D are owned writes (no atomics).
+//    dQ and D are owned writes (no atomics). Its prologue also writes the
+//    transposed copies Q^T and dO^T that the key-major kernel reads.
 //
-//  tc_key_major (grid: key tiles x kv heads): added below.
+//  tc_key_major (grid: key tiles x kv heads): dK and dV of 128 keys, summed
+//    over the G heads of the group, from S^T = K Q^T and dP^T = V dO^T
+//    (attention_backward_short_dKdV's key-major ownership); see below.
 //
 // Rows of a slab are ordered query-major: row r = (r / G)-th query, head
 // g*G + r % G, which is also the memory order of Q / dO / dQ for a group.
@@ -219,6 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kProducerWarps) {
     // ---------------- TMA producers: warp pw loads this CTA's part of the units i with i % 2 == pw ----------------
     const int pw = warp;
+    // debug build: the group's K / V / K^T rows exist and the last chunk
+    // starts inside the sequence (recorded only: a box outside the tensor
+    // reads the fill value)
+    (void)GQA_DCHECK(status, g < sh.Hk && kc0 >= 0 && (kc0 + nk - 1) * Cfg::BK1 < S, kChkTcQmLoad);
     if (elect_one()) {
       tma_prefetch_desc(&mapK);
       tma_prefetch_desc(&mapV);
@@ -392,7 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = 32 * (warp & 3) + lane;
     const int qi = r / G, q = q0 + qi;
     const int h = g * G + r % G;
-    const bool valid = q < S;
+    // (debug build: the row's Q / dO / dQ range and its LSE / D index lie in
+    // the tensors; a row that fails is treated as padding)
+    const bool valid = q < S && GQA_DCHECK(status, h < H && g < sh.Hk, kChkTcQmLoad);
     const uint32_t tl = lane_base(tmem, warp);
     const long long row_off = (long long)q * H * D + (long long)h * D;
     // Q (warpgroup 0) or dO (warpgroup 1) rows into TMEM, rounded to TF32:
@@ -405,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* src = (wg == 0) ? Q : dO;
       float* xt = (wg == 0) ? Qt : dOt;
       const long long col = (long long)q0 * G + r;
-      const bool in_ld = col < ld_qt;
+      const bool in_ld = col < ld_qt && GQA_DCHECK(status, g < sh.Hk && col >= 0, kChkTcQmStore);
       const uint32_t col0 = (wg == 0) ? Cfg::T_Q : Cfg::T_DO;
       float v[32];
       for (int cc = 0; cc < D; cc += 32) {
@@ -765,6 +776,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // free once its S^T / dP^T ran, Q^T / dO^T once its dV / dK ran. With
     // C = 2 this CTA loads its half of each block.
     const int pw = warp;
+    // debug build: the group's heads and rows exist (recorded only, as above)
+    (void)GQA_DCHECK(status, g < sh.Hk && (g + 1) * G <= H && kg0 < S, kChkTcKmLoad);
     if (elect_one()) {
       if (pw == 0) {
         tma_prefetch_desc(&mapQ);
@@ -943,6 +956,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = k0 + r;
     const uint32_t tl = lane_base(tmem, warp);
     const int wt = threadIdx.x - 32 * kFirstCompute - 128 * wg;   // 0..127 within the warpgroup
+    // (debug build: this kv head's K / dK / dV columns exist)
+    const bool g_ok = GQA_DCHECK(status, g < sh.Hk, kChkTcKmLoad);
     {
       // K rows into TMEM (A of S^T), rounded to TF32; warpgroup wg: half wg of the columns
       float v[16];
@@ -950,7 +965,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int cc = wg * (D / 2); cc < (wg + 1) * (D / 2); cc += 16) {   // D/2 >= 16
 #pragma unroll
         for (int i = 0; i < 16; i += 4) {
-          float4 x = (key < S) ? __ldg(reinterpret_cast<const float4*>(krow + cc + i))
+          float4 x = (key < S && g_ok) ? __ldg(reinterpret_cast<const float4*>(krow + cc + i))
                                : make_float4(0.f, 0.f, 0.f, 0.f);
           v[i] = to_tf32(x.x); v[i + 1] = to_tf32(x.y); v[i + 2] = to_tf32(x.z); v[i + 3] = to_tf32(x.w);
         }
@@ -977,7 +992,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int col = wg * HQ + wt;
         const int q = qb * QB + col / G, h = g * G + col % G;
         float4 m = make_float4(0.f, 0.f, __int_as_float(-1), __int_as_float(0x7fffffff));
-        if (q < S)
+        if (q < S && GQA_DCHECK(status, h < H, kChkTcKmLoad))
           m = make_float4(__ldg(LSE + (long long)q * H + h) * kLog2e, Dws[(long long)q * H + h],
                           __int_as_float(q), __int_as_float((int)__ldg(seg + q)));
         meta[wg][b][wt] = m;
@@ -1047,14 +1062,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(src + cc, a);
         tmem_ld_wait();
         if (n_split > 1) {
-          if (key < S) {
+          if (key < S && g_ok &&
+              GQA_DCHECK(status, (size_t)(wg * n_split + part + 1) * S * ((size_t)sh.Hk * D) >=
+                                     (size_t)(wg * n_split + part) * S * ((size_t)sh.Hk * D) + row + D &&
+                                 wg * n_split + part < 2 * n_split,
+                         kChkTcKmStore)) {
             float4* pp = reinterpret_cast<float4*>(part_row + cc);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               pp[i] = n > 0 ? make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3])
                             : make_float4(0.f, 0.f, 0.f, 0.f);
           }
-        } else if (key < S && n > 0) {
+        } else if (key < S && n > 0 && g_ok &&
+                   GQA_DCHECK(status, row + D <= (long long)S * sh.Hk * D, kChkTcKmStore)) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) a[i] = (a[i] == a[i]) ? a[i] : 0.f;
           if (wg == 0 && rope.on) {
@@ -1132,14 +1152,17 @@ __global__ void __launch_bounds__(256) group_transpose(const float* __restrict__
 // dK += R^T(sum of the key-major parts' dK), dV += sum of their dV: one
 // float4 per thread, parts added in order (a fixed order: deterministic),
 // NaN -> 0 on the sums as in the unsplit epilogue. parts holds [2][n_split]
-// planes of [S][Hk * d] (dK planes, then dV planes).
+// planes of [S][Hk * d] (dK planes, then dV planes). When a bounded wait of
+// the backward gave up (status word set), a part that aborted has not written
+// its slice and the planes may hold an earlier call's sums: nothing is added.
 __global__ void __launch_bounds__(256) km_split_reduce(const float* __restrict__ parts,
                                                        float* __restrict__ dK,
                                                        float* __restrict__ dV, int S, int hkd,
-                                                       int d, int n_split, const RopeParams rope) {
+                                                       int d, int n_split, const RopeParams rope,
+                                                       const uint32_t* __restrict__ status) {
   const long long n4 = (long long)S * hkd / 4;
   const long long i4 = (long long)blockIdx.x * 256 + threadIdx.x;
-  if (i4 >= 2 * n4) return;
+  if (i4 >= 2 * n4 || *status != 0u) return;
   const bool is_v = i4 >= n4;
   const long long e = (is_v ? i4 - n4 : i4) * 4;        // element index in [S][Hk * d]
   const size_t plane = (size_t)S * hkd;
@@ -1324,7 +1347,7 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
   if (r != GQA_OK || n_split == 1) return r;
   const long long n4 = (long long)sh.S * sh.Hk * D / 4;
   km_split_reduce<<<(unsigned)((2 * n4 + 255) / 256), 256, 0, st>>>(parts, dK, dV, sh.S, sh.Hk * D,
-                                                                   D, n_split, rope);
+                                                                   D, n_split, rope, status);
   note_launch();
   return check_launch("key-major part sums");
 }
@@ -1359,13 +1382,23 @@ int km_cta_group(const Shape& sh) {
 // when its grid is at least four waves deep (one CTA per SM), else enough
 // parts, at most four, to fill about four waves. Each part writes partial
 // dK / dV sums to the workspace; km_split_reduce adds them up.
-int km_split(const Shape& sh) {
+int km_split_for(const Shape& sh, int n_sm) {
   const int C = km_cta_group(sh);
   const long long ctas = (long long)(((sh.S + 127) / 128 + C - 1) / C) * C * sh.Hk;
-  const long long target = 4LL * sm_count();
+  const long long target = 4LL * n_sm;
   if (ctas >= target) return 1;
   const long long n = target / ctas;
   return (int)(n < 1 ? 1 : (n > 4 ? 4 : n));
+}
+// The workspace holds the parts of the split a device with kWsSmBound SMs
+// would take (km_split_for grows with the SM count), so that the workspace
+// size depends on the shape alone; a device with more SMs than that is held
+// to that split.
+constexpr int kWsSmBound = 192;
+int km_split_ws(const Shape& sh) { return km_split_for(sh, kWsSmBound); }
+int km_split(const Shape& sh) {
+  const int a = km_split_for(sh, sm_count()), b = km_split_ws(sh);
+  return a < b ? a : b;
 }
 template <int D>
 gqa_status km_launch(const float* Q, const float* K, const float* V, const float* dO,
@@ -1458,7 +1491,7 @@ TcWsLayout tc_ws_layout(int S, int H, int Hk, int d) {
   t.part_off = t.blkmax_off + align256((size_t)S * sizeof(uint32_t));
   // the key-major kernel's partial dK / dV when it splits its walk
   const Shape sh{S, H, Hk, d, (int)G, 1.f};
-  const int n_split = tc_supported(sh) ? km_split(sh) : 1;
+  const int n_split = tc_supported(sh) ? km_split_ws(sh) : 1;
   const size_t parts = n_split > 1 ? (size_t)2 * n_split * S * Hk * d * sizeof(float) : 0;
   t.total = t.part_off + align256(parts);
   return t;

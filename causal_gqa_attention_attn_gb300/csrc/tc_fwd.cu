@@ -208,7 +208,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int r = 32 * (warp & 3) + lane;
     const int qi = r / G, q = q0 + qi;
     const int h = g * G + r % G;
-    const bool valid = q < S;
+    // (debug build: the row's Q / O range and LSE index lie in the tensors;
+    // a row that fails is treated as padding)
+    const bool valid = q < S && GQA_DCHECK(status, h < H && g < sh.Hk, kChkFwd);
     const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const long long row_off = (long long)q * H * D + (long long)h * D;
     {

@@ -45,7 +45,8 @@ typedef enum {
   GQA_ERR_INVALID_ARG = 1,    /* bad pointer, size, alignment or workspace        */
   GQA_ERR_UNSUPPORTED = 2,    /* valid shape with no kernel (e.g. head_dim > 128) */
   GQA_ERR_CUDA = 3,           /* a CUDA launch or copy failed                     */
-  GQA_ERR_DEVICE_TIMEOUT = 4  /* a bounded device-side wait gave up (see below)   */
+  GQA_ERR_DEVICE_TIMEOUT = 4, /* a bounded device-side wait gave up (see below)   */
+  GQA_ERR_DEVICE_CHECK = 5    /* debug build only: a device-side check failed     */
 } gqa_status;
 
 /*
@@ -66,8 +67,10 @@ gqa_status attn_fwd_lse(const float* Q, const float* K, const float* V, const ui
  * attn_fwd_workspace_bytes / attn_fwd — the same forward as attn_fwd_lse (O
  * and LSE overwritten, same definitions and arguments), on tensor cores for
  * head_dim 32, 64, 128 (tcgen05 kind::tf32: S = scale Q.K^T with TF32
- * operands, fp32 accumulation; LSE from a first pass over the keys, then O =
- * sum_j exp(s_ij - LSE) v_j with P rounded to TF32), else on CUDA cores.
+ * operands, fp32 accumulation; one pass over the visible keys with an online
+ * softmax: a running row max m and sum l, P = exp(s - m) rounded to TF32 and
+ * O += P V, the accumulator rescaled when m rises; at the end O = O / l and
+ * LSE = m + ln l), else on CUDA cores.
  * workspace: >= attn_fwd_workspace_bytes(...) device bytes, caller-owned (a
  * status header and a transposed copy of V). Bounded device waits report
  * through attn_read_device_status(workspace) as for attn_bwd.
@@ -109,9 +112,13 @@ gqa_status attn_decode_bwd(const float* q, const float* k_hist, const float* v_h
                            size_t workspace_bytes, void* stream);
 
 /*
- * attn_bwd_workspace_bytes — bytes of device workspace attn_bwd needs for this
- * shape (a multiple of 256). The caller allocates it (any contents) and may
- * reuse it across calls that do not overlap on the GPU.
+ * attn_bwd_workspace_bytes — bytes of device workspace attn_bwd (and
+ * attn_bwd_o, attn_bwd_rope, attn_bwd_short, attn_bwd_simt) needs for this
+ * shape (a multiple of 256). It depends on the shape alone, not on the device
+ * (the part it reserves for a split key-tile walk is sized for devices with
+ * up to 192 SMs; a device with more SMs splits no further than that). The
+ * caller allocates it (any contents) and may reuse it across calls that do
+ * not overlap on the GPU.
  */
 size_t attn_bwd_workspace_bytes(int seq_len, int n_heads, int n_kv_heads, int head_dim);
 
@@ -233,8 +240,10 @@ gqa_status attn_bwd_simt(const float* Q, const float* K, const float* V, const f
  * holds the array until exit. All calls share it: calls whose GPU work
  * overlaps (other streams or host threads) race and give wrong results. The
  * first call on a device looks up the array's address with that device
- * current; make that first call before any stream capture. It runs the
- * CUDA-core kernels (same results as attn_bwd_simt); dQ, dK, dV are
+ * current; make that first call before any stream capture. The address is
+ * kept with the id of the device's current CUDA context and looked up again
+ * when another context is current (after cudaDeviceReset the array may have
+ * moved). It runs the CUDA-core kernels (same results as attn_bwd_simt); dQ, dK, dV are
  * accumulated (+=) as in attn_bwd.
  */
 gqa_status attn_bwd_noalloc(const float* Q, const float* K, const float* V, const float* dO,
@@ -249,9 +258,13 @@ gqa_status attn_bwd_noalloc(const float* Q, const float* K, const float* V, cons
  * head_dim/2 of every head at row s, with t = pos_offset + s and
  * theta = t * base^(-2p/head_dim):
  *   (x0, x1) <- (x0*cos theta + x1*sin theta, -x0*sin theta + x1*cos theta)
- * on columns (2p, 2p+1). The angle is reduced in fp64 on the device, so large
- * positions keep full fp32 accuracy. head_dim a multiple of 4 (at most 128),
- * base > 0, pos_offset >= 0.
+ * on columns (2p, 2p+1). The per-pair frequencies base^(-2p/head_dim) are
+ * formed in fp64 on the host; the angle is reduced modulo 2*pi before fp32
+ * sin/cos, so large positions keep fp32 accuracy (an fp32 product alone is
+ * ~1e-3 rad off at t = 16k): for t < 2^15 in fp32 (the frequency split into
+ * two floats, t * f_hi carried exactly with its FMA error term, 2*pi split
+ * into three constants: Cody & Waite's reduction), for larger t in fp64.
+ * head_dim a multiple of 4 (at most 128), base > 0, pos_offset >= 0.
  */
 gqa_status rope_bwd_inplace(float* dX, int seq_len, int n_heads, int head_dim,
                             int pos_offset, float base, void* stream);
@@ -261,6 +274,19 @@ gqa_status rope_bwd_inplace(float* dX, int seq_len, int n_heads, int head_dim,
  * reads the device-side status word that the last attn_bwd on this workspace
  * left (GQA_OK, or GQA_ERR_DEVICE_TIMEOUT if a bounded wait inside a kernel
  * gave up and the kernel returned early instead of hanging).
+ *
+ * Debug build. libgqa_attn_checks.so is the same library compiled with
+ * -DGQA_CHECKS (stand-ins for a memory checker, after the defensive clamps
+ * and guards of backward_attention.wgsl's attention_backward_short and
+ * attention_backward): every call taking a workspace first checks the
+ * precondition seg[s] <= s on the device, and the kernels check the indices
+ * of their global stores and loads (and the coordinates of their TMA boxes)
+ * against the tensors' extents. A failed check sets a bit in the status word
+ * (0x40000000 | site: 0x1 seg, 0x2/0x4 query-major store/load, 0x8/0x10
+ * key-major store/load, 0x20 short path, 0x40 CUDA-core path, 0x80 forward)
+ * and skips the access; it never traps. attn_read_device_status then
+ * returns GQA_ERR_DEVICE_CHECK (GQA_ERR_DEVICE_TIMEOUT takes precedence).
+ * In the release library the checks are compiled out.
  */
 gqa_status attn_read_device_status(const void* workspace, void* stream);
 

@@ -61,16 +61,32 @@ def test_causal16k_sampled_with_rope(ga):
     torch.cuda.synchronize()
     assert bool(torch.isfinite(dQ).all()) and bool(torch.isfinite(dK).all())
     assert bool(torch.isfinite(dV).all())
+    # run to run: a second call into fresh buffers is bit-identical (no atomics)
+    again = [torch.zeros_like(t) for t in (dQ, dK, dV)]
+    ga.attn_bwd_rope(Q, K, V, dO, LSE, seg, *again, H, Hk, d, sc, pos_offset=0, base=10000.0,
+                     workspace=ws)
+    ga.read_device_status(ws)
+    for nm, u, v in zip(("dQ", "dK", "dV"), (dQ, dK, dV), again):
+        assert torch.equal(u.view(torch.int32), v.view(torch.int32)), f"{nm} differs between runs"
+    del again
 
-    rows = np.unique(np.concatenate([[0, 1, 2, 63, 64, 127, 128, 129], np.arange(1000, S, 997),
+    # one row in every 32-query slab of the query-major kernel (128 rows = 32
+    # queries x 4 heads), at a varying offset inside the slab, plus the edges
+    slab = 128 // (H // Hk)
+    per_slab = np.arange(0, S, slab) + (np.arange(S // slab) * 7) % slab
+    rows = np.unique(np.concatenate([[0, 1, 2, 63, 64, 127, 128, 129], per_slab,
                                      [S - 129, S - 128, S - 65, S - 2, S - 1]]))
     rq = oracle.bwd_rows(x["Q"], x["K"], x["V"], x["dO"], lse32, x["seg"], H, Hk, d, sc, rows)
     rq = np.concatenate([oracle.rope_bwd(rq[i:i + 1], H, d, pos_offset=int(r))
                          for i, r in enumerate(rows)])
     _check("dQ (sampled rows, after RoPE)", dQ[torch.from_numpy(rows).cuda()].cpu().numpy(), rq)
 
+    # one key in every 128-key tile of the key-major kernel (both tiles of
+    # every SM pair), at a varying offset inside the tile, plus the edges
     g0 = 5
-    keys0 = np.array([0, 1, 31, 63, 64, 100, 127, 128, 4095, 8191, 8192, 12345, S - 1])
+    per_tile = np.arange(0, S, 128) + (np.arange(S // 128) * 37) % 128
+    keys0 = np.unique(np.concatenate([[0, 1, 31, 63, 64, 100, 127, 128, 4095, 8191, 8192, 12345,
+                                       S - 1], per_tile]))
     rk, rv = oracle.bwd_dkdv_keys(x["Q"], x["K"], x["V"], x["dO"], lse32, x["seg"], H, Hk, d, sc,
                                   keys0, kv_heads=[g0])
     cols = slice(g0 * d, (g0 + 1) * d)

@@ -38,7 +38,8 @@ def test_every_declared_symbol_is_exported(L):
 
 def test_status_strings(L):
     for code, name in ((0, "GQA_OK"), (1, "GQA_ERR_INVALID_ARG"), (2, "GQA_ERR_UNSUPPORTED"),
-                       (3, "GQA_ERR_CUDA"), (4, "GQA_ERR_DEVICE_TIMEOUT")):
+                       (3, "GQA_ERR_CUDA"), (4, "GQA_ERR_DEVICE_TIMEOUT"),
+                       (5, "GQA_ERR_DEVICE_CHECK")):
         assert L.gqa_status_str(code).decode() == name
 
 
@@ -100,10 +101,11 @@ def test_short_path_limits_and_switch(L):
 
 
 def test_workspace_reserves_key_major_parts(L):
-    """Where the key-major grid is under four waves (one CTA per SM; 148 SMs
-    assumed without a GPU) its walk is split into up to four parts whose
-    partial dK / dV live in the workspace: [2][parts][S][Hk*d] fp32. Deep
-    grids (the 16k workload) reserve nothing for them."""
+    """Where the key-major grid is under four waves (one CTA per SM) its walk
+    is split into up to four parts whose partial dK / dV live in the
+    workspace: [2][parts][S][Hk*d] fp32, sized for devices of up to 192 SMs,
+    so the size depends on the shape alone. Deep grids (the 16k workload)
+    reserve nothing for them."""
     S, H, Hk, d = 2048, 16, 4, 64           # 64 key-major CTAs: four parts
     parts = 2 * 4 * S * Hk * d * 4
     qt = Hk * d * (S * (H // Hk)) * 4       # Q^T (and dO^T) copies
@@ -198,7 +200,21 @@ def test_decode_backward_rejects_bad_arguments(L):
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
-    monkeypatch.setattr(ga, "_lib", None)
-    monkeypatch.setattr(ga, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(ga, "_libs", {})
+    monkeypatch.setattr(ga, "_LIB_PATHS", {"release": str(tmp_path / "missing.so"),
+                                            "checks": str(tmp_path / "missing_checks.so")})
     with pytest.raises(ga.GqaError):
         ga.lib()
+    with pytest.raises(ga.GqaError):
+        ga.lib("checks")
+
+
+def test_checks_library_exports_every_symbol():
+    """The debug build (-DGQA_CHECKS) exports the same C ABI as the release
+    build, and both name the debug-only status code."""
+    gbuild.build()
+    for variant in ("release", "checks"):
+        L = ga.lib(variant)
+        for name in _declared_functions():
+            assert hasattr(L, name), (variant, name)
+        assert L.gqa_status_str(5) == b"GQA_ERR_DEVICE_CHECK"
