@@ -30,6 +30,7 @@
 #include <stdlib.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "common.cuh"
 #include "tc_common.cuh"
@@ -172,9 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NU; ++i) {
-      // the producer warp of the unit arms its bytes; in the issuing CTA of a
-      // pair the odd CTA's forward of its half is the second arrival
-      mbar_init(&bars.full[i], issuer ? C : 1);
+      mbar_init(&bars.full[i], 1);        // armed by this CTA's producer warp (its bytes)
       mbar_init(&bars.empty[i], 1);       // released by the issuer's MMA commit
     }
     for (int i = 0; i < 2; ++i) {
@@ -259,24 +258,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i_lo = max(0, n_units - NU);
     for (int i = i_lo + (((i_lo & 1) != pw) ? 1 : 0); i < n_units; i += 2)
       warp_wait<kCl>(&bars.full[i % NU], (i / NU) & 1, abort, status, kSiteQmProducer);
-  } else if (warp == kMmaWarp && !issuer) {
-    // ---------------- C = 2, odd CTA: forward each landed unit to the issuer ----------------
-    for (int i = 0; i < n_units; ++i) {
-      if (!warp_wait<kCl>(&bars.full[i % NU], (i / NU) & 1, abort, status, kSiteQmMma)) break;
-      if (lane == 0) mbar_arrive_cl(mapa_u32(&bars.full[i % NU], 0));
-      __syncwarp();
-    }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp && issuer) {
     // ---------------- MMA issuer ----------------
+    // It waits on one barrier per step and never on a copy: the compute warps
+    // of both CTAs wait for the units that the MMAs issued after their next
+    // hand-back will read (each on its own CTA's copy barrier: its half of
+    // the unit) before they arrive on it (qdo_ready, s_free). A satisfied
+    // mbarrier wait costs the issuing warp ~100-150 cycles, and this warp,
+    // not the tensor core, paced the dQ pass; the compute warps wait while
+    // they would otherwise idle.
     constexpr uint32_t id_s1 = idesc_tf32(128 * C, Cfg::BK1, false, false);   // pass 1 S, dP: N = BK1
     constexpr uint32_t id_s2 = idesc_tf32(128 * C, Cfg::BK2, false, false);   // pass 2 S, dP: N = BK2
     constexpr uint32_t id_q = idesc_tf32(128 * C, D, false, false);           // dQ: N = d
     const uint64_t desc0 = sdesc(smem_u32(smem), 16, 1024);
     auto unit_desc = [&](int i) { return desc0 + (uint64_t)(((i % NU) * Cfg::UNIT_BYTES) >> 4); };
-    // both CTAs' parts of unit i have landed
-    auto unit_wait = [&](int i) {
-      return warp_wait<kCl>(&bars.full[i % NU], (i / NU) & 1, abort, status, kSiteQmMma);
-    };
     int use0 = 0, use1 = 0;       // pass-1 uses of each TMEM stage (s_free phases)
     // wait until the previous use of stage st has been released by its warpgroup(s)
     auto stage_free = [&](int st) {
@@ -300,9 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; ok && !GD && c < nk; ++c) {
       const int st = c & 1;
       const int ust = st ? use1 : use0;   // the stage's earlier uses (its release to wait for)
-      if (!warp_wait4<kCl>(ust > 0 ? 3 : 2, &bars.full[(2 * c) % NU], ((2 * c) / NU) & 1,
-                           &bars.full[(2 * c + 1) % NU], ((2 * c + 1) / NU) & 1,
-                           &bars.s_free[st], (ust - 1) & 1, nullptr, 0u, abort, status, kSiteQmMma)) {
+      // K, V of chunk c: covered by qdo_ready (c < 2) or by chunk c-2's release of the stage
+      if (ust > 0 && !warp_wait<kCl>(&bars.s_free[st], (ust - 1) & 1, abort, status, kSiteQmMma)) {
         ok = false;
         break;
       }
@@ -334,14 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_g<C>(&bars.empty[(ik + 1) % NU]);
       }
     };
-    // K and V of sub-chunk s2's chunk, waited for at the chunk's first sub-chunk
-    auto kv_wait = [&](int s2) {
-      const int ik = p2_base + 3 * (s2 / Cfg::NSUB);
-      return s2 % Cfg::NSUB != 0 || (unit_wait(ik) && unit_wait(ik + 1));
-    };
     // prologue: sub-chunks 0 and 1, each after the last pass-1 use of its stage
+    // (whose release covers their K, V units; qdo_ready does for a stage
+    // that pass 1 did not use)
     for (int s = 0; ok && s < 2 && s < n_sub; ++s) {
-      if (!kv_wait(s) || !stage_free(s & 1)) { ok = false; break; }
+      if (!stage_free(s & 1)) { ok = false; break; }
       if (elect_one()) sdp2(s);   // issue_sdp fences after the waits
       __syncwarp();
     }
@@ -349,26 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = s & 1, j = s / Cfg::NSUB, h = s % Cfg::NSUB, s2 = s + 2;
       const int ikt = p2_base + 3 * j + 2;
       const int u = (st ? use1 : use0) + (s >> 1);      // this sub-chunk's use of stage st
-      // dS(s) handed back, K^T of s's chunk (first sub-chunk) and K, V of
-      // s2's chunk (its first sub-chunk), waited for side by side
-      {
-        const int ik2 = p2_base + 3 * (s2 / Cfg::NSUB);
-        uint64_t* w1 = nullptr; uint64_t* w2 = nullptr; uint64_t* w3 = nullptr;
-        uint32_t p1 = 0, p2 = 0, p3 = 0;
-        int nw = 1;
-        auto add = [&](int unit) {
-          uint64_t* b = &bars.full[unit % NU];
-          const uint32_t p = (unit / NU) & 1;
-          if (nw == 1) { w1 = b; p1 = p; } else if (nw == 2) { w2 = b; p2 = p; } else { w3 = b; p3 = p; }
-          ++nw;
-        };
-        if (h == 0) add(ikt);
-        if (s2 < n_sub && s2 % Cfg::NSUB == 0) { add(ik2); add(ik2 + 1); }
-        if (!warp_wait4<kCl>(nw, &bars.s_free[st], u & 1, w1, p1, w2, p2, w3, p3, abort, status,
-                             kSiteQmMma)) {
-          ok = false;
-          break;
-        }
+      // dS(s) handed back (which also covers K^T of s's chunk and K, V of s2's)
+      if (!warp_wait<kCl>(&bars.s_free[st], u & 1, abort, status, kSiteQmMma)) {
+        ok = false;
+        break;
       }
       const uint32_t a_ds = tmem + Cfg::p2_stage(st), d_q = tmem + Cfg::T_DQ;
       const uint64_t bkt = unit_desc(ikt);
@@ -406,6 +381,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid = q < S && GQA_DCHECK(status, h < H && g < sh.Hk, kChkTcQmLoad);
     const uint32_t tl = lane_base(tmem, warp);
     const long long row_off = (long long)q * H * D + (long long)h * D;
+    // This CTA's copies of units [lo, lo + cnt) (those that exist) have
+    // landed: waited for by every compute warp before the hand-back after
+    // which the MMA warp issues the MMAs that read them.
+    auto units_landed = [&](int lo, int cnt) {
+      bool okw = true;
+      for (int i = lo; okw && i < lo + cnt && i < n_units; ++i)
+        okw = warp_wait<kCl>(&bars.full[i % NU], (i / NU) & 1, abort, status, kSiteQmCompute);
+      return okw;
+    };
+    // K, V units of pass-2 sub-chunk s2's chunk
+    auto p2_kv = [&](int s2) { return p2_base + 3 * (s2 / Cfg::NSUB); };
+    bool ok = true;
     // Q (warpgroup 0) or dO (warpgroup 1) rows into TMEM, rounded to TF32:
     // the A operands of S and dP. The same rows go, unrounded, to the
     // transposed copy Q^T / dO^T that the key-major kernel reads (column
@@ -434,22 +421,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
+      // the units of the MMAs issued after qdo_ready: pass-1 chunks 0 and 1,
+      // and pass-2 sub-chunk st's K, V for a stage st that pass 1 leaves unused
+      ok = GD || units_landed(0, 2 * min(nk, 2));
+      for (int st = 0; st < 2; ++st)
+        if (ok && (GD || st >= nk) && st < n_sub) ok = units_landed(p2_kv(st), 2);
       __syncwarp();
-      if (lane == 0) arrive_issuer<C>(&bars.qdo_ready);
+      if (ok && lane == 0) arrive_issuer<C>(&bars.qdo_ready);
     }
     const float sl2 = sh.scale * kLog2e;
     const float lse2 = valid ? __ldg(LSE + (long long)q * H + h) * kLog2e : 0.f;
     const int segq = valid ? (int)__ldg(seg + q) : 0;
     float Dpart = 0.f;
-    bool ok = true;
     // Both warpgroups take every chunk / sub-chunk, warpgroup wg the columns
     // [wg*W/2, (wg+1)*W/2) of it: the softmax of a chunk then finishes in
     // half the time, which is what the MMA warp waits for before dQ.
     // ---- pass 1: D = rowsum(P dP) ----
     constexpr int H1 = Cfg::BK1 / 2, H2 = Cfg::BK2 / 2;
     static_assert(H1 == 32 && (H2 == 16 || H2 == 32), "column split");
-    for (int c = 0; !GD && c < nk; ++c) {
+    for (int c = 0; ok && !GD && c < nk; ++c) {
       const int st = c & 1;
+      // units of the MMAs issued after this chunk's release of stage st:
+      // chunk c + 2's K, V, or after the stage's last pass-1 use, those of
+      // pass-2 sub-chunk st
+      if (!(c + 2 < nk ? units_landed(2 * (c + 2), 2) : (st >= n_sub || units_landed(p2_kv(st), 2)))) {
+        ok = false;
+        break;
+      }
       if (!mbar_wait<kCl>(&bars.s_full[st], (c >> 1) & 1, abort, status, kSiteQmCompute)) { ok = false; break; }
       tc_fence_after();
       const int k0 = (kc0 + c) * Cfg::BK1 + wg * H1;          // this warpgroup's first key
@@ -489,6 +487,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- pass 2: dS = scale P (dP - D) over S, for dQ += dS K ----
     for (int s = 0; ok && s < n_sub; ++s) {
       const int st = s & 1;
+      // units of the MMAs issued after dS(s) is handed back: K^T of s's
+      // chunk (at its first sub-chunk) and K, V of sub-chunk s + 2's chunk
+      // (when s + 2 starts a chunk)
+      if (!((s % Cfg::NSUB != 0 || units_landed(p2_base + 3 * (s / Cfg::NSUB) + 2, 1)) &&
+            (s + 2 >= n_sub || (s + 2) % Cfg::NSUB != 0 || units_landed(p2_kv(s + 2), 2)))) {
+        ok = false;
+        break;
+      }
       const int u1 = GD ? 0 : (st ? nk / 2 : (nk + 1) / 2);   // pass-1 uses of this stage
       if (!mbar_wait<kCl>(&bars.s_full[st], (u1 + (s >> 1)) & 1, abort, status, kSiteQmCompute)) {
         ok = false;
@@ -601,10 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The odd CTA's MMA warp forwards each of its landed copies to the even
 // (issuing) CTA, in the order the issuer consumes them.
 // ---------------------------------------------------------------------------
-template <int D_, int C_>
+template <int D_, int C_, bool W_ = false>
 struct KmCfg {
   static constexpr int D = D_, C = C_;
-  static constexpr int NQ = (D == 128) ? 32 : 64;         // (query, head) columns per block
+  // (query, head) columns per block: 64, or 32 at d = 128 unless W (wide:
+  // SM pairs only, one TMEM stage)
+  static constexpr int NQ = (D == 128 && !W_) ? 32 : 64;
   static constexpr int NQH = NQ / C;                      // this CTA's columns of a Q / dO block
   static constexpr int DH = D / C;                        // this CTA's rows of a Q^T / dO^T block
   static constexpr int V_PANEL_BYTES = 128 * 128;         // 128 keys x 32 floats
@@ -621,7 +629,8 @@ struct KmCfg {
   // its dynamic shared memory starts 1 KB aligned and reports an error
   // otherwise); with C = 2 the halved blocks leave room for deeper staging
   // and the slack.
-  static constexpr int NSQ = (C == 1) ? 3 : 4, NST = (C == 1) ? 2 : 4;
+  static constexpr int NSQ = (C == 1) ? 3 : (NQ * D > 4096 ? 2 : 4);
+  static constexpr int NST = (C == 1) ? 2 : (NQ * D > 4096 ? 2 : 4);
   static constexpr int SLACK = (C == 1) ? 0 : 1024;
   static constexpr int OFF_V = 0, OFF_QDO = V_BYTES, OFF_T = OFF_QDO + NSQ * 2 * BLK_BYTES;
   static constexpr int off_q(int b) { return OFF_QDO + b * 2 * BLK_BYTES; }
@@ -631,11 +640,13 @@ struct KmCfg {
   static constexpr int END = OFF_T + NST * 2 * BLK_BYTES;
   static constexpr int SMEM_BYTES = (END + SLACK > 120 * 1024) ? END + SLACK : 120 * 1024;
   static_assert(SMEM_BYTES <= 224 * 1024, "shared memory budget (with the static barriers)");
-  // TMEM columns: K | dK | dV | stage 0: S^T dP^T | stage 1: S^T dP^T
+  // TMEM columns: K | dK | dV | NS stages of S^T dP^T (two where they fit;
+  // at d = 128 with 64-column blocks one: 3 x 128 + 2 x 64 = 512)
+  static constexpr int NS = (3 * D + 4 * NQ <= 512) ? 2 : 1;
   static constexpr uint32_t T_K = 0, T_DK = D, T_DV = 2 * D;
   static constexpr uint32_t t_s(int b) { return 3 * D + b * 2 * NQ; }
   static constexpr uint32_t t_dp(int b) { return 3 * D + b * 2 * NQ + NQ; }
-  static_assert(3 * D + 4 * NQ <= 512, "TMEM budget");
+  static_assert(3 * D + 2 * NS * NQ <= 512, "TMEM budget");
 };
 
 struct KmBarriers {
@@ -681,7 +692,7 @@ struct BlockWalk {
   }
 };
 
-template <int D, int C>
+template <int D, int C, bool W>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_key_major(const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapQ,
                  const __grid_constant__ CUtensorMap mapDO, const __grid_constant__ CUtensorMap mapQt,
@@ -691,10 +702,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const uint32_t* __restrict__ blk_maxseg, float* __restrict__ dK,
                  float* __restrict__ dV, uint32_t* __restrict__ status, Shape sh,
                  const RopeParams rope, int band, int n_split, float* __restrict__ parts) {
-  using Cfg = KmCfg<D, C>;
-  constexpr int NQ = Cfg::NQ;
+  using Cfg = KmCfg<D, C, W>;
+  constexpr int NQ = Cfg::NQ, NS = Cfg::NS;
   constexpr bool kCl = C > 1;
-  static_assert(Cfg::NSQ <= 4 && Cfg::NST <= 4, "barrier arrays");
+  static_assert(Cfg::NSQ <= 4 && Cfg::NST <= 4 && NS <= 2, "barrier arrays");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ KmBarriers bars;
   __shared__ float4 meta[2][2][NQ / 2];   // [warpgroup][block parity] per column: (lse*log2e, D, query, seg)
@@ -734,9 +745,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qb0 = kg0 / QB, nqb = (S + QB - 1) / QB;
 
   if (threadIdx.x == 0) {
-    // A copy barrier is armed by this CTA's producer warp; in the issuing CTA
-    // of a pair the odd CTA's forward of its half is the second arrival.
-    const uint32_t nfull = issuer ? C : 1;
+    // A copy barrier is armed by this CTA's producer warp (its half of the
+    // tile); the compute warps of each CTA wait on their own CTA's.
+    const uint32_t nfull = 1;
     mbar_init(&bars.v_full, nfull);
     mbar_init(&bars.k_ready, C * kComputeWarps);          // every compute warp of each CTA
     for (int b = 0; b < Cfg::NSQ; ++b) {
@@ -818,46 +829,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (pw == 1) warp_wait<kCl>(&bars.v_full, 0, abort, status, kSiteKmProducer);
     for (int m = max(0, n - ns); m < n; ++m)
       warp_wait<kCl>(&full[m % ns], (m / ns) & 1, abort, status, kSiteKmProducer);
-  } else if (warp == kMmaWarp && !issuer) {
-    // ---------------- C = 2, odd CTA: forward each landed copy to the issuer ----------------
-    // in the issuer's order of use: V, then Q/dO of block n before Q^T/dO^T
-    // of block n-1
-    // (this CTA's barrier landed -> an arrive on the same barrier of the issuer)
-    auto forward = [&](uint64_t* bar, uint32_t ph) {
-      if (!warp_wait<kCl>(bar, ph, abort, status, kSiteKmMma)) return false;
-      if (lane == 0) mbar_arrive_cl(mapa_u32(bar, 0));
-      __syncwarp();
-      return true;
-    };
-    bool ok = forward(&bars.v_full, 0);
-    int n = 0;
-    for (int qb = walk.next(); ok && qb >= 0; qb = walk.next()) {
-      const int bs = n % Cfg::NSQ;
-      ok = forward(&bars.qdo_full[bs], (n / Cfg::NSQ) & 1);
-      if (ok && n >= 1) {
-        const int m = n - 1;
-        ok = forward(&bars.t_full[m % Cfg::NST], (m / Cfg::NST) & 1);
-      }
-      ++n;
-    }
-    if (ok && n >= 1) {
-      const int m = n - 1;
-      forward(&bars.t_full[m % Cfg::NST], (m / Cfg::NST) & 1);
-    }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp && issuer) {
     // ---------------- MMA issuer (warp-converged, elected issue) ----------------
+    // One barrier per step and never a copy: the compute warps of both CTAs
+    // wait for the copies that the MMAs issued after their next hand-back
+    // read (each on its own CTA's barriers) before they arrive on it (k_ready,
+    // p_ready), as in the query-major kernel.
     constexpr uint32_t id_s = idesc_tf32(128 * C, NQ, false, false);
     constexpr uint32_t id_g = idesc_tf32(128 * C, D, false, false);
-    // this CTA's copy and, with C = 2, the odd CTA's have landed (one barrier)
-    auto landed = [&](uint64_t* bar, uint32_t ph) {
-      return warp_wait<kCl>(bar, ph, abort, status, kSiteKmMma);
-    };
-    bool ok = landed(&bars.v_full, 0) && warp_wait<kCl>(&bars.k_ready, 0, abort, status, kSiteKmMma);
+    // V and the Q / dO tiles of blocks 0 .. NS-1 are covered by k_ready
+    bool ok = warp_wait<kCl>(&bars.k_ready, 0, abort, status, kSiteKmMma);
     const uint64_t desc0 = sdesc(smem_u32(smem), 16, 1024);
     const uint64_t av = desc0 + (uint64_t)(Cfg::OFF_V >> 4);
-    // S^T = K Q^T of block n into TMEM stage n & 1 (TS: A = K in TMEM)
+    // S^T = K Q^T of block n into TMEM stage n % NS (TS: A = K in TMEM)
     auto s_mma = [&](int n) {
-      const uint32_t d = tmem + Cfg::t_s(n & 1);
+      const uint32_t d = tmem + Cfg::t_s(n % NS);
       const uint64_t bq = desc0 + (uint64_t)(Cfg::off_q(n % Cfg::NSQ) >> 4);
       mma_ts_g<C>(d, tmem + Cfg::T_K, bq, id_s, 0u);
 #pragma unroll
@@ -868,18 +854,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // that hand the stage to the softmax and free the Q / dO tiles
     auto dp_mma = [&](int n) {
       const int bs = n % Cfg::NSQ;
-      const uint32_t d = tmem + Cfg::t_dp(n & 1);
+      const uint32_t d = tmem + Cfg::t_dp(n % NS);
       const uint64_t bdo = desc0 + (uint64_t)(Cfg::off_do(bs) >> 4);
       mma_ss_g<C>(d, av, bdo, id_s, 0u);
 #pragma unroll
       for (int ks = 1; ks < D / 8; ++ks)
         mma_ss_acc_g<C>(d, av + desc_off(ks, Cfg::V_PANEL_BYTES), bdo + desc_off(ks, Cfg::BLK_PANEL_BYTES), id_s);
-      mma_commit_g<C>(&bars.s_full[n & 1]);
+      mma_commit_g<C>(&bars.s_full[n % NS]);
       mma_commit_g<C>(&bars.qdo_empty[bs]);
     };
     // dV += P^T dO of block m (A = P^T over S^T in TMEM, B = its dO^T tile)
     auto dv_mma = [&](int m) {
-      const uint32_t a_p = tmem + Cfg::t_s(m & 1);
+      const uint32_t a_p = tmem + Cfg::t_s(m % NS);
       const uint64_t bdot = desc0 + (uint64_t)(Cfg::off_dot(m % Cfg::NST) >> 4);
       mma_ts_g<C>(tmem + Cfg::T_DV, a_p, bdot, id_g, m > 0 ? 1u : 0u);
 #pragma unroll
@@ -889,7 +875,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dK += dS^T Q of block m (A = dS^T over dP^T), then free its Q^T / dO^T tiles
     auto dk_mma = [&](int m) {
       const int bt = m % Cfg::NST;
-      const uint32_t a_ds = tmem + Cfg::t_dp(m & 1);
+      const uint32_t a_ds = tmem + Cfg::t_dp(m % NS);
       const uint64_t bqt = desc0 + (uint64_t)(Cfg::off_qt(bt) >> 4);
       mma_ts_g<C>(tmem + Cfg::T_DK, a_ds, bqt, id_g, m > 0 ? 1u : 0u);
 #pragma unroll
@@ -908,16 +894,87 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return n < fetched;
     };
-    // S^T / dP^T of blocks 0 and 1, then per block m one burst: dV(m),
-    // S^T(m+2), dK(m), dP^T(m+2). Block m + 2 uses block m's TMEM stage; MMAs
-    // run in issue order, so S^T(m+2) overwrites P^T only after dV(m) and
-    // dP^T(m+2) overwrites dS^T only after dK(m) have been issued. The slow
-    // shared-memory-A dP^T MMAs come last in the burst, keeping the tensor
-    // core's queue long while the issuing warp waits for the next block (this
-    // order ran the whole backward ~8% faster than dV, dK, then S^T / dP^T
-    // alternating by K step). One wait on the softmax and one burst per block.
-    for (int n = 0; ok && n < 2 && exists(n); ++n) {
-      if (!landed(&bars.qdo_full[n % Cfg::NSQ], (n / Cfg::NSQ) & 1)) { ok = false; break; }
+    // S^T / dP^T of blocks 0 .. NS-1, then per block m one burst: dV(m),
+    // S^T(m+NS), dK(m), dP^T(m+NS). Block m + NS uses block m's TMEM stage;
+    // MMAs run in issue order, so S^T(m+NS) overwrites P^T only after dV(m)
+    // and dP^T(m+NS) overwrites dS^T only after dK(m) have been issued. The
+    // slow shared-memory-A dP^T MMAs come last in the burst, keeping the
+    // tensor core's queue long while the issuing warp waits for the next
+    // block (this order ran the whole backward ~8% faster than dV, dK, then
+    // S^T / dP^T alternating by K step). One wait on the softmax and one
+    // burst per block. With one stage (64-column blocks at d = 128) the
+    // tensor core idles while a block's softmax runs, but each dP^T MMA reads
+    // its shared-memory A operand (V, 4 KB per K step) for 64 columns instead
+    // of 32.
+    if constexpr (NS == 1) {
+      // One TMEM stage of 64 columns, handed over in two halves of 32: half
+      // hf of a block is S^T columns [32hf, 32hf+32), made by an N = 32 MMA
+      // whose B rows come half from each CTA (rows 16hf.. of each CTA's Q
+      // tile): block columns 16hf + [0,16) and 32 + 16hf + [0,16). dP^T stays
+      // one N = 64 MMA (block column c in dP^T column c), so V, its
+      // shared-memory A operand, is read once per 64 columns. Per block m:
+      // wait half A's softmax, issue dV_A(m), dK_A(m), S^T_A(m+1); wait half
+      // B's, issue dV_B(m), dK_B(m), S^T_B(m+1), dP^T(m+1). The tensor core
+      // runs half A's products and the next S^T_A while half B's softmax runs.
+      constexpr uint32_t id_h = idesc_tf32(128 * C, NQ / 2, false, false);
+      constexpr int HR = Cfg::NQH / 2;                       // rows of each CTA's Q tile per half
+      auto s_half = [&](int n, int hf) {
+        const uint32_t d = tmem + Cfg::t_s(0) + 32 * hf;
+        const uint64_t bq = desc0 + (uint64_t)(Cfg::off_q(n % Cfg::NSQ) >> 4) + (uint64_t)((hf * HR * 128) >> 4);
+        mma_ts_g<C>(d, tmem + Cfg::T_K, bq, id_h, 0u);
+#pragma unroll
+        for (int ks = 1; ks < D / 8; ++ks)
+          mma_ts_acc_g<C>(d, tmem + Cfg::T_K + 8 * ks, bq + desc_off(ks, Cfg::BLK_PANEL_BYTES), id_h);
+      };
+      // dV += P^T dO and dK += dS^T Q over half hf's K steps: block columns
+      // 8kk.. with (kk % 4) / 2 == hf; P^T of those columns sits in S^T
+      // column 32 hf + 16 (kk / 4) + 8 (kk % 2), dS^T in dP^T column 8 kk
+      auto grads_half = [&](int m, int hf) {
+        const uint64_t bdot = desc0 + (uint64_t)(Cfg::off_dot(m % Cfg::NST) >> 4);
+        const uint64_t bqt = desc0 + (uint64_t)(Cfg::off_qt(m % Cfg::NST) >> 4);
+#pragma unroll
+        for (int i = 0; i < NQ / 16; ++i) {
+          const int kk = 4 * (i / 2) + 2 * hf + (i % 2);
+          const uint32_t acc = (m > 0 || hf > 0 || i > 0) ? 1u : 0u;
+          mma_ts_g<C>(tmem + Cfg::T_DV, tmem + Cfg::t_s(0) + 32 * hf + 16 * (kk / 4) + 8 * (kk % 2),
+                      bdot + desc_off(kk, Cfg::T_PANEL_BYTES), id_g, acc);
+        }
+#pragma unroll
+        for (int i = 0; i < NQ / 16; ++i) {
+          const int kk = 4 * (i / 2) + 2 * hf + (i % 2);
+          const uint32_t acc = (m > 0 || hf > 0 || i > 0) ? 1u : 0u;
+          mma_ts_g<C>(tmem + Cfg::T_DK, tmem + Cfg::t_dp(0) + 8 * kk,
+                      bqt + desc_off(kk, Cfg::T_PANEL_BYTES), id_g, acc);
+        }
+      };
+      if (ok && exists(0) && elect_one()) {
+        tc_fence_after();
+        s_half(0, 0);
+        s_half(0, 1);
+        dp_mma(0);
+      }
+      __syncwarp();
+      for (int m = 0; ok && exists(m); ++m) {
+        const bool more = exists(m + 1);
+        for (int hf = 0; hf < 2; ++hf) {
+          // half hf's softmax (half A's hand-over also covers block m's
+          // Q^T / dO^T tiles and block m+1's Q / dO tiles)
+          if (!warp_wait<kCl>(&bars.p_ready[hf], m & 1, abort, status, kSiteKmMma)) {
+            ok = false;
+            break;
+          }
+          if (elect_one()) {
+            tc_fence_after();
+            grads_half(m, hf);
+            if (hf == 1) mma_commit_g<C>(&bars.t_empty[m % Cfg::NST]);
+            if (more) s_half(m + 1, hf);
+            if (more && hf == 1) dp_mma(m + 1);
+          }
+          __syncwarp();
+        }
+      }
+    } else {
+    for (int n = 0; ok && n < NS && exists(n); ++n) {
       if (elect_one()) {
         tc_fence_after();
         s_mma(n);
@@ -926,13 +983,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
     for (int m = 0; ok && exists(m); ++m) {
-      const int n2 = m + 2;
+      const int n2 = m + NS;
       const bool more = exists(n2);
-      // block m's softmax, its Q^T / dO^T tiles and block m+2's Q / dO tiles, side by side
-      if (!warp_wait4<kCl>(more ? 3 : 2, &bars.p_ready[m & 1], (m >> 1) & 1,
-                           &bars.t_full[m % Cfg::NST], (m / Cfg::NST) & 1,
-                           &bars.qdo_full[n2 % Cfg::NSQ], (n2 / Cfg::NSQ) & 1, nullptr, 0u,
-                           abort, status, kSiteKmMma)) {
+      // block m's softmax (which also covers its Q^T / dO^T tiles and block
+      // m+NS's Q / dO tiles)
+      if (!warp_wait<kCl>(&bars.p_ready[m % NS], (m / NS) & 1, abort, status, kSiteKmMma)) {
         ok = false;
         break;
       }
@@ -945,12 +1000,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
+    }   // NS == 2
     if (elect_one()) mma_commit_g<C>(&bars.acc_done);   // also drains every MMA issued above
     __syncwarp();
     // no MMA of the group may still run when the CTAs leave
     warp_wait<kCl>(&bars.acc_done, 0, abort, status, kSiteKmMma);
-  } else {
+  } else if (warp >= kFirstCompute) {
     // ---------------- compute: thread = key (TMEM lane) ----------------
+    // (the odd CTA's MMA warp has no role and skips to the end)
     const int wg = (warp - kFirstCompute) >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int key = k0 + r;
@@ -973,9 +1030,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive_issuer<C>(&bars.k_ready);
     }
+    // Copies the MMA warp reads after this warp's next hand-back, waited for
+    // on this CTA's barriers: V and the Q / dO tiles of blocks 0 .. NS-1
+    // before k_ready; per block n, its Q^T / dO^T tiles and block n+NS's
+    // Q / dO tiles before p_ready(n). `ahead` walks NS blocks in front.
+    BlockWalk ahead(blk_minseg, (unsigned)k_hi, pb0, pb1);
+    int n_ahead = 0;                       // blocks the lookahead has found
+    bool ok = warp_wait<kCl>(&bars.v_full, 0, abort, status, kSiteKmCompute);
+    for (; ok && n_ahead < NS && ahead.next() >= 0; ++n_ahead)
+      ok = warp_wait<kCl>(&bars.qdo_full[n_ahead % Cfg::NSQ], (n_ahead / Cfg::NSQ) & 1, abort, status,
+                          kSiteKmCompute);
+    __syncwarp();
+    if (ok && lane == 0) arrive_issuer<C>(&bars.k_ready);
     // Both warpgroups take every block, warpgroup wg the columns
     // [wg*NQ/2, (wg+1)*NQ/2) of it: the softmax of a block then finishes in
     // half the time, which is what the MMA warp waits for before dV / dK.
@@ -983,68 +1050,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int HQ = NQ / 2;
     static_assert(HQ == 16 || HQ == 32, "column split");
     int n = 0;
-    bool ok = true;
-    for (int qb = walk.next(); qb >= 0; qb = walk.next()) {
-      const int b = n & 1;
+    for (int qb = walk.next(); ok && qb >= 0; qb = walk.next()) {
+      const int b = n & 1;            // metadata buffer
+      const int st = n % NS;          // TMEM stage
       const unsigned maxseg = __ldg(blk_maxseg + qb);   // loaded ahead of the waits below
-      // this warpgroup's columns' metadata (double-buffered; one named barrier per block)
+      // this warpgroup's columns' metadata (double-buffered; one named barrier
+      // per block): (lse log2 e, scale D, query, seg)
       if (wt < HQ) {
         const int col = wg * HQ + wt;
         const int q = qb * QB + col / G, h = g * G + col % G;
         float4 m = make_float4(0.f, 0.f, __int_as_float(-1), __int_as_float(0x7fffffff));
         if (q < S && GQA_DCHECK(status, h < H, kChkTcKmLoad))
-          m = make_float4(__ldg(LSE + (long long)q * H + h) * kLog2e, Dws[(long long)q * H + h],
+          m = make_float4(__ldg(LSE + (long long)q * H + h) * kLog2e, sh.scale * Dws[(long long)q * H + h],
                           __int_as_float(q), __int_as_float((int)__ldg(seg + q)));
         meta[wg][b][wt] = m;
       }
       asm volatile("bar.sync %0, 128;" ::"r"(1 + wg) : "memory");
+      // the copies read by the MMAs issued after this block's hand-back
+      // (blocks 0 .. n_ahead-1 are known to exist)
+      if (n_ahead == n + NS && ahead.next() >= 0) ++n_ahead;
+      const bool more = n_ahead > n + NS;
+      if (!warp_wait<kCl>(&bars.t_full[n % Cfg::NST], (n / Cfg::NST) & 1, abort, status, kSiteKmCompute) ||
+          (more &&
+           !warp_wait<kCl>(&bars.qdo_full[(n + NS) % Cfg::NSQ], ((n + NS) / Cfg::NSQ) & 1, abort, status,
+                           kSiteKmCompute))) {
+        ok = false;
+        break;
+      }
       // warp-uniform: every lane leaves the loop together (walk.next() is warp-collective)
-      if (!warp_wait<kCl>(&bars.s_full[b], (n >> 1) & 1, abort, status, kSiteKmCompute)) { ok = false; break; }
+      if (!warp_wait<kCl>(&bars.s_full[st], (n / NS) & 1, abort, status, kSiteKmCompute)) { ok = false; break; }
       tc_fence_after();
       // every (key, column) of the block visible: key <= first query and >= every seg
       const int q_first = qb * QB;
       const bool full = key <= q_first && key >= (int)maxseg && q_first + QB - 1 < S;
-      const float4* mt = meta[wg][b];
-      const uint32_t ts = tl + Cfg::t_s(b) + wg * HQ, tdp = tl + Cfg::t_dp(b) + wg * HQ;
-      float sv[HQ], dp[HQ];
-      if constexpr (HQ == 16) {
-        tmem_ld16(ts, sv);
-        tmem_ld16(tdp, dp);
-      } else {
-        tmem_ld32(ts, sv);
-        tmem_ld32(tdp, dp);
-      }
-      tmem_ld_wait();
-      if (full) {
+      // P^T = 2^(s log2e scale - lse log2e) and dS^T = P (scale dP - scale D),
+      // both rounded to TF32, over NC columns: S^T at TMEM column ts, dP^T at
+      // tdp, the columns' metadata at mt
+      auto softmax_cols = [&](auto nc, uint32_t ts, uint32_t tdp, const float4* mt) {
+        constexpr int NC = decltype(nc)::value;
+        float sv[NC], dp[NC];
+        if constexpr (NC == 16) {
+          tmem_ld16(ts, sv);
+          tmem_ld16(tdp, dp);
+        } else {
+          tmem_ld32(ts, sv);
+          tmem_ld32(tdp, dp);
+        }
+        tmem_ld_wait();
+        if (full) {
 #pragma unroll
-        for (int j = 0; j < HQ; ++j) {
-          const float4 m = mt[j];
-          const float pj = ex2(fmaf(sv[j], sl2, -m.x));
-          sv[j] = to_tf32(pj);
-          dp[j] = to_tf32(sh.scale * pj * (dp[j] - m.y));
+          for (int j = 0; j < NC; ++j) {
+            const float4 m = mt[j];
+            const float pj = ex2(fmaf(sv[j], sl2, -m.x));
+            sv[j] = to_tf32(pj);
+            dp[j] = to_tf32(pj * fmaf(dp[j], sh.scale, -m.y));
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < NC; ++j) {
+            const float4 m = mt[j];
+            const int q = __float_as_int(m.z), sq = __float_as_int(m.w);
+            const bool vis = key <= q && key >= sq;        // q = -1 for padding columns
+            const float pj = vis ? ex2(fmaf(sv[j], sl2, -m.x)) : 0.f;
+            sv[j] = to_tf32(pj);
+            dp[j] = to_tf32(pj * fmaf(dp[j], sh.scale, -m.y));
+          }
+        }
+        if constexpr (NC == 16) {
+          tmem_st16(ts, sv);
+          tmem_st16(tdp, dp);
+        } else {
+          tmem_st32(ts, sv);
+          tmem_st32(tdp, dp);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+      };
+      if constexpr (NS == 1) {
+        // two hand-overs per block: half hf of warpgroup wg is S^T columns
+        // 32 hf + 16 wg + [0, 16) and dP^T columns 32 wg + 16 hf + [0, 16)
+        // (block columns 32 wg + 16 hf + [0, 16): metadata entries 16 hf..)
+        for (int hf = 0; hf < 2; ++hf) {
+          softmax_cols(std::integral_constant<int, 16>{}, tl + Cfg::t_s(0) + 32 * hf + 16 * wg,
+                       tl + Cfg::t_dp(0) + 32 * wg + 16 * hf, meta[wg][b] + 16 * hf);
+          __syncwarp();
+          if (lane == 0) arrive_issuer<C>(&bars.p_ready[hf]);
         }
       } else {
-#pragma unroll
-        for (int j = 0; j < HQ; ++j) {
-          const float4 m = mt[j];
-          const int q = __float_as_int(m.z), sq = __float_as_int(m.w);
-          const bool vis = key <= q && key >= sq;        // q = -1 for padding columns
-          const float pj = vis ? ex2(fmaf(sv[j], sl2, -m.x)) : 0.f;
-          sv[j] = to_tf32(pj);
-          dp[j] = to_tf32(sh.scale * pj * (dp[j] - m.y));
-        }
+        softmax_cols(std::integral_constant<int, HQ>{}, tl + Cfg::t_s(st) + wg * HQ,
+                     tl + Cfg::t_dp(st) + wg * HQ, meta[wg][b]);
+        __syncwarp();
+        if (lane == 0) arrive_issuer<C>(&bars.p_ready[st]);
       }
-      if constexpr (HQ == 16) {
-        tmem_st16(ts, sv);
-        tmem_st16(tdp, dp);
-      } else {
-        tmem_st32(ts, sv);
-        tmem_st32(tdp, dp);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive_issuer<C>(&bars.p_ready[b]);
       ++n;
     }
     // epilogue: warpgroup 0 adds dK (rotated by the RoPE backward of the key's
@@ -1314,13 +1411,13 @@ int sm_count() {
   return n;
 }
 
-template <int D, int C>
+template <int D, int C, bool W>
 gqa_status km_launch_c(const float* Q, const float* K, const float* V, const float* dO,
                        const float* LSE, const uint32_t* seg, float* dK, float* dV, const float* Qt,
                        const float* dOt, long long ld_qt, const float* Dws, const uint32_t* blk_minseg,
                        const uint32_t* blk_maxseg, uint32_t* status, const Shape& sh,
                        cudaStream_t st, const RopeParams& rope, int n_split, float* parts) {
-  using Cfg = KmCfg<D, C>;
+  using Cfg = KmCfg<D, C, W>;
   const int QB = Cfg::NQ / sh.G;
   CUtensorMap mv, mq, mdo, mqt, mdot;
   gqa_status r;
@@ -1330,7 +1427,7 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
   if ((r = map_heads(&mdo, dO, D, sh.H, sh.S, sh.G, QB / C)) != GQA_OK) return r;
   if ((r = map_panels(&mqt, Qt, ld_qt, (long long)sh.Hk * D, ld_qt / 32, Cfg::DH, Cfg::T_PANELS)) != GQA_OK) return r;
   if ((r = map_panels(&mdot, dOt, ld_qt, (long long)sh.Hk * D, ld_qt / 32, Cfg::DH, Cfg::T_PANELS)) != GQA_OK) return r;
-  if (cudaFuncSetAttribute(tc_key_major<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tc_key_major<D, C, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess)
     return check_launch("key-major smem attribute");
   const int n_tiles = (sh.S + 127) / 128;
@@ -1340,7 +1437,7 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
   const bool few_waves = (long long)n_tg * C * sh.Hk < 4LL * sm_count();
   const int band = few_waves ? sh.Hk : (sh.Hk % 2 == 0 ? 2 : 1);
   const dim3 grid(C * band, (sh.Hk / band) * n_tg * n_split);
-  r = launch_clustered(tc_key_major<D, C>, grid, C, Cfg::SMEM_BYTES, st,
+  r = launch_clustered(tc_key_major<D, C, W>, grid, C, Cfg::SMEM_BYTES, st,
                                   "tensor-core key-major", mv, mq, mdo, mqt, mdot, K, LSE, Dws, seg,
                                   blk_minseg, blk_maxseg, dK, dV, status, sh, rope, band, n_split,
                                   parts);
@@ -1371,11 +1468,31 @@ int cta_group() {
   return c;
 }
 
+// Key-major block width at d = 128 on SM pairs: 64 (query, head) columns
+// with one TMEM stage (the default), or 32 with two (GQA_KM_NARROW=1). Read
+// once per process.
+bool km_wide() {
+  static bool w = [] {
+    const char* e = getenv("GQA_KM_NARROW");
+    return !(e != nullptr && atoi(e) == 1);
+  }();
+  return w;
+}
+
 // The key-major kernel runs on SM pairs when the pair's half block holds
 // whole queries (G divides NQ/2), else on one SM per key tile.
 int km_cta_group(const Shape& sh) {
-  const int nqh = (sh.d == 128) ? KmCfg<128, 2>::NQH : KmCfg<64, 2>::NQH;
+  const int nqh = (sh.d == 128) ? (km_wide() ? KmCfg<128, 2, true>::NQH : KmCfg<128, 2>::NQH)
+                                : KmCfg<64, 2>::NQH;
   return (cta_group() == 2 && nqh % sh.G == 0) ? 2 : 1;
+}
+
+// (query, head) columns per key-major block of the configuration that runs
+// this shape (the per-block seg minima are formed for blocks of NQ / G queries).
+int km_nq(const Shape& sh) {
+  if (sh.d != 128) return KmCfg<64, 1>::NQ;
+  if (km_cta_group(sh) == 2 && km_wide()) return KmCfg<128, 2, true>::NQ;
+  return KmCfg<128, 1>::NQ;
 }
 
 // Parts the key-major kernel splits each tile (pair)'s query walk into: 1
@@ -1407,11 +1524,17 @@ gqa_status km_launch(const float* Q, const float* K, const float* V, const float
                      const uint32_t* blk_maxseg, uint32_t* status, const Shape& sh,
                      cudaStream_t st, const RopeParams& rope, float* parts) {
   const int n_split = km_split(sh);
-  if (km_cta_group(sh) == 2)
-    return km_launch_c<D, 2>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, ld_qt, Dws, blk_minseg,
-                             blk_maxseg, status, sh, st, rope, n_split, parts);
-  return km_launch_c<D, 1>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, ld_qt, Dws, blk_minseg,
-                           blk_maxseg, status, sh, st, rope, n_split, parts);
+  if (km_cta_group(sh) == 2) {
+    if constexpr (D == 128) {
+      if (km_wide())
+        return km_launch_c<D, 2, true>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, ld_qt, Dws, blk_minseg,
+                                       blk_maxseg, status, sh, st, rope, n_split, parts);
+    }
+    return km_launch_c<D, 2, false>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, ld_qt, Dws, blk_minseg,
+                                    blk_maxseg, status, sh, st, rope, n_split, parts);
+  }
+  return km_launch_c<D, 1, false>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, ld_qt, Dws, blk_minseg,
+                                  blk_maxseg, status, sh, st, rope, n_split, parts);
 }
 
 template <int D, int C, bool GD>
@@ -1519,7 +1642,7 @@ gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* d
   uint32_t* blk = reinterpret_cast<uint32_t*>(ws + T.blk_off);
   uint32_t* blk_max = reinterpret_cast<uint32_t*>(ws + T.blkmax_off);
   float* parts = reinterpret_cast<float*>(ws + T.part_off);
-  const int QB = ((sh.d == 128) ? KmCfg<128, 1>::NQ : KmCfg<64, 1>::NQ) / sh.G;
+  const int QB = km_nq(sh) / sh.G;
   gqa_status r;
   if ((r = tile_minseg(seg, sh.S, QB, blk, st, blk_max)) != GQA_OK) return r;
   // K^T for the query-major kernel; Q^T and dO^T are written by the
