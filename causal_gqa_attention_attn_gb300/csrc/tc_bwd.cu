@@ -1049,36 +1049,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = sh.scale * kLog2e;
     constexpr int HQ = NQ / 2;
     static_assert(HQ == 16 || HQ == 32, "column split");
-    int n = 0;
-    for (int qb = walk.next(); ok && qb >= 0; qb = walk.next()) {
-      const int b = n & 1;            // metadata buffer
-      const int st = n % NS;          // TMEM stage
-      const unsigned maxseg = __ldg(blk_maxseg + qb);   // loaded ahead of the waits below
-      // this warpgroup's columns' metadata (double-buffered; one named barrier
-      // per block): (lse log2 e, scale D, query, seg)
-      if (wt < HQ) {
+    // metadata of block qb's columns into buffer bb (one thread per column
+    // of this warpgroup): (lse log2 e, scale D, query, seg)
+    auto load_meta = [&](int qb, int bb) {
+      if (qb >= 0 && wt < HQ) {
         const int col = wg * HQ + wt;
         const int q = qb * QB + col / G, h = g * G + col % G;
         float4 m = make_float4(0.f, 0.f, __int_as_float(-1), __int_as_float(0x7fffffff));
         if (q < S && GQA_DCHECK(status, h < H, kChkTcKmLoad))
           m = make_float4(__ldg(LSE + (long long)q * H + h) * kLog2e, sh.scale * Dws[(long long)q * H + h],
                           __int_as_float(q), __int_as_float((int)__ldg(seg + q)));
-        meta[wg][b][wt] = m;
+        meta[wg][bb][wt] = m;
       }
+    };
+    // Every warp runs one iteration per visible block (the walk is the same
+    // for all), so the warpgroup's named barrier is reached the same number
+    // of times by its four warps even after a bounded wait gave up: a failed
+    // wait clears ok and the remaining iterations skip their work. The next
+    // block's metadata is fetched at the end of each iteration, into the
+    // buffer block n-1 used (double-buffered, one named barrier per block).
+    int n = 0;
+    int qb = walk.next();
+    load_meta(qb, 0);
+    while (qb >= 0) {
+      const int b = n & 1;            // metadata buffer
+      const int st = n % NS;          // TMEM stage
+      // block n's metadata is written, and every warp of the warpgroup is
+      // done with block n-1's (whose buffer the next fetch reuses)
       asm volatile("bar.sync %0, 128;" ::"r"(1 + wg) : "memory");
+      const unsigned maxseg = __ldg(blk_maxseg + qb);
       // the copies read by the MMAs issued after this block's hand-back
       // (blocks 0 .. n_ahead-1 are known to exist)
       if (n_ahead == n + NS && ahead.next() >= 0) ++n_ahead;
       const bool more = n_ahead > n + NS;
-      if (!warp_wait<kCl>(&bars.t_full[n % Cfg::NST], (n / Cfg::NST) & 1, abort, status, kSiteKmCompute) ||
-          (more &&
-           !warp_wait<kCl>(&bars.qdo_full[(n + NS) % Cfg::NSQ], ((n + NS) / Cfg::NSQ) & 1, abort, status,
-                           kSiteKmCompute))) {
-        ok = false;
-        break;
-      }
-      // warp-uniform: every lane leaves the loop together (walk.next() is warp-collective)
-      if (!warp_wait<kCl>(&bars.s_full[st], (n / NS) & 1, abort, status, kSiteKmCompute)) { ok = false; break; }
+      if (ok)
+        ok = warp_wait<kCl>(&bars.t_full[n % Cfg::NST], (n / Cfg::NST) & 1, abort, status, kSiteKmCompute) &&
+             (!more || warp_wait<kCl>(&bars.qdo_full[(n + NS) % Cfg::NSQ], ((n + NS) / Cfg::NSQ) & 1, abort,
+                                      status, kSiteKmCompute));
+      if (ok) ok = warp_wait<kCl>(&bars.s_full[st], (n / NS) & 1, abort, status, kSiteKmCompute);
+      if (ok) {
       tc_fence_after();
       // every (key, column) of the block visible: key <= first query and >= every seg
       const int q_first = qb * QB;
@@ -1142,6 +1151,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) arrive_issuer<C>(&bars.p_ready[st]);
       }
+      }
+      qb = walk.next();
+      load_meta(qb, b ^ 1);
       ++n;
     }
     // epilogue: warpgroup 0 adds dK (rotated by the RoPE backward of the key's
