@@ -588,8 +588,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   dV  += P^T . dO       A = P^T (TMEM),  B = dO^T block (smem, K-major copy)
 //   dK  += dS^T . Q       A = dS^T (TMEM), B = Q^T block  (smem, K-major copy)
 // Blocks alternate between two TMEM stages, so block n's softmax runs while
-// the tensor core does S^T / dP^T of block n+1 and dV / dK of block n-1; both
-// compute warpgroups take every block, half its columns each. Q / dO blocks
+// the tensor core does S^T / dP^T of block n+1 and dV / dK of block n-1 (at
+// d = 128 on SM pairs, one stage of four slots cycled by halves of a block:
+// below); both compute warpgroups take every block, half its columns each. Q / dO blocks
 // and Q^T / dO^T blocks stream through their own shared-memory stages (a
 // block's copies take thousands of cycles to land while the tensor core is
 // busy). Blocks are visited from the end of the sequence down to the tile's
@@ -604,8 +605,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // as the A operand of dP^T, are what limits the one-SM kernel: its
 // shared-memory traffic per block is about twice what the tensor core needs
 // of it per flop. The pair walks the union of the two tiles' query blocks.
-// The odd CTA's MMA warp forwards each of its landed copies to the even
-// (issuing) CTA, in the order the issuer consumes them.
 // ---------------------------------------------------------------------------
 template <int D_, int C_, bool W_ = false>
 struct KmCfg {
@@ -647,6 +646,25 @@ struct KmCfg {
   static constexpr uint32_t t_s(int b) { return 3 * D + b * 2 * NQ; }
   static constexpr uint32_t t_dp(int b) { return 3 * D + b * 2 * NQ + NQ; }
   static_assert(3 * D + 2 * NS * NQ <= 512, "TMEM budget");
+  // W: the stage is four slots of 32 columns. A block has two halves of 32
+  // columns, E = block columns [0, 32) and O = [32, 64) (h = 0, 1), each with
+  // an S^T slot and a dP^T slot; the dP^T slots of a block are adjacent (E
+  // below O: one N = 64 MMA). Block parity p:
+  //   p = 0: S_E 0, dP_E 1, dP_O 2, S_O 3; half E is handed back first
+  //   p = 1: dP_E 0, dP_O 1, S_O 2, S_E 3; half O is handed back first
+  // The first half's two slots are adjacent and take the next block's dP^T;
+  // the second half's take the next block's S^T halves.
+  static constexpr int w_first(int p) { return p; }
+  static constexpr int w_s_slot(int p, int h) { return p == 0 ? 3 * h : 3 - h; }
+  static constexpr int w_dp_slot(int p, int h) { return 1 - p + h; }
+  static constexpr uint32_t t_slot(int sl) { return 3 * D + 32 * sl; }
+  // W: each CTA's Q tile is two sub-tiles of 16 rows, sub-tile h = block
+  // columns 32 h + 16 rank + [0, 16), so that S^T of half h (an N = 32 MMA
+  // taking 16 B rows from each CTA) holds block column 32 h + c in column c
+  static constexpr int QSUB_BYTES = BLK_BYTES / 2;
+  static constexpr int QSUB_PANEL_BYTES = BLK_PANEL_BYTES / 2;
+  static_assert(!W_ || (NS == 1 && NQ == 64 && C == 2 && QSUB_PANEL_BYTES % 1024 == 0),
+                "slot cycling: one stage of 64-column blocks on SM pairs");
 };
 
 struct KmBarriers {
@@ -814,7 +832,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&full[b], 2 * Cfg::BLK_BYTES);
         if (pw == 0) {   // 4-D boxes (32 dims, G heads, QB/C queries, d/32 panels)
           const int qh = q0 + (int)rank * (QB / C);
-          tma_load_4d(smem + Cfg::off_q(b), &mapQ, 0, g * G, qh, 0, &full[b]);
+          if constexpr (W) {
+            // Q as two sub-tiles of 16 (query, head) rows: boxes of (32 dims,
+            // min(G, 16) heads, 16 / min(G, 16) queries, d/32 panels)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int c0 = 32 * h + 16 * (int)rank;
+              tma_load_4d(smem + Cfg::off_q(b) + h * Cfg::QSUB_BYTES, &mapQ, 0, g * G + c0 % G,
+                          q0 + c0 / G, 0, &full[b]);
+            }
+          } else {
+            tma_load_4d(smem + Cfg::off_q(b), &mapQ, 0, g * G, qh, 0, &full[b]);
+          }
           tma_load_4d(smem + Cfg::off_do(b), &mapDO, 0, g * G, qh, 0, &full[b]);
         } else {         // d/C rows x NQ (query, head) columns, in 32-column panels
           const int row = g * D + (int)rank * Cfg::DH;
@@ -907,71 +936,102 @@ __global__ void __launch_bounds__(kThreads, 1)
     // its shared-memory A operand (V, 4 KB per K step) for 64 columns instead
     // of 32.
     if constexpr (NS == 1) {
-      // One TMEM stage of 64 columns, handed over in two halves of 32: half
-      // hf of a block is S^T columns [32hf, 32hf+32), made by an N = 32 MMA
-      // whose B rows come half from each CTA (rows 16hf.. of each CTA's Q
-      // tile): block columns 16hf + [0,16) and 32 + 16hf + [0,16). dP^T stays
-      // one N = 64 MMA (block column c in dP^T column c), so V, its
-      // shared-memory A operand, is read once per 64 columns. Per block m:
-      // wait half A's softmax, issue dV_A(m), dK_A(m), S^T_A(m+1); wait half
-      // B's, issue dV_B(m), dK_B(m), S^T_B(m+1), dP^T(m+1). The tensor core
-      // runs half A's products and the next S^T_A while half B's softmax runs.
+      // One TMEM stage of four 32-column slots (KmCfg: w_s_slot, w_dp_slot),
+      // handed over by halves. Per block m, with f its first half and l the
+      // other: wait half f's softmax, issue dV_f(m), dK_f(m) and, into the
+      // two slots those free, dP^T(m+1) (one N = 64 MMA: V, its shared-memory
+      // A operand, is read once per 64 columns); wait half l's, issue dK_l(m),
+      // S^T of block m+1's first half (into the slot dK_l freed), dV_l(m),
+      // then S^T of m+1's second half (into the slot dV_l freed). The next
+      // block's softmax can start as soon as its first S^T half lands, and
+      // the tensor core still holds dV_l(m) and the second S^T half then.
       constexpr uint32_t id_h = idesc_tf32(128 * C, NQ / 2, false, false);
-      constexpr int HR = Cfg::NQH / 2;                       // rows of each CTA's Q tile per half
-      auto s_half = [&](int n, int hf) {
-        const uint32_t d = tmem + Cfg::t_s(0) + 32 * hf;
-        const uint64_t bq = desc0 + (uint64_t)(Cfg::off_q(n % Cfg::NSQ) >> 4) + (uint64_t)((hf * HR * 128) >> 4);
+      // S^T of half h of block n (TS: A = K; B = sub-tile h of the Q tile)
+      auto s_half = [&](int n, int h) {
+        const uint32_t d = tmem + Cfg::t_slot(Cfg::w_s_slot(n & 1, h));
+        const uint64_t bq = desc0 + (uint64_t)((Cfg::off_q(n % Cfg::NSQ) + h * Cfg::QSUB_BYTES) >> 4);
         mma_ts_g<C>(d, tmem + Cfg::T_K, bq, id_h, 0u);
 #pragma unroll
         for (int ks = 1; ks < D / 8; ++ks)
-          mma_ts_acc_g<C>(d, tmem + Cfg::T_K + 8 * ks, bq + desc_off(ks, Cfg::BLK_PANEL_BYTES), id_h);
+          mma_ts_acc_g<C>(d, tmem + Cfg::T_K + 8 * ks, bq + desc_off(ks, Cfg::QSUB_PANEL_BYTES), id_h);
       };
-      // dV += P^T dO and dK += dS^T Q over half hf's K steps: block columns
-      // 8kk.. with (kk % 4) / 2 == hf; P^T of those columns sits in S^T
-      // column 32 hf + 16 (kk / 4) + 8 (kk % 2), dS^T in dP^T column 8 kk
-      auto grads_half = [&](int m, int hf) {
+      // dP^T of block n into its two adjacent dP^T slots (SS: A = V)
+      auto dp_pair = [&](int n) {
+        const uint32_t d = tmem + Cfg::t_slot(Cfg::w_dp_slot(n & 1, 0));
+        const uint64_t bdo = desc0 + (uint64_t)(Cfg::off_do(n % Cfg::NSQ) >> 4);
+        mma_ss_g<C>(d, av, bdo, id_s, 0u);
+#pragma unroll
+        for (int ks = 1; ks < D / 8; ++ks)
+          mma_ss_acc_g<C>(d, av + desc_off(ks, Cfg::V_PANEL_BYTES), bdo + desc_off(ks, Cfg::BLK_PANEL_BYTES), id_s);
+      };
+      // dV += P^T dO and dK += dS^T Q over half h of block m: K steps 4h + i
+      // (block columns 32 h + 8 i ..), P^T at column 8 i of the half's S^T
+      // slot, dS^T at column 8 i of its dP^T slot. Block 0 is even, so its
+      // half E issues the first (overwriting) MMA of each accumulator.
+      auto dv_half = [&](int m, int h) {
         const uint64_t bdot = desc0 + (uint64_t)(Cfg::off_dot(m % Cfg::NST) >> 4);
-        const uint64_t bqt = desc0 + (uint64_t)(Cfg::off_qt(m % Cfg::NST) >> 4);
+        const uint32_t a = tmem + Cfg::t_slot(Cfg::w_s_slot(m & 1, h));
 #pragma unroll
-        for (int i = 0; i < NQ / 16; ++i) {
-          const int kk = 4 * (i / 2) + 2 * hf + (i % 2);
-          const uint32_t acc = (m > 0 || hf > 0 || i > 0) ? 1u : 0u;
-          mma_ts_g<C>(tmem + Cfg::T_DV, tmem + Cfg::t_s(0) + 32 * hf + 16 * (kk / 4) + 8 * (kk % 2),
-                      bdot + desc_off(kk, Cfg::T_PANEL_BYTES), id_g, acc);
-        }
-#pragma unroll
-        for (int i = 0; i < NQ / 16; ++i) {
-          const int kk = 4 * (i / 2) + 2 * hf + (i % 2);
-          const uint32_t acc = (m > 0 || hf > 0 || i > 0) ? 1u : 0u;
-          mma_ts_g<C>(tmem + Cfg::T_DK, tmem + Cfg::t_dp(0) + 8 * kk,
-                      bqt + desc_off(kk, Cfg::T_PANEL_BYTES), id_g, acc);
-        }
+        for (int i = 0; i < 4; ++i)
+          mma_ts_g<C>(tmem + Cfg::T_DV, a + 8 * i, bdot + desc_off(4 * h + i, Cfg::T_PANEL_BYTES), id_g,
+                      (m > 0 || h > 0 || i > 0) ? 1u : 0u);
       };
+      auto dk_half = [&](int m, int h) {
+        const uint64_t bqt = desc0 + (uint64_t)(Cfg::off_qt(m % Cfg::NST) >> 4);
+        const uint32_t a = tmem + Cfg::t_slot(Cfg::w_dp_slot(m & 1, h));
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          mma_ts_g<C>(tmem + Cfg::T_DK, a + 8 * i, bqt + desc_off(4 * h + i, Cfg::T_PANEL_BYTES), id_g,
+                      (m > 0 || h > 0 || i > 0) ? 1u : 0u);
+      };
+      // block 0: dP^T, then its S^T halves in hand-over order (E first), each
+      // followed by the commit its softmax waits for
       if (ok && exists(0) && elect_one()) {
         tc_fence_after();
-        s_half(0, 0);
-        s_half(0, 1);
-        dp_mma(0);
+        dp_pair(0);
+        s_half(0, Cfg::w_first(0));
+        mma_commit_g<C>(&bars.s_full[0]);
+        s_half(0, Cfg::w_first(0) ^ 1);
+        mma_commit_g<C>(&bars.s_full[1]);
+        mma_commit_g<C>(&bars.qdo_empty[0]);
       }
       __syncwarp();
       for (int m = 0; ok && exists(m); ++m) {
         const bool more = exists(m + 1);
-        for (int hf = 0; hf < 2; ++hf) {
-          // half hf's softmax (half A's hand-over also covers block m's
-          // Q^T / dO^T tiles and block m+1's Q / dO tiles)
-          if (!warp_wait<kCl>(&bars.p_ready[hf], m & 1, abort, status, kSiteKmMma)) {
-            ok = false;
-            break;
-          }
-          if (elect_one()) {
-            tc_fence_after();
-            grads_half(m, hf);
-            if (hf == 1) mma_commit_g<C>(&bars.t_empty[m % Cfg::NST]);
-            if (more) s_half(m + 1, hf);
-            if (more && hf == 1) dp_mma(m + 1);
-          }
-          __syncwarp();
+        const int hf = Cfg::w_first(m & 1), hl = hf ^ 1;   // block m+1 hands hl back first
+        // the first half's hand-over also covers block m's Q^T / dO^T tiles
+        // and block m+1's Q / dO tiles
+        if (!warp_wait<kCl>(&bars.p_ready[0], m & 1, abort, status, kSiteKmMma)) {
+          ok = false;
+          break;
         }
+        if (elect_one()) {
+          tc_fence_after();
+          dv_half(m, hf);
+          dk_half(m, hf);
+          if (more) dp_pair(m + 1);
+        }
+        __syncwarp();
+        if (!warp_wait<kCl>(&bars.p_ready[1], m & 1, abort, status, kSiteKmMma)) {
+          ok = false;
+          break;
+        }
+        if (elect_one()) {
+          tc_fence_after();
+          dk_half(m, hl);
+          if (more) {
+            s_half(m + 1, hl);
+            mma_commit_g<C>(&bars.s_full[0]);
+          }
+          dv_half(m, hl);
+          mma_commit_g<C>(&bars.t_empty[m % Cfg::NST]);
+          if (more) {
+            s_half(m + 1, hf);
+            mma_commit_g<C>(&bars.s_full[1]);
+            mma_commit_g<C>(&bars.qdo_empty[(m + 1) % Cfg::NSQ]);
+          }
+        }
+        __syncwarp();
       }
     } else {
     for (int n = 0; ok && n < NS && exists(n); ++n) {
@@ -1050,10 +1110,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int HQ = NQ / 2;
     static_assert(HQ == 16 || HQ == 32, "column split");
     // metadata of block qb's columns into buffer bb (one thread per column
-    // of this warpgroup): (lse log2 e, scale D, query, seg)
+    // of this warpgroup): (lse log2 e, scale D, query, seg). With one stage
+    // (W) warpgroup wg takes columns 16 wg + [0, 16) of each half: entry
+    // 16 h + j is block column 32 h + 16 wg + j; else entry j is column
+    // HQ wg + j.
     auto load_meta = [&](int qb, int bb) {
       if (qb >= 0 && wt < HQ) {
-        const int col = wg * HQ + wt;
+        const int col = (NS == 1) ? 32 * (wt >> 4) + 16 * wg + (wt & 15) : wg * HQ + wt;
         const int q = qb * QB + col / G, h = g * G + col % G;
         float4 m = make_float4(0.f, 0.f, __int_as_float(-1), __int_as_float(0x7fffffff));
         if (q < S && GQA_DCHECK(status, h < H, kChkTcKmLoad))
@@ -1136,14 +1199,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
       };
       if constexpr (NS == 1) {
-        // two hand-overs per block: half hf of warpgroup wg is S^T columns
-        // 32 hf + 16 wg + [0, 16) and dP^T columns 32 wg + 16 hf + [0, 16)
-        // (block columns 32 wg + 16 hf + [0, 16): metadata entries 16 hf..)
-        for (int hf = 0; hf < 2; ++hf) {
-          softmax_cols(std::integral_constant<int, 16>{}, tl + Cfg::t_s(0) + 32 * hf + 16 * wg,
-                       tl + Cfg::t_dp(0) + 32 * wg + 16 * hf, meta[wg][b] + 16 * hf);
+        // two hand-overs per block, in the order of KmCfg::w_first: half h of
+        // warpgroup wg is columns 16 wg + [0, 16) of the half's S^T and dP^T
+        // slots (block columns 32 h + 16 wg + [0, 16): metadata entries 16 h..).
+        // The first half's S^T slot is ready with s_full[0] (which also
+        // covers the block's dP^T), the second's with s_full[1].
+        const int p = n & 1;
+        for (int i = 0; i < 2; ++i) {
+          const int h = Cfg::w_first(p) ^ i;
+          if (i == 1) {
+            if (!warp_wait<kCl>(&bars.s_full[1], (n / NS) & 1, abort, status, kSiteKmCompute)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          softmax_cols(std::integral_constant<int, 16>{}, tl + Cfg::t_slot(Cfg::w_s_slot(p, h)) + 16 * wg,
+                       tl + Cfg::t_slot(Cfg::w_dp_slot(p, h)) + 16 * wg, meta[wg][b] + 16 * h);
           __syncwarp();
-          if (lane == 0) arrive_issuer<C>(&bars.p_ready[hf]);
+          if (lane == 0) arrive_issuer<C>(&bars.p_ready[i]);
         }
       } else {
         softmax_cols(std::integral_constant<int, HQ>{}, tl + Cfg::t_s(st) + wg * HQ,
@@ -1435,7 +1509,9 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
   gqa_status r;
   const long long kv_panels = (long long)sh.Hk * D / 32;
   if ((r = map_panels(&mv, V, (long long)sh.Hk * D, sh.S, kv_panels, 128, D / 32)) != GQA_OK) return r;
-  if ((r = map_heads(&mq, Q, D, sh.H, sh.S, sh.G, QB / C)) != GQA_OK) return r;
+  // W: Q in sub-tiles of 16 (query, head) rows (G divides 32 on SM pairs)
+  const int qbh = W ? (sh.G < 16 ? sh.G : 16) : sh.G;
+  if ((r = map_heads(&mq, Q, D, sh.H, sh.S, qbh, W ? 16 / qbh : QB / C)) != GQA_OK) return r;
   if ((r = map_heads(&mdo, dO, D, sh.H, sh.S, sh.G, QB / C)) != GQA_OK) return r;
   if ((r = map_panels(&mqt, Qt, ld_qt, (long long)sh.Hk * D, ld_qt / 32, Cfg::DH, Cfg::T_PANELS)) != GQA_OK) return r;
   if ((r = map_panels(&mdot, dOt, ld_qt, (long long)sh.Hk * D, ld_qt / 32, Cfg::DH, Cfg::T_PANELS)) != GQA_OK) return r;
