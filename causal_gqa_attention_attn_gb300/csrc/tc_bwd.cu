@@ -726,7 +726,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(Cfg::NSQ <= 4 && Cfg::NST <= 4 && NS <= 2, "barrier arrays");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ KmBarriers bars;
-  __shared__ float4 meta[2][2][NQ / 2];   // [warpgroup][block parity] per column: (lse*log2e, D, query, seg)
+  __shared__ float4 meta[2][2][NQ / 2];   // [warpgroup][block parity] per column: (lse*log2e, scale*D, query, seg)
+  __shared__ unsigned meta_max[2][2];     // [warpgroup][block parity]: the block's max seg
+  __shared__ uint32_t meta_raw[2][2][4][NQ / 2];   // [warpgroup][block parity] copies: lse, D, seg; max seg
   unsigned char* smem = smem_raw;
   if constexpr (C == 1) {
     if ((smem_u32(smem) & 1023u) != 0) {  // the layout has no alignment slack
@@ -1114,40 +1116,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (W) warpgroup wg takes columns 16 wg + [0, 16) of each half: entry
     // 16 h + j is block column 32 h + 16 wg + j; else entry j is column
     // HQ wg + j.
-    auto load_meta = [&](int qb, int bb) {
+    // The metadata of block n+1 is copied with cp.async right after block
+    // n's named barrier (issue_meta, into its raw slot) and scaled into its
+    // buffer when block n ends (finish_meta): no ordinary load is outstanding
+    // when the named barrier or an mbarrier acquire runs, and both would wait
+    // for it. Only the copying thread reads its raw slots.
+    auto meta_col = [&](int qb, int& q, int& h) {
+      const int col = (NS == 1) ? 32 * (wt >> 4) + 16 * wg + (wt & 15) : wg * HQ + wt;
+      q = qb * QB + col / G;
+      h = g * G + col % G;
+    };
+    auto issue_meta = [&](int qb, int sl) {
       if (qb >= 0 && wt < HQ) {
-        const int col = (NS == 1) ? 32 * (wt >> 4) + 16 * wg + (wt & 15) : wg * HQ + wt;
-        const int q = qb * QB + col / G, h = g * G + col % G;
+        int q, h;
+        meta_col(qb, q, h);
+        if (q < S && GQA_DCHECK(status, h < H, kChkTcKmLoad)) {
+          cp_async4(&meta_raw[wg][sl][0][wt], LSE + (long long)q * H + h);
+          cp_async4(&meta_raw[wg][sl][1][wt], Dws + (long long)q * H + h);
+          cp_async4(&meta_raw[wg][sl][2][wt], seg + q);
+        }
+        if (wt == 0) cp_async4(&meta_raw[wg][sl][3][0], blk_maxseg + qb);
+      }
+      cp_async_commit();
+    };
+    auto finish_meta = [&](int qb, int sl, int bb) {
+      cp_async_wait_all_groups();
+      if (qb >= 0 && wt < HQ) {
+        int q, h;
+        meta_col(qb, q, h);
         float4 m = make_float4(0.f, 0.f, __int_as_float(-1), __int_as_float(0x7fffffff));
         if (q < S && GQA_DCHECK(status, h < H, kChkTcKmLoad))
-          m = make_float4(__ldg(LSE + (long long)q * H + h) * kLog2e, sh.scale * Dws[(long long)q * H + h],
-                          __int_as_float(q), __int_as_float((int)__ldg(seg + q)));
+          m = make_float4(__uint_as_float(meta_raw[wg][sl][0][wt]) * kLog2e,
+                          sh.scale * __uint_as_float(meta_raw[wg][sl][1][wt]), __int_as_float(q),
+                          __uint_as_float(meta_raw[wg][sl][2][wt]));
         meta[wg][bb][wt] = m;
+        if (wt == 0) meta_max[wg][bb] = meta_raw[wg][sl][3][0];
       }
     };
     // Every warp runs one iteration per visible block (the walk is the same
     // for all), so the warpgroup's named barrier is reached the same number
     // of times by its four warps even after a bounded wait gave up: a failed
     // wait clears ok and the remaining iterations skip their work. The next
-    // block's metadata is fetched at the end of each iteration, into the
+    // block's metadata is stored at the end of each iteration, into the
     // buffer block n-1 used (double-buffered, one named barrier per block).
+    // Block j's raw slot and buffer are j & 1.
     int n = 0;
     int qb = walk.next();
-    load_meta(qb, 0);
+    issue_meta(qb, 0);
+    finish_meta(qb, 0, 0);
+    int qb_next = walk.next();            // after the last block: -1 on every call
     while (qb >= 0) {
       const int b = n & 1;            // metadata buffer
       const int st = n % NS;          // TMEM stage
       // block n's metadata is written, and every warp of the warpgroup is
       // done with block n-1's (whose buffer the next fetch reuses)
       asm volatile("bar.sync %0, 128;" ::"r"(1 + wg) : "memory");
-      const unsigned maxseg = __ldg(blk_maxseg + qb);
+      const unsigned maxseg = meta_max[wg][b];
+      issue_meta(qb_next, b ^ 1);         // block n+1, finished at the end of this iteration
       // the copies read by the MMAs issued after this block's hand-back
       // (blocks 0 .. n_ahead-1 are known to exist)
       if (n_ahead == n + NS && ahead.next() >= 0) ++n_ahead;
       const bool more = n_ahead > n + NS;
       if (ok)
-        ok = warp_wait<kCl>(&bars.t_full[n % Cfg::NST], (n / Cfg::NST) & 1, abort, status, kSiteKmCompute) &&
-             (!more || warp_wait<kCl>(&bars.qdo_full[(n + NS) % Cfg::NSQ], ((n + NS) / Cfg::NSQ) & 1, abort,
+        ok = warp_wait(&bars.t_full[n % Cfg::NST], (n / Cfg::NST) & 1, abort, status, kSiteKmCompute) &&
+             (!more || warp_wait(&bars.qdo_full[(n + NS) % Cfg::NSQ], ((n + NS) / Cfg::NSQ) & 1, abort,
                                       status, kSiteKmCompute));
       if (ok) ok = warp_wait<kCl>(&bars.s_full[st], (n / NS) & 1, abort, status, kSiteKmCompute);
       if (ok) {
@@ -1226,10 +1258,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) arrive_issuer<C>(&bars.p_ready[st]);
       }
       }
-      qb = walk.next();
-      load_meta(qb, b ^ 1);
+      finish_meta(qb_next, b ^ 1, b ^ 1);
+      qb = qb_next;
+      qb_next = walk.next();
       ++n;
     }
+    cp_async_wait_all_groups();           // nothing in flight into shared memory past the loop
     // epilogue: warpgroup 0 adds dK (rotated by the RoPE backward of the key's
     // position when rope.on), warpgroup 1 adds dV (owned rows, NaN-guarded).
     // With n_split > 1 each part stores its partial sums instead (zeros when

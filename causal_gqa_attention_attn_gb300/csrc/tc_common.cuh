@@ -135,6 +135,16 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// 4-byte asynchronous copy global -> shared (cp.async). Its completion is
+// tracked only by cp.async.wait_group in the issuing thread: a bar.sync or an
+// mbarrier acquire that follows does not wait for it, whereas either waits for
+// the thread's outstanding ordinary loads.
+__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all_groups() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // TMA tile loads (no multicast)
 // ---------------------------------------------------------------------------
