@@ -49,7 +49,9 @@ inline WsLayout ws_layout(int S, int H) {
 // (128 or 64)/G queries.
 struct TcWsLayout {
   long long ld_kt, ld_qt;
-  size_t kt_off, qt_off, dot_off, blk_off, blkmax_off, part_off;
+  long long rows_kp;   // rows of K' (S rounded up to 64; 0 when there is no K')
+  long long ld_meta;   // key-major column records per kv head (S*G rounded up to 64)
+  size_t kt_off, qt_off, dot_off, blk_off, blkmax_off, kp_off, meta_off, part_off;
   size_t total;
 };
 TcWsLayout tc_ws_layout(int S, int H, int Hk, int d);
@@ -131,8 +133,11 @@ gqa_status simt_bwd(const float* Q, const float* K, const float* V, const float*
                     const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
                     const Shape& sh, char* ws, cudaStream_t st, const RopeParams& rope);
 
+// Per tile of `tile` queries: min seg into out[t] and, with out_max, max seg
+// into out_max[t * max_stride] (max_stride 4: a 16-byte record per tile,
+// its other three words zero).
 gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cudaStream_t st,
-                       uint32_t* out_max = nullptr);
+                       uint32_t* out_max = nullptr, int max_stride = 1);
 
 // Tensor-core backward, tc_bwd.cu: true if this shape has a tensor-core path.
 bool tc_supported(const Shape& sh);

@@ -114,6 +114,23 @@ struct QmCfg {
   static __device__ __forceinline__ int key_of(int h, int n) {
     return (n / HALF2) * HALF1 + h * HALF2 + (n % HALF2);
   }
+  // CYC (d = 128 on SM pairs): pass 2 goes by chunk, in the four 32-column
+  // slots of the pass-1 stage-0 columns, cycled by halves of a chunk as in
+  // the key-major kernel (slot functions below). Half h = keys 32 h + [0, 32)
+  // of the chunk: S of a half by its own N = 32 MMA, dP of the chunk by one
+  // N = 64 MMA into two adjacent slots (half 0 below half 1). For S of half
+  // h to hold key 32 h + c in column c, the K chunk is read from K' (a copy
+  // of K whose rows are permuted within each 64-key chunk): rows 16 h + i of
+  // CTA r's unit are keys 32 h + 16 r + i. Pass 1's N = 64 S then holds key
+  // c in column c for c in [0, 16) and [48, 64), key c + 16 for [16, 32) and
+  // key c - 16 for [32, 48); V (and so dP) stays in key order.
+  static constexpr bool CYC = (D == 128 && C == 2);
+  static constexpr uint32_t t_slot(int sl) { return T_ST + 32 * sl; }
+  static constexpr int c_first(int p) { return p; }
+  static constexpr int c_s_slot(int p, int h) { return p == 0 ? 3 * h : 3 - h; }
+  static constexpr int c_dp_slot(int p, int h) { return 1 - p + h; }
+  static_assert(!CYC || (BK1 == 64 && HALF1 == 32 && T_ST + 128 <= 512 && P1_IN_DQ),
+                "chunk-level pass 2: 64-key chunks, four slots in the pass-1 stage-0 columns");
 };
 
 struct QmBarriers {
@@ -144,8 +161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const float* __restrict__ Q, const float* __restrict__ dO,
                    const float* __restrict__ LSE, const uint32_t* __restrict__ seg,
                    float* __restrict__ dQ, float* __restrict__ Dws, float* __restrict__ Qt,
-                   float* __restrict__ dOt, long long ld_qt, uint32_t* __restrict__ status,
-                   Shape sh, const RopeParams rope, int slab_major) {
+                   float* __restrict__ dOt, long long ld_qt, float4* __restrict__ kmeta,
+                   long long ld_meta, uint32_t* __restrict__ status, Shape sh,
+                   const RopeParams rope, int slab_major) {
   using Cfg = QmCfg<D, C>;
   constexpr int NU = Cfg::NUNIT;
   constexpr bool kCl = C > 1;
@@ -309,6 +327,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (st) ++use1; else ++use0;
     }
+    if constexpr (Cfg::CYC) {
+    // ---- pass 2 by chunk j (QmCfg::CYC): per chunk, with f = its first half
+    // and l the other: wait f's dS, issue dQ_f(j) and, into the two slots
+    // that frees (dQ_f reads f's S slot; its dP slot is free once the
+    // softmax read it), dP(j+1); wait l's dS, issue S of (j+1)'s first half
+    // into l's dP slot, dQ_l(j), then S of (j+1)'s second half into l's S
+    // slot. MMAs run in issue order, so no slot is rewritten before the MMA
+    // that reads it.
+    constexpr uint32_t id_h = idesc_tf32(128 * C, 32, false, false);
+    // S of half h of chunk j (B = rows 16h.. of each CTA's K' unit)
+    auto s_half = [&](int j, int h) {
+      const uint32_t d = tmem + Cfg::t_slot(Cfg::c_s_slot(j & 1, h));
+      const uint64_t bk = unit_desc(p2_base + 3 * j) + (uint64_t)((h * 16 * 128) >> 4);
+      mma_ts_g<C>(d, tmem + Cfg::T_Q, bk, id_h, 0u);
+#pragma unroll
+      for (int ks = 1; ks < D / 8; ++ks)
+        mma_ts_acc_g<C>(d, tmem + Cfg::T_Q + 8 * ks, bk + desc_off(ks, Cfg::KV_PANEL_BYTES), id_h);
+    };
+    // dP of chunk j into its two dP slots (N = 64)
+    auto dp_pair = [&](int j) {
+      const uint32_t d = tmem + Cfg::t_slot(Cfg::c_dp_slot(j & 1, 0));
+      const uint64_t bv = unit_desc(p2_base + 3 * j + 1);
+      mma_ts_g<C>(d, tmem + Cfg::T_DO, bv, id_s1, 0u);
+#pragma unroll
+      for (int ks = 1; ks < D / 8; ++ks)
+        mma_ts_acc_g<C>(d, tmem + Cfg::T_DO + 8 * ks, bv + desc_off(ks, Cfg::KV_PANEL_BYTES), id_s1);
+    };
+    // dQ += dS_h K_h: K steps 4h + i (keys 32 h + 8 i ..), dS at column 8 i
+    // of the half's S slot, B = the K^T unit (panel h). Chunk 0 is even, so
+    // its half 0 issues the first (overwriting) MMA.
+    auto dq_half = [&](int j, int h) {
+      const uint32_t a = tmem + Cfg::t_slot(Cfg::c_s_slot(j & 1, h));
+      const uint64_t bkt = unit_desc(p2_base + 3 * j + 2);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        mma_ts_g<C>(tmem + Cfg::T_DQ, a + 8 * i, bkt + desc_off(4 * h + i, Cfg::KT_PANEL_BYTES), id_q,
+                    (j > 0 || h > 0 || i > 0) ? 1u : 0u);
+    };
+    // prologue: the slots lie in pass-1 stage 0's columns and dQ in stage
+    // 1's, so both are released first (their releases cover chunk 0's K', V)
+    if (ok) ok = stage_free(0) && stage_free(1);
+    if (ok && elect_one()) {
+      tc_fence_after();
+      dp_pair(0);
+      s_half(0, Cfg::c_first(0));
+      mma_commit_g<C>(&bars.s_full[0]);
+      s_half(0, Cfg::c_first(0) ^ 1);
+      mma_commit_g<C>(&bars.s_full[1]);
+      mma_commit_g<C>(&bars.empty[p2_base % NU]);
+      mma_commit_g<C>(&bars.empty[(p2_base + 1) % NU]);
+    }
+    __syncwarp();
+    for (int j = 0; ok && j < nk; ++j) {
+      const bool more = j + 1 < nk;
+      const int hf = Cfg::c_first(j & 1), hl = hf ^ 1;   // chunk j+1 hands hl back first
+      const int ik = p2_base + 3 * j;
+      // first half back (which also covers K^T of chunk j and K', V of j+1)
+      if (!warp_wait<kCl>(&bars.s_free[0], (use0 + j) & 1, abort, status, kSiteQmMma)) {
+        ok = false;
+        break;
+      }
+      if (elect_one()) {
+        tc_fence_after();
+        dq_half(j, hf);
+        if (more) dp_pair(j + 1);
+      }
+      __syncwarp();
+      if (!warp_wait<kCl>(&bars.s_free[1], (use1 + j) & 1, abort, status, kSiteQmMma)) {
+        ok = false;
+        break;
+      }
+      if (elect_one()) {
+        tc_fence_after();
+        if (more) {
+          s_half(j + 1, hl);
+          mma_commit_g<C>(&bars.s_full[0]);
+        }
+        dq_half(j, hl);
+        mma_commit_g<C>(&bars.empty[(ik + 2) % NU]);
+        if (more) {
+          s_half(j + 1, hf);
+          mma_commit_g<C>(&bars.s_full[1]);
+          mma_commit_g<C>(&bars.empty[(ik + 3) % NU]);
+          mma_commit_g<C>(&bars.empty[(ik + 4) % NU]);
+        }
+      }
+      __syncwarp();
+    }
+    } else {
     // ---- pass 2: sub-chunk s (chunk s / NSUB, part s % NSUB) in stage s & 1 ----
     // dQ(s) and S / dP of sub-chunk s + 2 (the same stage: MMAs run in issue
     // order, so the stage is rewritten only after dQ(s) has read dS(s)) go out
@@ -362,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     }
+    }   // CYC
     if (elect_one()) mma_commit_g<C>(&bars.dq_done);   // also drains every MMA issued above
     __syncwarp();
     // no MMA of the group may still run when the CTAs leave
@@ -390,8 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         okw = warp_wait<kCl>(&bars.full[i % NU], (i / NU) & 1, abort, status, kSiteQmCompute);
       return okw;
     };
-    // K, V units of pass-2 sub-chunk s2's chunk
-    auto p2_kv = [&](int s2) { return p2_base + 3 * (s2 / Cfg::NSUB); };
+    // K, V units of pass-2 sub-chunk s2's chunk (CYC: of chunk s2)
+    auto p2_kv = [&](int s2) { return p2_base + 3 * (Cfg::CYC ? s2 : s2 / Cfg::NSUB); };
     bool ok = true;
     // Q (warpgroup 0) or dO (warpgroup 1) rows into TMEM, rounded to TF32:
     // the A operands of S and dP. The same rows go, unrounded, to the
@@ -422,10 +530,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       // the units of the MMAs issued after qdo_ready: pass-1 chunks 0 and 1,
-      // and pass-2 sub-chunk st's K, V for a stage st that pass 1 leaves unused
+      // and pass-2 sub-chunk st's K, V for a stage st that pass 1 leaves
+      // unused (CYC: pass-2 chunk 0 is issued after both stages' last pass-1
+      // releases, or right away when pass 1 is skipped)
       ok = GD || units_landed(0, 2 * min(nk, 2));
-      for (int st = 0; st < 2; ++st)
-        if (ok && (GD || st >= nk) && st < n_sub) ok = units_landed(p2_kv(st), 2);
+      if constexpr (Cfg::CYC) {
+        if (ok && GD) ok = units_landed(p2_kv(0), 2);
+      } else {
+        for (int st = 0; st < 2; ++st)
+          if (ok && (GD || st >= nk) && st < n_sub) ok = units_landed(p2_kv(st), 2);
+      }
       __syncwarp();
       if (ok && lane == 0) arrive_issuer<C>(&bars.qdo_ready);
     }
@@ -444,7 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // units of the MMAs issued after this chunk's release of stage st:
       // chunk c + 2's K, V, or after the stage's last pass-1 use, those of
       // pass-2 sub-chunk st
-      if (!(c + 2 < nk ? units_landed(2 * (c + 2), 2) : (st >= n_sub || units_landed(p2_kv(st), 2)))) {
+      if (!(c + 2 < nk ? units_landed(2 * (c + 2), 2)
+                       : (Cfg::CYC ? units_landed(p2_kv(0), 2) : (st >= n_sub || units_landed(p2_kv(st), 2))))) {
         ok = false;
         break;
       }
@@ -455,7 +570,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool full = valid && k0 >= segq && k0 + H1 - 1 <= q;
       const uint32_t ts = tl + Cfg::p1_stage(st) + wg * H1;
       float sv[32], dp[32];
-      tmem_ld32(ts, sv);
+      if constexpr (Cfg::CYC) {
+        // keys 32 wg + [0, 32) of the chunk: S columns 16 wg + [0, 16) and
+        // 32 + 16 wg + [0, 16) (K' order), dP columns 32 wg + [0, 32)
+        const uint32_t s0 = tl + Cfg::p1_stage(st) + 16 * wg;
+        tmem_ld16(s0, sv);
+        tmem_ld16(s0 + 32, sv + 16);
+      } else {
+        tmem_ld32(ts, sv);
+      }
       tmem_ld32(ts + Cfg::BK1, dp);
       tmem_ld_wait();
       if (full) {
@@ -484,6 +607,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("bar.sync 2, 256;" ::: "memory");
       Drow = bars.dx[0][r] + bars.dx[1][r];
     }
+    // the key-major kernel's record of this row's column (the column of
+    // Q^T / dO^T; padding rows get a record that masks the column out)
+    if (wg == 0) {
+      const long long col = (long long)q0 * G + r;
+      if (col < ld_meta && GQA_DCHECK(status, g < sh.Hk && col >= 0, kChkTcQmStore))
+        kmeta[(long long)g * ld_meta + col] =
+            valid ? make_float4(lse2, sh.scale * Drow, __int_as_float(q), __int_as_float(segq))
+                  : make_float4(0.f, 0.f, __int_as_float(-1), __int_as_float(0x7fffffff));
+    }
+    // ---- pass 2: dS = scale P (dP - D) over S, for dQ += dS K ----
+    if constexpr (Cfg::CYC) {
+      // by chunk j, its halves in hand-over order (QmCfg: c_first): half h of
+      // warpgroup wg is columns 16 wg + [0, 16) of the half's S and dP slots,
+      // keys 32 h + 16 wg + [0, 16) of the chunk. The first half's S (and the
+      // chunk's dP) is ready with s_full[0], the second's with s_full[1].
+      for (int j = 0; ok && j < nk; ++j) {
+        // units of the MMAs issued after this chunk's hand-backs: K^T of
+        // chunk j, and K', V of chunk j + 1
+        if (!(units_landed(p2_base + 3 * j + 2, 1) && (j + 1 >= nk || units_landed(p2_kv(j + 1), 2)))) {
+          ok = false;
+          break;
+        }
+        const int p = j & 1, kc = (kc0 + j) * Cfg::BK1;
+        for (int i = 0; i < 2; ++i) {
+          const int hh = Cfg::c_first(p) ^ i;
+          const int u1 = GD ? 0 : (i == 0 ? (nk + 1) / 2 : nk / 2);   // pass-1 uses of s_full[i]
+          if (!mbar_wait<kCl>(&bars.s_full[i], (u1 + j) & 1, abort, status, kSiteQmCompute)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int k0 = kc + 32 * hh + 16 * wg;
+          const bool full = valid && k0 >= segq && k0 + 15 <= q;
+          const uint32_t ts = tl + Cfg::t_slot(Cfg::c_s_slot(p, hh)) + 16 * wg;
+          float sv[16], dp[16];
+          tmem_ld16(ts, sv);
+          tmem_ld16(tl + Cfg::t_slot(Cfg::c_dp_slot(p, hh)) + 16 * wg, dp);
+          tmem_ld_wait();
+          if (full) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              sv[jj] = to_tf32(sh.scale * ex2(fmaf(sv[jj], sl2, -lse2)) * (dp[jj] - Drow));
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int key = k0 + jj;
+              const bool vis = valid && key >= segq && key <= q;
+              const float pj = vis ? ex2(fmaf(sv[jj], sl2, -lse2)) : 0.f;
+              sv[jj] = to_tf32(sh.scale * pj * (dp[jj] - Drow));
+            }
+          }
+          tmem_st16(ts, sv);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) arrive_issuer<C>(&bars.s_free[i]);
+        }
+      }
+    } else {
     // ---- pass 2: dS = scale P (dP - D) over S, for dQ += dS K ----
     for (int s = 0; ok && s < n_sub; ++s) {
       const int st = s & 1;
@@ -536,6 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) arrive_issuer<C>(&bars.s_free[st]);
     }
+    }   // CYC
     // epilogue: dQ += accumulated tile (warpgroup wg: half wg of the columns),
     // NaN-guarded and, with rope.on, rotated by the RoPE backward of row q;
     // D to the workspace
@@ -636,9 +819,17 @@ struct KmCfg {
   static constexpr int off_do(int b) { return OFF_QDO + b * 2 * BLK_BYTES + BLK_BYTES; }
   static constexpr int off_qt(int b) { return OFF_T + b * 2 * BLK_BYTES; }
   static constexpr int off_dot(int b) { return OFF_T + b * 2 * BLK_BYTES + BLK_BYTES; }
-  static constexpr int END = OFF_T + NST * 2 * BLK_BYTES;
+  // per Q^T / dO^T stage: the block's column records (NQ x 16 bytes: lse
+  // log2 e, scale D, query, seg) and its 16-byte max-seg record, copied with
+  // the stage's tiles
+  static constexpr int META_BYTES = NQ * 16;
+  static constexpr int META_STRIDE = (META_BYTES + 16 + 127) / 128 * 128;
+  static constexpr int OFF_META = OFF_T + NST * 2 * BLK_BYTES;
+  static constexpr int off_meta(int b) { return OFF_META + b * META_STRIDE; }
+  static constexpr int END = OFF_META + NST * META_STRIDE;
   static constexpr int SMEM_BYTES = (END + SLACK > 120 * 1024) ? END + SLACK : 120 * 1024;
-  static_assert(SMEM_BYTES <= 224 * 1024, "shared memory budget (with the static barriers)");
+  // 227 KB per CTA, of which the static barriers take under 1 KB
+  static_assert(SMEM_BYTES <= 226 * 1024, "shared memory budget (with the static barriers)");
   // TMEM columns: K | dK | dV | NS stages of S^T dP^T (two where they fit;
   // at d = 128 with 64-column blocks one: 3 x 128 + 2 x 64 = 512)
   static constexpr int NS = (3 * D + 4 * NQ <= 512) ? 2 : 1;
@@ -715,9 +906,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_key_major(const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapQ,
                  const __grid_constant__ CUtensorMap mapDO, const __grid_constant__ CUtensorMap mapQt,
                  const __grid_constant__ CUtensorMap mapDOt, const float* __restrict__ K,
-                 const float* __restrict__ LSE, const float* __restrict__ Dws,
-                 const uint32_t* __restrict__ seg, const uint32_t* __restrict__ blk_minseg,
-                 const uint32_t* __restrict__ blk_maxseg, float* __restrict__ dK,
+                 const float4* __restrict__ kmeta, long long ld_meta,
+                 const uint32_t* __restrict__ blk_minseg, const uint4* __restrict__ blk_maxseg,
+                 float* __restrict__ dK,
                  float* __restrict__ dV, uint32_t* __restrict__ status, Shape sh,
                  const RopeParams rope, int band, int n_split, float* __restrict__ parts) {
   using Cfg = KmCfg<D, C, W>;
@@ -726,9 +917,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(Cfg::NSQ <= 4 && Cfg::NST <= 4 && NS <= 2, "barrier arrays");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ KmBarriers bars;
-  __shared__ float4 meta[2][2][NQ / 2];   // [warpgroup][block parity] per column: (lse*log2e, scale*D, query, seg)
-  __shared__ unsigned meta_max[2][2];     // [warpgroup][block parity]: the block's max seg
-  __shared__ uint32_t meta_raw[2][2][4][NQ / 2];   // [warpgroup][block parity] copies: lse, D, seg; max seg
   unsigned char* smem = smem_raw;
   if constexpr (C == 1) {
     if ((smem_u32(smem) & 1023u) != 0) {  // the layout has no alignment slack
@@ -740,6 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~uintptr_t(1023));
   }
+  const int smem_shift = (int)(smem - smem_raw);   // 0 .. 1023
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int G = sh.G, QB = NQ / G;        // queries per block
   const int S = sh.S, H = sh.H;
@@ -831,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = qb * QB;
       if (n >= ns && !warp_wait<kCl>(&empty[b], ((n / ns) - 1) & 1, abort, status, kSiteKmProducer)) break;
       if (elect_one()) {
-        mbar_arrive_expect_tx(&full[b], 2 * Cfg::BLK_BYTES);
+        mbar_arrive_expect_tx(&full[b], 2 * Cfg::BLK_BYTES + (pw == 1 ? Cfg::META_BYTES + 16 : 0));
         if (pw == 0) {   // 4-D boxes (32 dims, G heads, QB/C queries, d/32 panels)
           const int qh = q0 + (int)rank * (QB / C);
           if constexpr (W) {
@@ -851,6 +1040,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int row = g * D + (int)rank * Cfg::DH;
           tma_load_3d(smem + Cfg::off_qt(b), &mapQt, 0, row, (q0 * G) / 32, &full[b]);
           tma_load_3d(smem + Cfg::off_dot(b), &mapDOt, 0, row, (q0 * G) / 32, &full[b]);
+          // block qb's column records start at column qb * NQ = q0 * G
+          bulk_load(smem + Cfg::off_meta(b), kmeta + (long long)g * ld_meta + (long long)qb * NQ,
+                    Cfg::META_BYTES, &full[b]);
+          bulk_load(smem + Cfg::off_meta(b) + Cfg::META_BYTES, blk_maxseg + qb, 16, &full[b]);
         }
       }
       __syncwarp();
@@ -1111,68 +1304,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = sh.scale * kLog2e;
     constexpr int HQ = NQ / 2;
     static_assert(HQ == 16 || HQ == 32, "column split");
-    // metadata of block qb's columns into buffer bb (one thread per column
-    // of this warpgroup): (lse log2 e, scale D, query, seg). With one stage
-    // (W) warpgroup wg takes columns 16 wg + [0, 16) of each half: entry
-    // 16 h + j is block column 32 h + 16 wg + j; else entry j is column
-    // HQ wg + j.
-    // The metadata of block n+1 is copied with cp.async right after block
-    // n's named barrier (issue_meta, into its raw slot) and scaled into its
-    // buffer when block n ends (finish_meta): no ordinary load is outstanding
-    // when the named barrier or an mbarrier acquire runs, and both would wait
-    // for it. Only the copying thread reads its raw slots.
-    auto meta_col = [&](int qb, int& q, int& h) {
-      const int col = (NS == 1) ? 32 * (wt >> 4) + 16 * wg + (wt & 15) : wg * HQ + wt;
-      q = qb * QB + col / G;
-      h = g * G + col % G;
-    };
-    auto issue_meta = [&](int qb, int sl) {
-      if (qb >= 0 && wt < HQ) {
-        int q, h;
-        meta_col(qb, q, h);
-        if (q < S && GQA_DCHECK(status, h < H, kChkTcKmLoad)) {
-          cp_async4(&meta_raw[wg][sl][0][wt], LSE + (long long)q * H + h);
-          cp_async4(&meta_raw[wg][sl][1][wt], Dws + (long long)q * H + h);
-          cp_async4(&meta_raw[wg][sl][2][wt], seg + q);
-        }
-        if (wt == 0) cp_async4(&meta_raw[wg][sl][3][0], blk_maxseg + qb);
-      }
-      cp_async_commit();
-    };
-    auto finish_meta = [&](int qb, int sl, int bb) {
-      cp_async_wait_all_groups();
-      if (qb >= 0 && wt < HQ) {
-        int q, h;
-        meta_col(qb, q, h);
-        float4 m = make_float4(0.f, 0.f, __int_as_float(-1), __int_as_float(0x7fffffff));
-        if (q < S && GQA_DCHECK(status, h < H, kChkTcKmLoad))
-          m = make_float4(__uint_as_float(meta_raw[wg][sl][0][wt]) * kLog2e,
-                          sh.scale * __uint_as_float(meta_raw[wg][sl][1][wt]), __int_as_float(q),
-                          __uint_as_float(meta_raw[wg][sl][2][wt]));
-        meta[wg][bb][wt] = m;
-        if (wt == 0) meta_max[wg][bb] = meta_raw[wg][sl][3][0];
-      }
-    };
-    // Every warp runs one iteration per visible block (the walk is the same
-    // for all), so the warpgroup's named barrier is reached the same number
-    // of times by its four warps even after a bounded wait gave up: a failed
-    // wait clears ok and the remaining iterations skip their work. The next
-    // block's metadata is stored at the end of each iteration, into the
-    // buffer block n-1 used (double-buffered, one named barrier per block).
-    // Block j's raw slot and buffer are j & 1.
+    // Block n's column records (lse log2 e, scale D, query, seg; written by
+    // the query-major kernel) and its max-seg record arrive with its Q^T /
+    // dO^T tiles (t_full), in that stage's shared memory, which the MMAs
+    // release only after this block's last hand-back: the loop makes no
+    // global load of its own. With one stage (W) warpgroup wg takes columns
+    // 16 wg + [0, 16) of each half (records 32 h + 16 wg ..), else columns
+    // HQ wg + [0, HQ).
+    // A failed bounded wait clears ok, and the remaining iterations skip
+    // their work.
     int n = 0;
-    int qb = walk.next();
-    issue_meta(qb, 0);
-    finish_meta(qb, 0, 0);
-    int qb_next = walk.next();            // after the last block: -1 on every call
-    while (qb >= 0) {
-      const int b = n & 1;            // metadata buffer
+    for (int qb = walk.next(); qb >= 0; qb = walk.next(), ++n) {
       const int st = n % NS;          // TMEM stage
-      // block n's metadata is written, and every warp of the warpgroup is
-      // done with block n-1's (whose buffer the next fetch reuses)
-      asm volatile("bar.sync %0, 128;" ::"r"(1 + wg) : "memory");
-      const unsigned maxseg = meta_max[wg][b];
-      issue_meta(qb_next, b ^ 1);         // block n+1, finished at the end of this iteration
       // the copies read by the MMAs issued after this block's hand-back
       // (blocks 0 .. n_ahead-1 are known to exist)
       if (n_ahead == n + NS && ahead.next() >= 0) ++n_ahead;
@@ -1184,12 +1327,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = warp_wait<kCl>(&bars.s_full[st], (n / NS) & 1, abort, status, kSiteKmCompute);
       if (ok) {
       tc_fence_after();
+      // the block's records, addressed from the shared array itself (an
+      // offset, not a cast address) so that they are read as shared memory
+      const int rec_off = smem_shift + Cfg::off_meta(n % Cfg::NST);
+      const float4* rec = reinterpret_cast<const float4*>(smem_raw + rec_off);
+      const unsigned maxseg = *reinterpret_cast<const unsigned*>(smem_raw + rec_off + Cfg::META_BYTES);
       // every (key, column) of the block visible: key <= first query and >= every seg
       const int q_first = qb * QB;
       const bool full = key <= q_first && key >= (int)maxseg && q_first + QB - 1 < S;
       // P^T = 2^(s log2e scale - lse log2e) and dS^T = P (scale dP - scale D),
       // both rounded to TF32, over NC columns: S^T at TMEM column ts, dP^T at
-      // tdp, the columns' metadata at mt
+      // tdp, the columns' records at mt
       auto softmax_cols = [&](auto nc, uint32_t ts, uint32_t tdp, const float4* mt) {
         constexpr int NC = decltype(nc)::value;
         float sv[NC], dp[NC];
@@ -1247,23 +1395,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
           }
           softmax_cols(std::integral_constant<int, 16>{}, tl + Cfg::t_slot(Cfg::w_s_slot(p, h)) + 16 * wg,
-                       tl + Cfg::t_slot(Cfg::w_dp_slot(p, h)) + 16 * wg, meta[wg][b] + 16 * h);
+                       tl + Cfg::t_slot(Cfg::w_dp_slot(p, h)) + 16 * wg, rec + 32 * h + 16 * wg);
           __syncwarp();
           if (lane == 0) arrive_issuer<C>(&bars.p_ready[i]);
         }
       } else {
         softmax_cols(std::integral_constant<int, HQ>{}, tl + Cfg::t_s(st) + wg * HQ,
-                     tl + Cfg::t_dp(st) + wg * HQ, meta[wg][b]);
+                     tl + Cfg::t_dp(st) + wg * HQ, rec + wg * HQ);
         __syncwarp();
         if (lane == 0) arrive_issuer<C>(&bars.p_ready[st]);
       }
       }
-      finish_meta(qb_next, b ^ 1, b ^ 1);
-      qb = qb_next;
-      qb_next = walk.next();
-      ++n;
     }
-    cp_async_wait_all_groups();           // nothing in flight into shared memory past the loop
     // epilogue: warpgroup 0 adds dK (rotated by the RoPE backward of the key's
     // position when rope.on), warpgroup 1 adds dV (owned rows, NaN-guarded).
     // With n_split > 1 each part stores its partial sums instead (zeros when
@@ -1328,12 +1471,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 // With Gx = 1 this is K^T per kv head; with Gx = G it lays the (query, head)
 // rows of a kv group out as the contiguous K dimension of a K-major operand.
 // ld is S*Gx rounded up to 32; the grid covers all ld columns.
+// With Xp (Gx = 1 only) it also writes K' for the query-major kernel: X with
+// its rows permuted within each 64-row chunk, row 64c + 32r + 16a + i = row
+// 64c + 32a + 16r + i of X (r, a in {0, 1}, i < 16), rows rows_p (S rounded
+// up to 64) in all, those past S zero.
 // ---------------------------------------------------------------------------
-constexpr int kTrRows = 64;   // rows r of X per CTA of the transpose
+constexpr int kTrRows = 64;   // rows r of X per CTA of the transpose (one K' chunk)
 
 __global__ void __launch_bounds__(256) group_transpose(const float* __restrict__ X,
                                                        float* __restrict__ Xt, int S, int Hk,
-                                                       int Gx, int d, long long ld) {
+                                                       int Gx, int d, long long ld,
+                                                       float* __restrict__ Xp, long long rows_p) {
   __shared__ float tile[kTrRows][33];
   constexpr int PER = kTrRows / 8;                        // rows per thread (blockDim.y = 8)
   const int g = blockIdx.z, e0 = blockIdx.y * 32;
@@ -1353,6 +1501,15 @@ __global__ void __launch_bounds__(256) group_transpose(const float* __restrict__
 #pragma unroll
   for (int k = 0; k < PER; ++k) tile[threadIdx.y + 8 * k][threadIdx.x] = v[k];
   __syncthreads();
+  if (Xp != nullptr) {
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int i = threadIdx.y + 8 * k;                  // K' row in the chunk: 32r + 16a + (i % 16)
+      const int src = 32 * ((i >> 4) & 1) + 16 * (i >> 5) + (i & 15);
+      const long long rp = (long long)r0 + i;
+      if (rp < rows_p) Xp[rp * row_stride + (long long)g * d + e0 + threadIdx.x] = tile[src][threadIdx.x];
+    }
+  }
   // columns nrows .. ld-1 are padding: written as zeros (the panel view of
   // the copy reads them as ordinary elements, masked to zero weight)
 #pragma unroll
@@ -1533,9 +1690,9 @@ int sm_count() {
 
 template <int D, int C, bool W>
 gqa_status km_launch_c(const float* Q, const float* K, const float* V, const float* dO,
-                       const float* LSE, const uint32_t* seg, float* dK, float* dV, const float* Qt,
-                       const float* dOt, long long ld_qt, const float* Dws, const uint32_t* blk_minseg,
-                       const uint32_t* blk_maxseg, uint32_t* status, const Shape& sh,
+                       float* dK, float* dV, const float* Qt, const float* dOt, long long ld_qt,
+                       const float4* kmeta, long long ld_meta, const uint32_t* blk_minseg,
+                       const uint4* blk_maxseg, uint32_t* status, const Shape& sh,
                        cudaStream_t st, const RopeParams& rope, int n_split, float* parts) {
   using Cfg = KmCfg<D, C, W>;
   const int QB = Cfg::NQ / sh.G;
@@ -1560,7 +1717,7 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
   const int band = few_waves ? sh.Hk : (sh.Hk % 2 == 0 ? 2 : 1);
   const dim3 grid(C * band, (sh.Hk / band) * n_tg * n_split);
   r = launch_clustered(tc_key_major<D, C, W>, grid, C, Cfg::SMEM_BYTES, st,
-                                  "tensor-core key-major", mv, mq, mdo, mqt, mdot, K, LSE, Dws, seg,
+                                  "tensor-core key-major", mv, mq, mdo, mqt, mdot, K, kmeta, ld_meta,
                                   blk_minseg, blk_maxseg, dK, dV, status, sh, rope, band, n_split,
                                   parts);
   if (r != GQA_OK || n_split == 1) return r;
@@ -1572,9 +1729,11 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
 }
 
 gqa_status transpose_launch(const float* X, float* Xt, int S, int Hk, int Gx, int d, long long ld,
-                            cudaStream_t st) {
-  dim3 grid((unsigned)((ld + kTrRows - 1) / kTrRows), d / 32, Hk);   // ld >= S * Gx
-  group_transpose<<<grid, dim3(32, 8), 0, st>>>(X, Xt, S, Hk, Gx, d, ld);
+                            cudaStream_t st, float* Xp = nullptr, long long rows_p = 0) {
+  // ld >= S * Gx; with Xp (Gx = 1) the grid's 64-row tiles also cover rows_p
+  // = S rounded up to 64 (ld is S rounded up to 32)
+  dim3 grid((unsigned)((ld + kTrRows - 1) / kTrRows), d / 32, Hk);
+  group_transpose<<<grid, dim3(32, 8), 0, st>>>(X, Xt, S, Hk, Gx, d, ld, Xp, rows_p);
   note_launch();
   return check_launch("group transpose");
 }
@@ -1642,34 +1801,41 @@ int km_split(const Shape& sh) {
 template <int D>
 gqa_status km_launch(const float* Q, const float* K, const float* V, const float* dO,
                      const float* LSE, const uint32_t* seg, float* dK, float* dV, const float* Qt,
-                     const float* dOt, long long ld_qt, const float* Dws, const uint32_t* blk_minseg,
-                     const uint32_t* blk_maxseg, uint32_t* status, const Shape& sh,
-                     cudaStream_t st, const RopeParams& rope, float* parts) {
+                     const float* dOt, long long ld_qt, const float4* kmeta, long long ld_meta,
+                     const uint32_t* blk_minseg, const uint32_t* blk_maxseg, uint32_t* status,
+                     const Shape& sh, cudaStream_t st, const RopeParams& rope, float* parts) {
+  (void)LSE;
+  (void)seg;   // both reach the key-major kernel through the column records
   const int n_split = km_split(sh);
+  const uint4* bmax = reinterpret_cast<const uint4*>(blk_maxseg);   // 16-byte records
+#define GQA_KM_ARGS Q, K, V, dO, dK, dV, Qt, dOt, ld_qt, kmeta, ld_meta, blk_minseg, bmax, status, sh, st, \
+                    rope, n_split, parts
   if (km_cta_group(sh) == 2) {
     if constexpr (D == 128) {
-      if (km_wide())
-        return km_launch_c<D, 2, true>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, ld_qt, Dws, blk_minseg,
-                                       blk_maxseg, status, sh, st, rope, n_split, parts);
+      if (km_wide()) return km_launch_c<D, 2, true>(GQA_KM_ARGS);
     }
-    return km_launch_c<D, 2, false>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, ld_qt, Dws, blk_minseg,
-                                    blk_maxseg, status, sh, st, rope, n_split, parts);
+    return km_launch_c<D, 2, false>(GQA_KM_ARGS);
   }
-  return km_launch_c<D, 1, false>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, ld_qt, Dws, blk_minseg,
-                                  blk_maxseg, status, sh, st, rope, n_split, parts);
+  return km_launch_c<D, 1, false>(GQA_KM_ARGS);
+#undef GQA_KM_ARGS
 }
 
 template <int D, int C, bool GD>
 gqa_status qm_launch_c(const float* Q, const float* K, const float* V, const float* dO,
                        const float* LSE, const uint32_t* seg, float* dQ, const float* Kt,
-                       long long ld_kt, float* Dws, float* Qt, float* dOt, long long ld_qt,
-                       uint32_t* status, const Shape& sh, cudaStream_t st,
-                       const RopeParams& rope) {
+                       long long ld_kt, const float* Kp, long long rows_kp, float4* kmeta,
+                       long long ld_meta, float* Dws, float* Qt, float* dOt, long long ld_qt,
+                       uint32_t* status, const Shape& sh, cudaStream_t st, const RopeParams& rope) {
   using Cfg = QmCfg<D, C>;
   CUtensorMap mk, mv, mkt;
   gqa_status r;
   const long long kv_panels = (long long)sh.Hk * D / 32;
-  if ((r = map_panels(&mk, K, (long long)sh.Hk * D, sh.S, kv_panels, Cfg::HALF1, D / 32)) != GQA_OK) return r;
+  // CYC: K chunks from K' (rows permuted within 64-key chunks, padded to rows_kp)
+  if (Cfg::CYC && (Kp == nullptr || rows_kp < sh.S))
+    return set_error(GQA_ERR_INVALID_ARG, "query-major: K' missing from the workspace");
+  if ((r = map_panels(&mk, Cfg::CYC ? Kp : K, (long long)sh.Hk * D, Cfg::CYC ? rows_kp : sh.S, kv_panels,
+                      Cfg::HALF1, D / 32)) != GQA_OK)
+    return r;
   if ((r = map_panels(&mv, V, (long long)sh.Hk * D, sh.S, kv_panels, Cfg::HALF1, D / 32)) != GQA_OK) return r;
   if ((r = map_panels(&mkt, Kt, ld_kt, (long long)sh.Hk * D, ld_kt / 32, Cfg::KT_ROWS, Cfg::KT_PANELS)) != GQA_OK) return r;
   if (cudaFuncSetAttribute(tc_query_major<D, C, GD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1683,23 +1849,25 @@ gqa_status qm_launch_c(const float* Q, const float* K, const float* V, const flo
   const dim3 grid = slab_major ? dim3(C * sh.Hk, n_sg) : dim3(n_sg * C, sh.Hk);
   return launch_clustered(tc_query_major<D, C, GD>, grid, C, Cfg::SMEM_BYTES, st,
                           "tensor-core query-major", mk, mv, mkt, Q, dO, LSE, seg, dQ, Dws, Qt, dOt,
-                          ld_qt, status, sh, rope, slab_major);
+                          ld_qt, kmeta, ld_meta, status, sh, rope, slab_major);
 }
 
 template <int D>
 gqa_status qm_launch(const float* Q, const float* K, const float* V, const float* dO,
                      const float* LSE, const uint32_t* seg, float* dQ, const float* Kt,
-                     long long ld_kt, float* Dws, float* Qt, float* dOt, long long ld_qt,
+                     long long ld_kt, const float* Kp, long long rows_kp, float4* kmeta,
+                     long long ld_meta, float* Dws, float* Qt, float* dOt, long long ld_qt,
                      uint32_t* status, const Shape& sh, cudaStream_t st, const RopeParams& rope,
                      bool given_d) {
+#define GQA_QM_ARGS Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Kp, rows_kp, kmeta, ld_meta, Dws, Qt, dOt, ld_qt, \
+                    status, sh, st, rope
   if (given_d) {
-    if (cta_group() == 1)
-      return qm_launch_c<D, 1, true>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
-    return qm_launch_c<D, 2, true>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
+    if (cta_group() == 1) return qm_launch_c<D, 1, true>(GQA_QM_ARGS);
+    return qm_launch_c<D, 2, true>(GQA_QM_ARGS);
   }
-  if (cta_group() == 1)
-    return qm_launch_c<D, 1, false>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
-  return qm_launch_c<D, 2, false>(Q, K, V, dO, LSE, seg, dQ, Kt, ld_kt, Dws, Qt, dOt, ld_qt, status, sh, st, rope);
+  if (cta_group() == 1) return qm_launch_c<D, 1, false>(GQA_QM_ARGS);
+  return qm_launch_c<D, 2, false>(GQA_QM_ARGS);
+#undef GQA_QM_ARGS
 }
 
 }  // namespace
@@ -1733,7 +1901,13 @@ TcWsLayout tc_ws_layout(int S, int H, int Hk, int d) {
   t.dot_off = t.qt_off + align256((size_t)Hk * d * t.ld_qt * sizeof(float));
   t.blk_off = t.dot_off + align256((size_t)Hk * d * t.ld_qt * sizeof(float));
   t.blkmax_off = t.blk_off + align256((size_t)S * sizeof(uint32_t));
-  t.part_off = t.blkmax_off + align256((size_t)S * sizeof(uint32_t));
+  // K' (rows permuted within 64-key chunks) for the query-major kernel at d = 128
+  t.rows_kp = (d == 128) ? ((long long)S + 63) / 64 * 64 : 0;
+  t.kp_off = t.blkmax_off + align256((size_t)S * 4 * sizeof(uint32_t));   // 16-byte max-seg records
+  // the key-major kernel's per-column records (lse log2 e, scale D, query, seg)
+  t.ld_meta = ((long long)S * G + 63) / 64 * 64;
+  t.meta_off = t.kp_off + align256((size_t)t.rows_kp * Hk * d * sizeof(float));
+  t.part_off = t.meta_off + align256((size_t)Hk * t.ld_meta * 4 * sizeof(float));
   // the key-major kernel's partial dK / dV when it splits its walk
   const Shape sh{S, H, Hk, d, (int)G, 1.f};
   const int n_split = tc_supported(sh) ? km_split_ws(sh) : 1;
@@ -1766,10 +1940,12 @@ gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* d
   float* parts = reinterpret_cast<float*>(ws + T.part_off);
   const int QB = km_nq(sh) / sh.G;
   gqa_status r;
-  if ((r = tile_minseg(seg, sh.S, QB, blk, st, blk_max)) != GQA_OK) return r;
+  if ((r = tile_minseg(seg, sh.S, QB, blk, st, blk_max, 4)) != GQA_OK) return r;
+  float4* kmeta = reinterpret_cast<float4*>(ws + T.meta_off);
   // K^T for the query-major kernel; Q^T and dO^T are written by the
   // query-major kernel itself for the key-major one
-  if ((r = transpose_launch(K, Kt, sh.S, sh.Hk, 1, sh.d, T.ld_kt, st)) != GQA_OK) return r;
+  float* Kp = T.rows_kp > 0 ? reinterpret_cast<float*>(ws + T.kp_off) : nullptr;
+  if ((r = transpose_launch(K, Kt, sh.S, sh.Hk, 1, sh.d, T.ld_kt, st, Kp, T.rows_kp)) != GQA_OK) return r;
   // with O given, D = rowsum(dO * O) replaces the query-major kernel's pass 1
   if (O != nullptr) {
     const long long rows = (long long)sh.S * sh.H;
@@ -1780,24 +1956,24 @@ gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* d
   profile_before(st, "tc_query_major+tc_key_major");
   switch (sh.d) {
     case 32:
-      r = qm_launch<32>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope,
+      r = qm_launch<32>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Kp, T.rows_kp, kmeta, T.ld_meta, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope,
                         O != nullptr);
       if (r == GQA_OK)
-        r = km_launch<32>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope,
+        r = km_launch<32>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, kmeta, T.ld_meta, blk, blk_max, status, sh, st, rope,
                            parts);
       break;
     case 64:
-      r = qm_launch<64>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope,
+      r = qm_launch<64>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Kp, T.rows_kp, kmeta, T.ld_meta, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope,
                         O != nullptr);
       if (r == GQA_OK)
-        r = km_launch<64>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope,
+        r = km_launch<64>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, kmeta, T.ld_meta, blk, blk_max, status, sh, st, rope,
                            parts);
       break;
     default:
-      r = qm_launch<128>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope,
+      r = qm_launch<128>(Q, K, V, dO, LSE, seg, dQ, Kt, T.ld_kt, Kp, T.rows_kp, kmeta, T.ld_meta, Dws, Qt, dOt, T.ld_qt, status, sh, st, rope,
                         O != nullptr);
       if (r == GQA_OK)
-        r = km_launch<128>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, Dws, blk, blk_max, status, sh, st, rope,
+        r = km_launch<128>(Q, K, V, dO, LSE, seg, dK, dV, Qt, dOt, T.ld_qt, kmeta, T.ld_meta, blk, blk_max, status, sh, st, rope,
                            parts);
       break;
   }

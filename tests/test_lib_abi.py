@@ -105,13 +105,14 @@ def test_workspace_reserves_key_major_parts(L):
     is split into up to four parts whose partial dK / dV live in the
     workspace: [2][parts][S][Hk*d] fp32, sized for devices of up to 192 SMs,
     so the size depends on the shape alone. Deep grids (the 16k workload)
-    reserve nothing for them."""
+    reserve nothing for them, only the operand copies."""
     S, H, Hk, d = 2048, 16, 4, 64           # 64 key-major CTAs: four parts
     parts = 2 * 4 * S * Hk * d * 4
     qt = Hk * d * (S * (H // Hk)) * 4       # Q^T (and dO^T) copies
     assert L.attn_bwd_workspace_bytes(S, H, Hk, d) >= parts + 2 * qt
     S, H, Hk, d = 16384, 32, 8, 128         # 1024 key-major CTAs: no split
-    copies = 2 * Hk * d * (S * (H // Hk)) * 4 + Hk * d * S * 4   # Q^T, dO^T, K^T
+    # Q^T, dO^T, K^T, and at d = 128 K' (K's rows permuted within 64-key chunks)
+    copies = 2 * Hk * d * (S * (H // Hk)) * 4 + 2 * Hk * d * S * 4
     one_part = 2 * S * Hk * d * 4                                # what a single part would add
     assert copies <= L.attn_bwd_workspace_bytes(S, H, Hk, d) < copies + one_part // 2
 
