@@ -15,8 +15,11 @@
 //    S, dP, then dS = scale P (dP - D) written back to TMEM over S and
 //    dQ += dS K (Pass B), with B = the matching chunk of K^T (a transposed
 //    copy of K in the workspace: the TF32 MMA reads both operands K-major).
+//    At d = 128 on SM pairs pass 2 goes by chunk in four cycled TMEM slots
+//    and reads K from K', a row-permuted copy (QmCfg::CYC).
 //    dQ and D are owned writes (no atomics). Its prologue also writes the
-//    transposed copies Q^T and dO^T that the key-major kernel reads.
+//    transposed copies Q^T and dO^T that the key-major kernel reads, and
+//    each row's record for it (lse log2 e, scale D, query, seg).
 //
 //  tc_key_major (grid: key tiles x kv heads): dK and dV of 128 keys, summed
 //    over the G heads of the group, from S^T = K Q^T and dP^T = V dO^T

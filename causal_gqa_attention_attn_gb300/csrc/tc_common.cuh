@@ -104,27 +104,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-// Waits on up to four barriers at once, lane i < n on barrier bi at parity
-// pi; warp-uniform result. A satisfied wait (try_wait and the warp vote) costs
-// ~80 cycles, so an MMA warp that needs a step's copies and its softmax
-// hand-off waits for them side by side instead of one after another.
-// __syncwarp orders every lane's acquire before what the warp issues next.
-template <bool kCluster = false>
-__device__ __forceinline__ bool warp_wait4(int n, uint64_t* b0, uint32_t p0, uint64_t* b1,
-                                           uint32_t p1, uint64_t* b2, uint32_t p2, uint64_t* b3,
-                                           uint32_t p3, volatile int* abort, uint32_t* status,
-                                           uint32_t site) {
-  const int lane = threadIdx.x % 32;
-  bool ok = true;
-  if (lane < n) {
-    uint64_t* b = lane == 0 ? b0 : lane == 1 ? b1 : lane == 2 ? b2 : b3;
-    const uint32_t p = lane == 0 ? p0 : lane == 1 ? p1 : lane == 2 ? p2 : p3;
-    ok = mbar_wait<kCluster>(b, p, abort, status, site);
-  }
-  __syncwarp();
-  return __all_sync(0xffffffffu, ok);
-}
-
 // One lane of a converged warp (the same one each time): issue point for
 // TMA, MMA and commit instructions whose operands the warp computed.
 __device__ __forceinline__ bool elect_one() {
@@ -134,16 +113,6 @@ __device__ __forceinline__ bool elect_one() {
       : "+r"(pred));
   return pred != 0;
 }
-
-// 4-byte asynchronous copy global -> shared (cp.async). Its completion is
-// tracked only by cp.async.wait_group in the issuing thread: a bar.sync or an
-// mbarrier acquire that follows does not wait for it, whereas either waits for
-// the thread's outstanding ordinary loads.
-__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all_groups() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // Contiguous copy global -> this CTA's shared memory by the TMA unit
 // (cp.async.bulk): both addresses 16-byte aligned, bytes a multiple of 16;
