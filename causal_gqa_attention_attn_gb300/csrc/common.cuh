@@ -133,11 +133,8 @@ gqa_status simt_bwd(const float* Q, const float* K, const float* V, const float*
                     const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
                     const Shape& sh, char* ws, cudaStream_t st, const RopeParams& rope);
 
-// Per tile of `tile` queries: min seg into out[t] and, with out_max, max seg
-// into out_max[t * max_stride] (max_stride 4: a 16-byte record per tile,
-// its other three words zero).
 gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cudaStream_t st,
-                       uint32_t* out_max = nullptr, int max_stride = 1);
+                       uint32_t* out_max = nullptr);
 
 // Tensor-core backward, tc_bwd.cu: true if this shape has a tensor-core path.
 bool tc_supported(const Shape& sh);

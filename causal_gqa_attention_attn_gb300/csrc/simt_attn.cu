@@ -473,7 +473,7 @@ gqa_status bwd_launch(const float* Q, const float* K, const float* V, const floa
 // Smallest (and optionally largest) seg over each `tile`-row query tile (one warp per tile).
 __global__ void tile_minseg_kernel(const uint32_t* __restrict__ seg, int S, int tile,
                                    uint32_t* __restrict__ out, uint32_t* __restrict__ out_max,
-                                   int n_tiles, int max_stride) {
+                                   int n_tiles) {
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
   if (w >= n_tiles) return;
   unsigned v = 0xffffffffu, m = 0u;
@@ -491,8 +491,7 @@ __global__ void tile_minseg_kernel(const uint32_t* __restrict__ seg, int S, int 
   }
   if (lane == 0) {
     out[w] = v;
-    if (out_max != nullptr && max_stride == 4) reinterpret_cast<uint4*>(out_max)[w] = make_uint4(m, 0u, 0u, 0u);
-    else if (out_max != nullptr) out_max[w] = m;
+    if (out_max) out_max[w] = m;
   }
 }
 
@@ -520,11 +519,11 @@ gqa_status debug_check_seg(const uint32_t* seg, int S, void* ws, cudaStream_t st
 }
 
 gqa_status tile_minseg(const uint32_t* seg, int S, int tile, uint32_t* out, cudaStream_t st,
-                       uint32_t* out_max, int max_stride) {
+                       uint32_t* out_max) {
   const int n_tiles = (S + tile - 1) / tile;
   const int warps_per_block = 8;
   tile_minseg_kernel<<<(n_tiles + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0,
-                       st>>>(seg, S, tile, out, out_max, n_tiles, max_stride);
+                       st>>>(seg, S, tile, out, out_max, n_tiles);
   note_launch();
   return check_launch("tile min seg");
 }

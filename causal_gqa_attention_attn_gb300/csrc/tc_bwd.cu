@@ -1478,13 +1478,49 @@ __global__ void __launch_bounds__(kThreads, 1)
 // its rows permuted within each 64-row chunk, row 64c + 32r + 16a + i = row
 // 64c + 32a + 16r + i of X (r, a in {0, 1}, i < 16), rows rows_p (S rounded
 // up to 64) in all, those past S zero.
+// With ms.seg, a last z slice of the grid (blockIdx.z == Hk) instead forms
+// the key-major kernel's per-block seg minima and 16-byte max records (one
+// warp per block of ms.tile queries, grid-stride), so that the backward's
+// metadata costs no launch of its own.
 // ---------------------------------------------------------------------------
 constexpr int kTrRows = 64;   // rows r of X per CTA of the transpose (one K' chunk)
+
+struct MinsegJob {
+  const uint32_t* seg = nullptr;   // null: no job
+  int tile = 0, n_tiles = 0;
+  uint32_t* out_min = nullptr;
+  uint4* out_max = nullptr;
+};
 
 __global__ void __launch_bounds__(256) group_transpose(const float* __restrict__ X,
                                                        float* __restrict__ Xt, int S, int Hk,
                                                        int Gx, int d, long long ld,
-                                                       float* __restrict__ Xp, long long rows_p) {
+                                                       float* __restrict__ Xp, long long rows_p,
+                                                       MinsegJob ms) {
+  if (ms.seg != nullptr && (int)blockIdx.z == Hk) {
+    const int lane = threadIdx.x, wib = threadIdx.y;      // blockDim (32, 8)
+    const int n_warps = (int)(gridDim.x * gridDim.y) * 8;
+    for (int w = (int)(blockIdx.y * gridDim.x + blockIdx.x) * 8 + wib; w < ms.n_tiles; w += n_warps) {
+      unsigned mn = 0xffffffffu, mx = 0u;
+      for (int i = lane; i < ms.tile; i += 32) {
+        const int q = w * ms.tile + i;
+        if (q < S) {
+          const unsigned x = __ldg(ms.seg + q);
+          mn = min(mn, x);
+          mx = max(mx, x);
+        }
+      }
+      for (int o = 16; o >= 1; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      if (lane == 0) {
+        ms.out_min[w] = mn;
+        ms.out_max[w] = make_uint4(mx, 0u, 0u, 0u);
+      }
+    }
+    return;
+  }
   __shared__ float tile[kTrRows][33];
   constexpr int PER = kTrRows / 8;                        // rows per thread (blockDim.y = 8)
   const int g = blockIdx.z, e0 = blockIdx.y * 32;
@@ -1732,11 +1768,13 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
 }
 
 gqa_status transpose_launch(const float* X, float* Xt, int S, int Hk, int Gx, int d, long long ld,
-                            cudaStream_t st, float* Xp = nullptr, long long rows_p = 0) {
+                            cudaStream_t st, float* Xp = nullptr, long long rows_p = 0,
+                            MinsegJob ms = MinsegJob{}) {
   // ld >= S * Gx; with Xp (Gx = 1) the grid's 64-row tiles also cover rows_p
-  // = S rounded up to 64 (ld is S rounded up to 32)
-  dim3 grid((unsigned)((ld + kTrRows - 1) / kTrRows), d / 32, Hk);
-  group_transpose<<<grid, dim3(32, 8), 0, st>>>(X, Xt, S, Hk, Gx, d, ld, Xp, rows_p);
+  // = S rounded up to 64 (ld is S rounded up to 32); with ms.seg one more z
+  // slice forms the per-block seg records
+  dim3 grid((unsigned)((ld + kTrRows - 1) / kTrRows), d / 32, Hk + (ms.seg != nullptr ? 1 : 0));
+  group_transpose<<<grid, dim3(32, 8), 0, st>>>(X, Xt, S, Hk, Gx, d, ld, Xp, rows_p, ms);
   note_launch();
   return check_launch("group transpose");
 }
@@ -1943,12 +1981,18 @@ gqa_status tc_bwd(const float* Q, const float* K, const float* V, const float* d
   float* parts = reinterpret_cast<float*>(ws + T.part_off);
   const int QB = km_nq(sh) / sh.G;
   gqa_status r;
-  if ((r = tile_minseg(seg, sh.S, QB, blk, st, blk_max, 4)) != GQA_OK) return r;
   float4* kmeta = reinterpret_cast<float4*>(ws + T.meta_off);
-  // K^T for the query-major kernel; Q^T and dO^T are written by the
-  // query-major kernel itself for the key-major one
+  // One launch: K^T and K' for the query-major kernel, and (its last z slice)
+  // the per-block seg min / max records for the key-major one. Q^T, dO^T and
+  // the column records are written by the query-major kernel itself.
   float* Kp = T.rows_kp > 0 ? reinterpret_cast<float*>(ws + T.kp_off) : nullptr;
-  if ((r = transpose_launch(K, Kt, sh.S, sh.Hk, 1, sh.d, T.ld_kt, st, Kp, T.rows_kp)) != GQA_OK) return r;
+  MinsegJob ms;
+  ms.seg = seg;
+  ms.tile = QB;
+  ms.n_tiles = (sh.S + QB - 1) / QB;
+  ms.out_min = blk;
+  ms.out_max = reinterpret_cast<uint4*>(blk_max);
+  if ((r = transpose_launch(K, Kt, sh.S, sh.Hk, 1, sh.d, T.ld_kt, st, Kp, T.rows_kp, ms)) != GQA_OK) return r;
   // with O given, D = rowsum(dO * O) replaces the query-major kernel's pass 1
   if (O != nullptr) {
     const long long rows = (long long)sh.S * sh.H;
