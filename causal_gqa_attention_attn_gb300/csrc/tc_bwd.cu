@@ -945,7 +945,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 2.0 GB of DRAM reads per launch); band = Hk: the heaviest tiles of every
   // head first, which matters when the grid is only a few waves deep (packed
   // 4k documents: 1.12 -> 0.99 ms; at 16k it read 13.7 GB). The host picks.
-  // With n_split > 1 (a grid under four waves deep) y also carries the part
+  // With n_split > 1 (a grid under one wave deep) y also carries the part
   // of the tile pair's query walk this CTA takes (innermost).
   const int n_tg = ((S + 127) / 128 + C - 1) / C;
   const int yy = (int)blockIdx.y / n_split, part = (int)blockIdx.y % n_split;
@@ -1818,14 +1818,16 @@ int km_nq(const Shape& sh) {
 }
 
 // Parts the key-major kernel splits each tile (pair)'s query walk into: 1
-// when its grid is at least four waves deep (one CTA per SM), else enough
-// parts, at most four, to fill about four waves. Each part writes partial
-// dK / dV sums to the workspace; km_split_reduce adds them up.
+// when its grid fills at least one wave (one CTA per SM), else enough parts,
+// at most four, to fill about four waves. Each part writes partial dK / dV
+// sums to the workspace; km_split_reduce adds them up. (Packed 4k documents,
+// a 1.7-wave grid: unsplit 839 us, two parts 857 us; packed 2k documents, 0.4
+// waves: four parts 94 us, unsplit 134 us.)
 int km_split_for(const Shape& sh, int n_sm) {
   const int C = km_cta_group(sh);
   const long long ctas = (long long)(((sh.S + 127) / 128 + C - 1) / C) * C * sh.Hk;
   const long long target = 4LL * n_sm;
-  if (ctas >= target) return 1;
+  if (ctas >= n_sm) return 1;
   const long long n = target / ctas;
   return (int)(n < 1 ? 1 : (n > 4 ? 4 : n));
 }

@@ -101,7 +101,7 @@ def test_short_path_limits_and_switch(L):
 
 
 def test_workspace_reserves_key_major_parts(L):
-    """Where the key-major grid is under four waves (one CTA per SM) its walk
+    """Where the key-major grid is under one wave (one CTA per SM) its walk
     is split into up to four parts whose partial dK / dV live in the
     workspace: [2][parts][S][Hk*d] fp32, sized for devices of up to 192 SMs,
     so the size depends on the shape alone. Deep grids (the 16k workload)
