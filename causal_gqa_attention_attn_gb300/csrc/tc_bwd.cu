@@ -1384,7 +1384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (NS == 1) {
         // two hand-overs per block, in the order of KmCfg::w_first: half h of
         // warpgroup wg is columns 16 wg + [0, 16) of the half's S^T and dP^T
-        // slots (block columns 32 h + 16 wg + [0, 16): metadata entries 16 h..).
+        // slots (block columns 32 h + 16 wg + [0, 16): records 32 h + 16 wg ..).
         // The first half's S^T slot is ready with s_full[0] (which also
         // covers the block's dP^T), the second's with s_full[1].
         const int p = n & 1;
