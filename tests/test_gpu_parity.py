@@ -206,8 +206,9 @@ EDGE = [
     (127, 4, 1, 32, "nonmonotone"), (129, 6, 3, 64, "docs"), (200, 8, 8, 128, "causal"),
     (333, 16, 2, 64, "nonmonotone"), (97, 4, 2, 100, "docs"), (64, 2, 1, 16, "causal"),
     (300, 8, 1, 128, "docs"), (513, 4, 2, 32, "docs"), (256, 16, 2, 128, "causal"),
-    # key-major block halves of one query (G = 16 at d = 128), and groups too
-    # wide for the SM-pair key-major kernel (G = 32 at d = 128, 64 at d = 64)
+    # wide groups: at d = 128 a key-major Q sub-tile of 16 rows is one query's
+    # 16 heads (G = 16) or half of one query's heads (G = 32); G = 64 at d = 64
+    # is too wide for the SM-pair key-major kernel and runs on one SM
     (90, 16, 1, 128, "docs"), (160, 32, 1, 128, "causal"), (70, 64, 1, 64, "nonmonotone"),
 ]
 
