@@ -23,6 +23,10 @@
 //               passes move about the same bytes).
 //  decode_dq:   d_q += the partials added in a fixed order.
 // No atomics: results do not depend on scheduling.
+// The last three launch as programmatic dependents of the one before (each
+// kernel lets its successor start once all its CTAs run): decode_dkv loads
+// its key and d_k rows, which no earlier kernel writes, before it waits for
+// the staged dP and D; decode_dsum and decode_dq wait first.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -82,6 +86,12 @@ __device__ __forceinline__ void store_cols(float* p, const float* v) {
   }
 }
 
+// Programmatic dependent launch: let the next kernel of the stream start, and
+// wait until the previous one has completed with its writes visible (both
+// no-ops for a kernel not launched as a dependent).
+__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prev() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -98,6 +108,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_dp(const float* __restrict
                                                          int Hk, int G) {
   constexpr int D = 32 * E, KPW = dec_kpw(E);
   extern __shared__ float red[];                  // [kDecWarps][G] per-warp partial sums
+  pdl_launch_next();
   const int g = blockIdx.y, blk = blockIdx.x;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int j0 = blk * dec_keys(E) + warp * KPW;
@@ -161,6 +172,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_dp(const float* __restrict
 __global__ void __launch_bounds__(256) decode_dsum(const float* __restrict__ dpart,
                                                    float* __restrict__ dsum, int nblk, int H) {
   __shared__ float part[8];
+  pdl_launch_next();
+  pdl_wait_prev();                                // decode_dp's partial sums
   const int h = blockIdx.x;
   float s = 0.f;
   for (int b = threadIdx.x; b < nblk; b += 256) s += dpart[(long long)b * H + h];
@@ -201,6 +214,8 @@ __global__ void __launch_bounds__(kDecThreads, E >= 3 ? 4 : 3) decode_dkv(
       for (int e = 0; e < E; ++e) kr[k][e] = dk[k][e] = 0.f;
     }
   }
+  pdl_launch_next();
+  pdl_wait_prev();                                // D and the staged dP of the earlier kernels
   for (int c0 = 0; c0 < G; c0 += HC) {
     // lane l: probs and the staged dP (decode_dp) of head c0 + l / KPW, key
     // j0 + l % KPW (0 past the ends), loaded before this chunk's d_scores
@@ -266,6 +281,7 @@ __global__ void __launch_bounds__(32 * kDqWarps) decode_dq(const float* __restri
                                                            float* __restrict__ dq, int nblk, int H,
                                                            int D) {
   __shared__ float part[kDqWarps][33];
+  pdl_wait_prev();                                // decode_dkv's partial d_q
   const int h = blockIdx.x, lane = threadIdx.x % 32, w = threadIdx.x / 32;
   const int c = blockIdx.y * 32 + lane;
   float s = 0.f;
@@ -287,6 +303,24 @@ __global__ void __launch_bounds__(32 * kDqWarps) decode_dq(const float* __restri
     for (int i = 0; i < kDqWarps; ++i) t += part[i][lane];
     dq[(long long)h * D + c] += t;
   }
+}
+
+// Launch as a programmatic dependent of the stream's previous kernel (it may
+// start before that one completes and waits in griddepcontrol.wait).
+template <class... KArgs, class... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 template <int E>
@@ -311,15 +345,20 @@ gqa_status decode_launch(const float* q, const float* k_hist, const float* v_his
   note_launch();
   gqa_status r;
   if ((r = check_launch("decode dP")) != GQA_OK) return r;
-  decode_dsum<<<H, 256, 0, st>>>(dpart, dsum, w.nblk, H);
+  cudaError_t e = launch_dependent(decode_dsum, dim3((unsigned)H), dim3(256), 0, st,
+                                   (const float*)dpart, dsum, w.nblk, H);
   note_launch();
+  if (e != cudaSuccess) return set_error(GQA_ERR_CUDA, "decode D: %s", cudaGetErrorString(e));
   if ((r = check_launch("decode D")) != GQA_OK) return r;
-  decode_dkv<E><<<grid, kDecThreads, 0, st>>>(q, k_hist, probs, d_out, d_scores, dsum, d_k, qpart,
-                                              L, H, Hk, G, scale);
+  e = launch_dependent(decode_dkv<E>, grid, dim3(kDecThreads), 0, st, q, k_hist, probs, d_out,
+                       d_scores, (const float*)dsum, d_k, qpart, L, H, Hk, G, scale);
   note_launch();
+  if (e != cudaSuccess) return set_error(GQA_ERR_CUDA, "decode dK dV: %s", cudaGetErrorString(e));
   if ((r = check_launch("decode dK dV")) != GQA_OK) return r;
-  decode_dq<<<dim3((unsigned)H, D / 32), 32 * kDqWarps, 0, st>>>(qpart, d_q, w.nblk, H, D);
+  e = launch_dependent(decode_dq, dim3((unsigned)H, D / 32), dim3(32 * kDqWarps), 0, st,
+                       (const float*)qpart, d_q, w.nblk, H, D);
   note_launch();
+  if (e != cudaSuccess) return set_error(GQA_ERR_CUDA, "decode dQ: %s", cudaGetErrorString(e));
   return check_launch("decode dQ");
 }
 
