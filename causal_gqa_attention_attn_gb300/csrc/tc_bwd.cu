@@ -156,6 +156,14 @@ __device__ __forceinline__ void arrive_issuer(uint64_t* bar) {
   else mbar_arrive_cl(mapa_u32(bar, 0));
 }
 
+// Programmatic dependent launch (the query-major, key-major and part-sum
+// kernels are launched as dependents of the kernel before them): let the
+// next kernel of the stream start once every CTA of this one runs, and wait
+// until the previous kernel has completed with its writes visible. Both are
+// no-ops for a kernel not launched as a dependent.
+__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prev() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // GD: D is given (precomputed from O, attn_bwd_o): pass 1 is skipped.
 template <int D, int C, bool GD>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -191,6 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int slab = top_slab - (int)rank;
   const int q0 = slab * QR;
   const int S = sh.S, H = sh.H;
+  // The key-major kernel may start once every CTA of this one runs. Until
+  // this kernel waits (pdl_wait_prev), it reads only the call's inputs: the
+  // K' / K^T copies and the per-block records of the kernel before are read
+  // after the producers' waits, D (given O) after the compute warps'.
+  pdl_launch_next();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NU; ++i) {
@@ -254,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&mapKt);
     }
     __syncwarp();
+    pdl_wait_prev();                       // K' and K^T of the kernel before
     for (int i = pw; i < n_units; i += 2) {
       const int u = i % NU;
       if (i >= NU &&
@@ -532,6 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
+      pdl_wait_prev();                     // the kernel before (D when given) has completed
       // the units of the MMAs issued after qdo_ready: pass-1 chunks 0 and 1,
       // and pass-2 sub-chunk st's K, V for a stage st that pass 1 leaves
       // unused (CYC: pass-2 chunk 0 is issued after both stages' last pass-1
@@ -991,7 +1006,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // this CTA's part of the query blocks [qb0, nqb) (all of them when n_split = 1)
   const int pb0 = qb0 + (int)((long long)(nqb - qb0) * part / n_split);
   const int pb1 = qb0 + (int)((long long)(nqb - qb0) * (part + 1) / n_split);
-  BlockWalk walk(blk_minseg, (unsigned)k_hi, pb0, pb1);
+  // The per-block records (blk_minseg / blk_maxseg) come from two kernels
+  // back and the column records, Q^T and dO^T from the query-major kernel, so
+  // every role waits (pdl_wait_prev) before its block walk; before that only
+  // the call's inputs are read (K into TMEM, V).
+  pdl_launch_next();
 
   if (warp < kProducerWarps) {
     // ---------------- TMA producers: warp 0 loads Q and dO, warp 1 Q^T, dO^T and V ----------------
@@ -1014,6 +1033,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+    pdl_wait_prev();
+    BlockWalk walk(blk_minseg, (unsigned)k_hi, pb0, pb1);
     uint64_t* full = pw == 0 ? bars.qdo_full : bars.t_full;
     uint64_t* empty = pw == 0 ? bars.qdo_empty : bars.t_empty;
     const int ns = pw == 0 ? Cfg::NSQ : Cfg::NST;      // this warp's stages
@@ -1057,6 +1078,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int m = max(0, n - ns); m < n; ++m)
       warp_wait<kCl>(&full[m % ns], (m / ns) & 1, abort, status, kSiteKmProducer);
   } else if (warp == kMmaWarp && issuer) {
+    pdl_wait_prev();
+    BlockWalk walk(blk_minseg, (unsigned)k_hi, pb0, pb1);
     // ---------------- MMA issuer (warp-converged, elected issue) ----------------
     // One barrier per step and never a copy: the compute warps of both CTAs
     // wait for the copies that the MMAs issued after their next hand-back
@@ -1289,6 +1312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
     }
+    pdl_wait_prev();
+    BlockWalk walk(blk_minseg, (unsigned)k_hi, pb0, pb1);
     // Copies the MMA warp reads after this warp's next hand-back, waited for
     // on this CTA's barriers: V and the Q / dO tiles of blocks 0 .. NS-1
     // before k_ready; per block n, its Q^T / dO^T tiles and block n+NS's
@@ -1497,6 +1522,9 @@ __global__ void __launch_bounds__(256) group_transpose(const float* __restrict__
                                                        int Gx, int d, long long ld,
                                                        float* __restrict__ Xp, long long rows_p,
                                                        MinsegJob ms) {
+  // the query-major kernel (a programmatic dependent) may start its prologue,
+  // which reads none of this kernel's outputs, once every CTA here runs
+  pdl_launch_next();
   if (ms.seg != nullptr && (int)blockIdx.z == Hk) {
     const int lane = threadIdx.x, wib = threadIdx.y;      // blockDim (32, 8)
     const int n_warps = (int)(gridDim.x * gridDim.y) * 8;
@@ -1573,6 +1601,7 @@ __global__ void __launch_bounds__(256) km_split_reduce(const float* __restrict__
                                                        float* __restrict__ dV, int S, int hkd,
                                                        int d, int n_split, const RopeParams rope,
                                                        const uint32_t* __restrict__ status) {
+  pdl_wait_prev();                         // the key-major kernel's parts
   const long long n4 = (long long)S * hkd / 4;
   const long long i4 = (long long)blockIdx.x * 256 + threadIdx.x;
   if (i4 >= 2 * n4 || *status != 0u) return;
@@ -1699,13 +1728,17 @@ gqa_status launch_clustered(void (*kern)(KArgs...), dim3 grid, int cluster, int 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // a programmatic dependent of the stream's previous kernel (the kernels
+  // launched here wait in pdl_wait_prev before they read its outputs)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
   note_launch();
   if (e != cudaSuccess) return set_error(GQA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -1761,9 +1794,20 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
                                   parts);
   if (r != GQA_OK || n_split == 1) return r;
   const long long n4 = (long long)sh.S * sh.Hk * D / 4;
-  km_split_reduce<<<(unsigned)((2 * n4 + 255) / 256), 256, 0, st>>>(parts, dK, dV, sh.S, sh.Hk * D,
-                                                                   D, n_split, rope, status);
+  // a programmatic dependent of the key-major kernel (it waits first)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((2 * n4 + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, km_split_reduce, (const float*)parts, dK, dV, sh.S,
+                                           sh.Hk * D, D, n_split, rope, (const uint32_t*)status);
   note_launch();
+  if (e != cudaSuccess) return set_error(GQA_ERR_CUDA, "key-major part sums: %s", cudaGetErrorString(e));
   return check_launch("key-major part sums");
 }
 
