@@ -55,10 +55,31 @@ def counted_flops(head_dim: int, n_heads: int, pairs: int) -> float:
 
 
 def executed_flops(head_dim: int, n_heads: int, pairs: int, contractions: int = 9) -> float:
-    """What the tensor-core path multiplies: the query-major kernel forms S and
-    dP twice (D pass, dS pass) plus dS K, the key-major kernel S^T and dP^T
-    again plus P^T dO and dS^T Q: nine d-deep contractions per pair and head."""
+    """What the tensor-core path multiplies: ``contractions`` d-deep
+    contractions per pair and head (``executed_contractions``)."""
     return 2.0 * contractions * head_dim * n_heads * pairs
+
+
+def _env_flag(env, name: str) -> bool:
+    try:
+        return int(env.get(name, "0") or 0) == 1
+    except ValueError:
+        return False
+
+
+def executed_contractions(head_dim: int, given_o: bool, env=None) -> int:
+    """Contractions per pair and head that the tensor-core backward runs. The
+    key-major kernel always runs four (S^T, dP^T, P^T dO, dS^T Q). The
+    query-major kernel runs three with O given (S, dP, dS K), four in its
+    single pass at d = 128 on SM pairs (S, dP, (P dP) K, P K), else five (S
+    and dP in the D pass and again in the dS pass, dS K). GQA_TC_CTA_GROUP=1
+    and GQA_QM_TWO_PASS=1 select the forms without the single pass, as in the
+    library."""
+    env = os.environ if env is None else env
+    if given_o:
+        return 7
+    single = head_dim == 128 and not _env_flag(env, "GQA_TC_CTA_GROUP") and not _env_flag(env, "GQA_QM_TWO_PASS")
+    return 8 if single else 9
 
 
 def dist_env() -> tuple[int, int, int]:
@@ -494,7 +515,7 @@ def run_gpu(args) -> dict | None:
                  "traffic": _traffic(stage, w.name), "stage_ms": stage_ms,
                  "flops_per_launch": flops})
     if tensor_path:
-        ex = executed_flops(d, H, pairs, 7 if args.given_o else 9)
+        ex = executed_flops(d, H, pairs, executed_contractions(d, args.given_o))
         roof.update({"executed_flops_per_launch": ex,
                      "executed_tflops": ex / (stage_ms / 1e3) / 1e12,
                      "executed_frac": ex / (stage_ms / 1e3) / 1e12 / peak,

@@ -16,7 +16,10 @@
 //    dQ += dS K (Pass B), with B = the matching chunk of K^T (a transposed
 //    copy of K in the workspace: the TF32 MMA reads both operands K-major).
 //    At d = 128 on SM pairs pass 2 goes by chunk in four cycled TMEM slots
-//    and reads K from K', a row-permuted copy (QmCfg::CYC).
+//    and reads K from K', a row-permuted copy (QmCfg::CYC), and by default
+//    the two passes are one (QmCfg::SP): the walk accumulates U = sum P dP K
+//    and W = sum P K beside D = rowsum(P dP), and dQ = scale (U - D W), since
+//    dS K = scale (P dP - D P) K. Four contractions per chunk instead of five.
 //    dQ and D are owned writes (no atomics). Its prologue also writes the
 //    transposed copies Q^T and dO^T that the key-major kernel reads, and
 //    each row's record for it (lse log2 e, scale D, query, seg).
@@ -78,9 +81,10 @@ enum : uint32_t {
 // pass-2 sub-chunk h is made of keys h*BK2/2 + [0, BK2/2) of each CTA's half
 // (a fixed permutation of the chunk's keys, undone by key_of()).
 // ---------------------------------------------------------------------------
-template <int D_, int C_>
+template <int D_, int C_, bool SP_ = false>
 struct QmCfg {
   static constexpr int D = D_, C = C_;
+  static constexpr bool SP = SP_;
   static constexpr int BK1 = 64;                            // keys per chunk
   static constexpr int BK2 = (D == 128) ? 32 : 64;          // keys per pass-2 sub-chunk
   static constexpr int NSUB = BK1 / BK2;
@@ -92,17 +96,30 @@ struct QmCfg {
   static constexpr int KT_PANELS = BK1 / 32;
   static constexpr int KT_PANEL_BYTES = KT_ROWS * 128;
   static_assert(KT_PANELS * KT_PANEL_BYTES == UNIT_BYTES, "K^T unit size");
-  static constexpr int NUNIT = (192 * 1024 / UNIT_BYTES < 12) ? 192 * 1024 / UNIT_BYTES : 12;
+  // SP (single pass, below): the slab's dO rows in shared memory ahead of
+  // the ring, 128 rows x 32 floats per panel, as the A operand of dP
+  static constexpr int DO_PANEL_BYTES = 128 * 128;
+  static constexpr int DO_BYTES = SP ? PANELS * DO_PANEL_BYTES : 0;
+  static constexpr int OFF_DO = 0, OFF_RING = DO_BYTES;
+  // (SP: 9 units, three chunks: the producers stay about two chunks ahead
+  // of the MMAs that read them)
+  static constexpr int RING_BUDGET = (SP ? 144 : 192) * 1024;
+  static constexpr int NUNIT = (RING_BUDGET / UNIT_BYTES < 12) ? RING_BUDGET / UNIT_BYTES : 12;
   static_assert(NUNIT >= 6, "ring depth");
   // + alignment slack; at least 120 KB so that one CTA (holding all 512 TMEM
   // columns) runs per SM and a second never waits in tcgen05.alloc
-  static constexpr int SMEM_BYTES =
-      (NUNIT * UNIT_BYTES + 1024 > 120 * 1024) ? NUNIT * UNIT_BYTES + 1024 : 120 * 1024;
+  static constexpr int SMEM_BYTES = (DO_BYTES + NUNIT * UNIT_BYTES + 1024 > 120 * 1024)
+                                        ? DO_BYTES + NUNIT * UNIT_BYTES + 1024
+                                        : 120 * 1024;
+  // 227 KB per CTA, of which the static barriers and row sums take 2 KB
+  static_assert(SMEM_BYTES <= 225 * 1024, "shared memory budget (with the static barriers)");
   // TMEM columns: Q | dO | dQ | stages. A pass-1 stage holds S and dP of a
   // chunk (2 BK1 columns); when two do not fit beside dQ, stage 1 of pass 1
   // uses the dQ columns, which pass 1 does not touch. The two pass-2 stages
   // (2 BK2 columns each) lie inside the pass-1 stage columns.
+  // SP: Q | U | W | four slots, U and W in the dO and dQ columns.
   static constexpr uint32_t T_Q = 0, T_DO = D, T_DQ = 2 * D, T_ST = 3 * D;
+  static constexpr uint32_t T_U = D, T_W = 2 * D;
   static constexpr uint32_t W1 = 2 * BK1, W2 = 2 * BK2;
   static constexpr bool P1_IN_DQ = T_ST + 2 * W1 > 512;
   static constexpr uint32_t p1_stage(int st) { return st == 0 ? T_ST : (P1_IN_DQ ? T_DQ : T_ST + W1); }
@@ -134,6 +151,13 @@ struct QmCfg {
   static constexpr int c_dp_slot(int p, int h) { return 1 - p + h; }
   static_assert(!CYC || (BK1 == 64 && HALF1 == 32 && T_ST + 128 <= 512 && P1_IN_DQ),
                 "chunk-level pass 2: 64-key chunks, four slots in the pass-1 stage-0 columns");
+  // SP (single pass, CYC shapes without a given D): one walk over the chunks
+  // accumulates U = sum_k P dP K and W = sum_k P K beside D = rowsum(P dP);
+  // the epilogue forms dQ = scale (U - D W). Per chunk: S halves (A = Q in
+  // TMEM), dP (A = dO in shared memory: SS), then per half W += P K (A = P
+  // over S) and U += (P dP) K (A = P dP over dP), with the slots cycled as in
+  // the key-major kernel (W in the role of dV, U in that of dK).
+  static_assert(!SP || (CYC && DO_PANEL_BYTES % 1024 == 0), "single pass: d = 128 on SM pairs");
 };
 
 struct QmBarriers {
@@ -165,7 +189,8 @@ __device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol
 __device__ __forceinline__ void pdl_wait_prev() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // GD: D is given (precomputed from O, attn_bwd_o): pass 1 is skipped.
-template <int D, int C, bool GD>
+// SP: the single pass of QmCfg (d = 128 on SM pairs, D not given).
+template <int D, int C, bool GD, bool SP>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_query_major(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
                    const __grid_constant__ CUtensorMap mapKt,
@@ -175,12 +200,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                    float* __restrict__ dOt, long long ld_qt, float4* __restrict__ kmeta,
                    long long ld_meta, uint32_t* __restrict__ status, Shape sh,
                    const RopeParams rope, int slab_major) {
-  using Cfg = QmCfg<D, C>;
+  using Cfg = QmCfg<D, C, SP>;
+  static_assert(!SP || !GD, "the single pass forms D itself");
   constexpr int NU = Cfg::NUNIT;
   constexpr bool kCl = C > 1;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int smem_shift = (int)(smem - smem_raw);   // 0 .. 1023
   __shared__ QmBarriers bars;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int G = sh.G, QR = 128 / G;
@@ -245,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q_last = min(top_slab * QR + QR, S) - 1;
   const int kc0 = (int)(min(bars.kmin, (unsigned)q_last) / Cfg::BK1);
   const int nk = q_last / Cfg::BK1 - kc0 + 1;          // chunks per pass
-  const int p2_base = GD ? 0 : 2 * nk;                 // first pass-2 unit
+  const int p2_base = (GD || SP) ? 0 : 2 * nk;         // first pass-2 unit
   const int n_units = p2_base + 3 * nk;                // 2 per pass-1 chunk, 3 per pass-2 chunk
   const int n_sub = Cfg::NSUB * nk;                    // pass-2 sub-chunks
   volatile int* abort = &bars.abort;
@@ -278,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int chunk = p1 ? i / 2 : (i - p2_base) / 3;
       const int kind = p1 ? i % 2 : (i - p2_base) % 3;
       const int key0 = (kc0 + chunk) * Cfg::BK1;
-      unsigned char* dst = smem + u * Cfg::UNIT_BYTES;
+      unsigned char* dst = smem + Cfg::OFF_RING + u * Cfg::UNIT_BYTES;
       if (elect_one()) {
         mbar_arrive_expect_tx(&bars.full[u], Cfg::UNIT_BYTES);
         if (kind == 2)
@@ -305,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t id_s1 = idesc_tf32(128 * C, Cfg::BK1, false, false);   // pass 1 S, dP: N = BK1
     constexpr uint32_t id_s2 = idesc_tf32(128 * C, Cfg::BK2, false, false);   // pass 2 S, dP: N = BK2
     constexpr uint32_t id_q = idesc_tf32(128 * C, D, false, false);           // dQ: N = d
-    const uint64_t desc0 = sdesc(smem_u32(smem), 16, 1024);
+    const uint64_t desc0 = sdesc(smem_u32(smem + Cfg::OFF_RING), 16, 1024);
     auto unit_desc = [&](int i) { return desc0 + (uint64_t)(((i % NU) * Cfg::UNIT_BYTES) >> 4); };
     int use0 = 0, use1 = 0;       // pass-1 uses of each TMEM stage (s_free phases)
     // wait until the previous use of stage st has been released by its warpgroup(s)
@@ -327,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = warp_wait<kCl>(&bars.qdo_ready, 0, abort, status, kSiteQmMma);
     // ---- pass 1: chunk c in stage c & 1 ----
-    for (int c = 0; ok && !GD && c < nk; ++c) {
+    for (int c = 0; ok && !GD && !SP && c < nk; ++c) {
       const int st = c & 1;
       const int ust = st ? use1 : use0;   // the stage's earlier uses (its release to wait for)
       // K, V of chunk c: covered by qdo_ready (c < 2) or by chunk c-2's release of the stage
@@ -344,7 +371,97 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (st) ++use1; else ++use0;
     }
-    if constexpr (Cfg::CYC) {
+    if constexpr (SP) {
+    // ---- single pass by chunk j (QmCfg::SP): per chunk, with f = its first
+    // half and l the other: wait f's P / P dP, issue W_f(j), U_f(j) and, into
+    // the two slots they read, dP(j+1); wait l's, issue U_l(j), S of (j+1)'s
+    // first half into l's dP slot, W_l(j), then S of (j+1)'s second half into
+    // l's S slot. MMAs run in issue order, so no slot is rewritten before the
+    // MMA that reads it.
+    constexpr uint32_t id_h = idesc_tf32(128 * C, 32, false, false);
+    const uint64_t a_do = sdesc(smem_u32(smem + Cfg::OFF_DO), 16, 1024);   // the slab's dO rows
+    auto s_half = [&](int j, int h) {
+      const uint32_t d = tmem + Cfg::t_slot(Cfg::c_s_slot(j & 1, h));
+      const uint64_t bk = unit_desc(3 * j) + (uint64_t)((h * 16 * 128) >> 4);
+      mma_ts_g<C>(d, tmem + Cfg::T_Q, bk, id_h, 0u);
+#pragma unroll
+      for (int ks = 1; ks < D / 8; ++ks)
+        mma_ts_acc_g<C>(d, tmem + Cfg::T_Q + 8 * ks, bk + desc_off(ks, Cfg::KV_PANEL_BYTES), id_h);
+    };
+    // dP of chunk j into its two dP slots (N = 64; SS: A = dO)
+    auto dp_pair = [&](int j) {
+      const uint32_t d = tmem + Cfg::t_slot(Cfg::c_dp_slot(j & 1, 0));
+      const uint64_t bv = unit_desc(3 * j + 1);
+      mma_ss_g<C>(d, a_do, bv, id_s1, 0u);
+#pragma unroll
+      for (int ks = 1; ks < D / 8; ++ks)
+        mma_ss_acc_g<C>(d, a_do + desc_off(ks, Cfg::DO_PANEL_BYTES), bv + desc_off(ks, Cfg::KV_PANEL_BYTES),
+                        id_s1);
+    };
+    // acc += X_h K_h over half h of chunk j: K steps 4h + i (keys 32 h + 8 i
+    // ..), X at column 8 i of slot sl, B = the K^T unit (panel h). Chunk 0 is
+    // even, so its half 0 issues the first (overwriting) MMA.
+    auto acc_half = [&](int j, int h, uint32_t acc, int sl) {
+      const uint32_t a = tmem + Cfg::t_slot(sl);
+      const uint64_t bkt = unit_desc(3 * j + 2);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        mma_ts_g<C>(tmem + acc, a + 8 * i, bkt + desc_off(4 * h + i, Cfg::KT_PANEL_BYTES), id_q,
+                    (j > 0 || h > 0 || i > 0) ? 1u : 0u);
+    };
+    auto w_half = [&](int j, int h) { acc_half(j, h, Cfg::T_W, Cfg::c_s_slot(j & 1, h)); };
+    auto u_half = [&](int j, int h) { acc_half(j, h, Cfg::T_U, Cfg::c_dp_slot(j & 1, h)); };
+    // chunk 0 (qdo_ready covers dO in shared memory and its K', V units)
+    if (ok && elect_one()) {
+      tc_fence_after();
+      dp_pair(0);
+      s_half(0, Cfg::c_first(0));
+      mma_commit_g<C>(&bars.s_full[0]);
+      s_half(0, Cfg::c_first(0) ^ 1);
+      mma_commit_g<C>(&bars.s_full[1]);
+      mma_commit_g<C>(&bars.empty[0]);
+      mma_commit_g<C>(&bars.empty[1]);
+    }
+    __syncwarp();
+    for (int j = 0; ok && j < nk; ++j) {
+      const bool more = j + 1 < nk;
+      const int hf = Cfg::c_first(j & 1), hl = hf ^ 1;   // chunk j+1 hands hl back first
+      const int ik = 3 * j;
+      // first half back (which also covers K^T of chunk j and K', V of j+1)
+      if (!warp_wait<kCl>(&bars.s_free[0], j & 1, abort, status, kSiteQmMma)) {
+        ok = false;
+        break;
+      }
+      if (elect_one()) {
+        tc_fence_after();
+        w_half(j, hf);
+        u_half(j, hf);
+        if (more) dp_pair(j + 1);
+      }
+      __syncwarp();
+      if (!warp_wait<kCl>(&bars.s_free[1], j & 1, abort, status, kSiteQmMma)) {
+        ok = false;
+        break;
+      }
+      if (elect_one()) {
+        tc_fence_after();
+        u_half(j, hl);
+        if (more) {
+          s_half(j + 1, hl);
+          mma_commit_g<C>(&bars.s_full[0]);
+        }
+        w_half(j, hl);
+        mma_commit_g<C>(&bars.empty[(ik + 2) % NU]);
+        if (more) {
+          s_half(j + 1, hf);
+          mma_commit_g<C>(&bars.s_full[1]);
+          mma_commit_g<C>(&bars.empty[(ik + 3) % NU]);
+          mma_commit_g<C>(&bars.empty[(ik + 4) % NU]);
+        }
+      }
+      __syncwarp();
+    }
+    } else if constexpr (Cfg::CYC) {
     // ---- pass 2 by chunk j (QmCfg::CYC): per chunk, with f = its first half
     // and l the other: wait f's dS, issue dQ_f(j) and, into the two slots
     // that frees (dQ_f reads f's S slot; its dP slot is free once the
@@ -493,10 +610,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     warp_wait<kCl>(&bars.dq_done, 0, abort, status, kSiteQmMma);
   } else if (warp >= kFirstCompute) {
     // ---------------- compute: two warpgroups, one TMEM lane (= one row) per thread ----------------
-    // Warpgroup wg takes the chunks / sub-chunks of TMEM stage wg, so two are
-    // in flight at once; each keeps a partial row sum of P dP over its pass-1
-    // chunks, and the two partials are added through shared memory before the
-    // first dS is formed.
+    // Each warpgroup keeps a partial row sum of P dP over its columns of the
+    // pass-1 chunks (SP: of the single pass), and the two partials are added
+    // through shared memory before the first dS (SP: the epilogue) needs D.
     const int wg = (warp - kFirstCompute) >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int qi = r / G, q = q0 + qi;
@@ -519,11 +635,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto p2_kv = [&](int s2) { return p2_base + 3 * (Cfg::CYC ? s2 : s2 / Cfg::NSUB); };
     bool ok = true;
     // Q (warpgroup 0) or dO (warpgroup 1) rows into TMEM, rounded to TF32:
-    // the A operands of S and dP. The same rows go, unrounded, to the
-    // transposed copy Q^T / dO^T that the key-major kernel reads (column
-    // q0*G + r of kv group g; a warp's 32 rows are 32 adjacent columns, so
-    // each store instruction writes 128 contiguous bytes). Rows past the
-    // sequence write the zero padding columns.
+    // the A operands of S and dP (SP: dO into shared memory instead, in the
+    // 128-byte-swizzled layout a TMA load of 32-float boxes would give). The
+    // same rows go, unrounded, to the transposed copy Q^T / dO^T that the
+    // key-major kernel reads (column q0*G + r of kv group g; a warp's 32 rows
+    // are 32 adjacent columns, so each store instruction writes 128
+    // contiguous bytes). Rows past the sequence write the zero padding columns.
     {
       const float* src = (wg == 0) ? Q : dO;
       float* xt = (wg == 0) ? Qt : dOt;
@@ -542,8 +659,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           v[i] = to_tf32(x.x); v[i + 1] = to_tf32(x.y); v[i + 2] = to_tf32(x.z); v[i + 3] = to_tf32(x.w);
         }
-        tmem_st32(tl + col0 + cc, v);
+        if (SP && wg == 1) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(smem_raw + smem_shift + Cfg::OFF_DO + sw128_offset(r, cc + i, 128)) =
+                make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+          tmem_st32(tl + col0 + cc, v);
+        }
       }
+      if (SP && wg == 1) fence_proxy_async_smem();   // dO, read by the tensor core
       tmem_st_wait();
       tc_fence_before();
       pdl_wait_prev();                     // the kernel before (D when given) has completed
@@ -551,14 +676,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // and pass-2 sub-chunk st's K, V for a stage st that pass 1 leaves
       // unused (CYC: pass-2 chunk 0 is issued after both stages' last pass-1
       // releases, or right away when pass 1 is skipped)
-      ok = GD || units_landed(0, 2 * min(nk, 2));
+      ok = GD || SP || units_landed(0, 2 * min(nk, 2));
       if constexpr (Cfg::CYC) {
-        if (ok && GD) ok = units_landed(p2_kv(0), 2);
+        if (ok && (GD || SP)) ok = units_landed(p2_kv(0), 2);
       } else {
         for (int st = 0; st < 2; ++st)
           if (ok && (GD || st >= nk) && st < n_sub) ok = units_landed(p2_kv(st), 2);
       }
       __syncwarp();
+      // SP: the warp's dO rows (each lane fenced its own) are released with
+      // the arrive
+      if (SP && wg == 1 && lane == 0) fence_acq_rel_cluster();
       if (ok && lane == 0) arrive_issuer<C>(&bars.qdo_ready);
     }
     const float sl2 = sh.scale * kLog2e;
@@ -571,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- pass 1: D = rowsum(P dP) ----
     constexpr int H1 = Cfg::BK1 / 2, H2 = Cfg::BK2 / 2;
     static_assert(H1 == 32 && (H2 == 16 || H2 == 32), "column split");
-    for (int c = 0; ok && !GD && c < nk; ++c) {
+    for (int c = 0; ok && !GD && !SP && c < nk; ++c) {
       const int st = c & 1;
       // units of the MMAs issued after this chunk's release of stage st:
       // chunk c + 2's K, V, or after the stage's last pass-1 use, those of
@@ -616,26 +744,94 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // both warpgroups' partial sums (each has finished reading the pass-1
     // stages), or the given D
-    float Drow;
-    if constexpr (GD) {
-      Drow = valid ? Dws[(long long)q * H + h] : 0.f;
-    } else {
+    // (SP: both formed after the single pass)
+    auto sum_d = [&]() {
       bars.dx[wg][r] = Dpart;
       tc_fence_before();
       asm volatile("bar.sync 2, 256;" ::: "memory");
-      Drow = bars.dx[0][r] + bars.dx[1][r];
-    }
+      return bars.dx[0][r] + bars.dx[1][r];
+    };
     // the key-major kernel's record of this row's column (the column of
     // Q^T / dO^T; padding rows get a record that masks the column out)
-    if (wg == 0) {
-      const long long col = (long long)q0 * G + r;
-      if (col < ld_meta && GQA_DCHECK(status, g < sh.Hk && col >= 0, kChkTcQmStore))
-        kmeta[(long long)g * ld_meta + col] =
-            valid ? make_float4(lse2, sh.scale * Drow, __int_as_float(q), __int_as_float(segq))
-                  : make_float4(0.f, 0.f, __int_as_float(-1), __int_as_float(0x7fffffff));
+    auto write_record = [&](float Dr) {
+      if (wg == 0) {
+        const long long col = (long long)q0 * G + r;
+        if (col < ld_meta && GQA_DCHECK(status, g < sh.Hk && col >= 0, kChkTcQmStore))
+          kmeta[(long long)g * ld_meta + col] =
+              valid ? make_float4(lse2, sh.scale * Dr, __int_as_float(q), __int_as_float(segq))
+                    : make_float4(0.f, 0.f, __int_as_float(-1), __int_as_float(0x7fffffff));
+      }
+    };
+    float Drow = 0.f;
+    if constexpr (GD) {
+      Drow = valid ? Dws[(long long)q * H + h] : 0.f;
+      write_record(Drow);
+    } else if constexpr (!SP) {
+      Drow = sum_d();
+      write_record(Drow);
     }
-    // ---- pass 2: dS = scale P (dP - D) over S, for dQ += dS K ----
-    if constexpr (Cfg::CYC) {
+    if constexpr (SP) {
+      // ---- single pass: P over S and P dP over dP, D += rowsum(P dP) ----
+      // By chunk j, its halves in hand-over order (QmCfg: c_first): half h of
+      // warpgroup wg is columns 16 wg + [0, 16) of the half's S and dP slots,
+      // keys 32 h + 16 wg + [0, 16) of the chunk. The first half's S (and the
+      // chunk's dP) is ready with s_full[0], the second's with s_full[1].
+      for (int j = 0; ok && j < nk; ++j) {
+        // units of the MMAs issued after this chunk's hand-backs: K^T of
+        // chunk j, and K', V of chunk j + 1
+        if (!(units_landed(3 * j + 2, 1) && (j + 1 >= nk || units_landed(p2_kv(j + 1), 2)))) {
+          ok = false;
+          break;
+        }
+        const int p = j & 1, kc = (kc0 + j) * Cfg::BK1;
+        for (int i = 0; i < 2; ++i) {
+          const int hh = Cfg::c_first(p) ^ i;
+          if (!mbar_wait<kCl>(&bars.s_full[i], j & 1, abort, status, kSiteQmCompute)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int k0 = kc + 32 * hh + 16 * wg;
+          const bool full = valid && k0 >= segq && k0 + 15 <= q;
+          const uint32_t ts = tl + Cfg::t_slot(Cfg::c_s_slot(p, hh)) + 16 * wg;
+          const uint32_t tdp = tl + Cfg::t_slot(Cfg::c_dp_slot(p, hh)) + 16 * wg;
+          float sv[16], dp[16];
+          tmem_ld16(ts, sv);
+          tmem_ld16(tdp, dp);
+          tmem_ld_wait();
+          if (full) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const float pj = ex2(fmaf(sv[jj], sl2, -lse2));
+              const float x = pj * dp[jj];
+              Dpart += x;
+              sv[jj] = to_tf32(pj);
+              dp[jj] = to_tf32(x);
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) {
+              const int key = k0 + jj;
+              const bool vis = valid && key >= segq && key <= q;
+              const float pj = vis ? ex2(fmaf(sv[jj], sl2, -lse2)) : 0.f;
+              const float x = pj * dp[jj];
+              Dpart += x;
+              sv[jj] = to_tf32(pj);
+              dp[jj] = to_tf32(x);
+            }
+          }
+          tmem_st16(ts, sv);
+          tmem_st16(tdp, dp);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) arrive_issuer<C>(&bars.s_free[i]);
+        }
+      }
+      // every compute warp gets here (a failed wait only skips work)
+      Drow = sum_d();
+      write_record(Drow);
+    } else if constexpr (Cfg::CYC) {
       // by chunk j, its halves in hand-over order (QmCfg: c_first): half h of
       // warpgroup wg is columns 16 wg + [0, 16) of the half's S and dP slots,
       // keys 32 h + 16 wg + [0, 16) of the chunk. The first half's S (and the
@@ -744,8 +940,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       for (int cc = wg * (D / 2); cc < (wg + 1) * (D / 2); cc += 16) {
         float v[16];
-        tmem_ld16(tl + Cfg::T_DQ + cc, v);
-        tmem_ld_wait();
+        if constexpr (SP) {
+          // dQ = scale (U - D W)
+          float w[16];
+          tmem_ld16(tl + Cfg::T_U + cc, v);
+          tmem_ld16(tl + Cfg::T_W + cc, w);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = sh.scale * fmaf(-Drow, w[i], v[i]);
+        } else {
+          tmem_ld16(tl + Cfg::T_DQ + cc, v);
+          tmem_ld_wait();
+        }
         if (valid) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] = (v[i] == v[i]) ? v[i] : 0.f;
@@ -1907,13 +2113,24 @@ gqa_status km_launch(const float* Q, const float* K, const float* V, const float
 #undef GQA_KM_ARGS
 }
 
-template <int D, int C, bool GD>
+// Query-major form at d = 128 on SM pairs without a given D: the single
+// pass (QmCfg::SP, the default) or the two passes (GQA_QM_TWO_PASS=1). Read
+// once per process.
+bool qm_single_pass() {
+  static bool sp = [] {
+    const char* e = getenv("GQA_QM_TWO_PASS");
+    return !(e != nullptr && atoi(e) == 1);
+  }();
+  return sp;
+}
+
+template <int D, int C, bool GD, bool SP = false>
 gqa_status qm_launch_c(const float* Q, const float* K, const float* V, const float* dO,
                        const float* LSE, const uint32_t* seg, float* dQ, const float* Kt,
                        long long ld_kt, const float* Kp, long long rows_kp, float4* kmeta,
                        long long ld_meta, float* Dws, float* Qt, float* dOt, long long ld_qt,
                        uint32_t* status, const Shape& sh, cudaStream_t st, const RopeParams& rope) {
-  using Cfg = QmCfg<D, C>;
+  using Cfg = QmCfg<D, C, SP>;
   CUtensorMap mk, mv, mkt;
   gqa_status r;
   const long long kv_panels = (long long)sh.Hk * D / 32;
@@ -1925,7 +2142,7 @@ gqa_status qm_launch_c(const float* Q, const float* K, const float* V, const flo
     return r;
   if ((r = map_panels(&mv, V, (long long)sh.Hk * D, sh.S, kv_panels, Cfg::HALF1, D / 32)) != GQA_OK) return r;
   if ((r = map_panels(&mkt, Kt, ld_kt, (long long)sh.Hk * D, ld_kt / 32, Cfg::KT_ROWS, Cfg::KT_PANELS)) != GQA_OK) return r;
-  if (cudaFuncSetAttribute(tc_query_major<D, C, GD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tc_query_major<D, C, GD, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess)
     return check_launch("query-major smem attribute");
   const int QR = 128 / sh.G;
@@ -1934,7 +2151,7 @@ gqa_status qm_launch_c(const float* Q, const float* K, const float* V, const flo
   // one CTA per SM (the kernel holds all of TMEM): slab-major below four waves
   const int slab_major = (long long)n_sg * C * sh.Hk < 4LL * sm_count() ? 1 : 0;
   const dim3 grid = slab_major ? dim3(C * sh.Hk, n_sg) : dim3(n_sg * C, sh.Hk);
-  return launch_clustered(tc_query_major<D, C, GD>, grid, C, Cfg::SMEM_BYTES, st,
+  return launch_clustered(tc_query_major<D, C, GD, SP>, grid, C, Cfg::SMEM_BYTES, st,
                           "tensor-core query-major", mk, mv, mkt, Q, dO, LSE, seg, dQ, Dws, Qt, dOt,
                           ld_qt, kmeta, ld_meta, status, sh, rope, slab_major);
 }
@@ -1953,6 +2170,9 @@ gqa_status qm_launch(const float* Q, const float* K, const float* V, const float
     return qm_launch_c<D, 2, true>(GQA_QM_ARGS);
   }
   if (cta_group() == 1) return qm_launch_c<D, 1, false>(GQA_QM_ARGS);
+  if constexpr (QmCfg<D, 2>::CYC) {
+    if (qm_single_pass()) return qm_launch_c<D, 2, false, true>(GQA_QM_ARGS);
+  }
   return qm_launch_c<D, 2, false>(GQA_QM_ARGS);
 #undef GQA_QM_ARGS
 }

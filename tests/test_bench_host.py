@@ -19,6 +19,15 @@ def test_counted_flops_and_pairs():
     assert bench.executed_flops(128, 32, pairs) == pytest.approx(bench.counted_flops(128, 32, pairs) * 9 / 5)
 
 
+def test_executed_contractions():
+    assert bench.executed_contractions(128, False, {}) == 8
+    assert bench.executed_contractions(64, False, {}) == 9
+    assert bench.executed_contractions(128, True, {}) == 7
+    assert bench.executed_contractions(128, False, {"GQA_QM_TWO_PASS": "1"}) == 9
+    assert bench.executed_contractions(128, False, {"GQA_TC_CTA_GROUP": "1"}) == 9
+    assert bench.executed_contractions(128, False, {"GQA_TC_CTA_GROUP": "2"}) == 8
+
+
 def test_tf32_peak_from_measured_bf16():
     p = {"bf16_tflops": 1925.9, "bf16_tflops_sustained": 1732.4}
     assert bench.tf32_peak(p, sustained=False) == pytest.approx(1925.9 * 1100 / 2250)

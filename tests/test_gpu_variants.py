@@ -1,8 +1,9 @@
 """Both tensor-core backward kernels run on SM pairs (cta_group::2, M = 256) by
 default; GQA_TC_CTA_GROUP=1 selects the one-SM variants (one query slab / one
-key tile per SM). The group size is read once per process, so the variant runs
-in a child process, against the oracle on edge shapes (ragged tails, documents,
-all head dims)."""
+key tile per SM). At d = 128 on SM pairs the query-major kernel runs its single
+pass by default; GQA_QM_TWO_PASS=1 selects the two-pass form. Both switches are
+read once per process, so each variant runs in a child process, against the
+oracle on edge shapes (ragged tails, documents, all head dims)."""
 import os
 import subprocess
 import sys
@@ -37,13 +38,21 @@ print("ok")
 """
 
 
-def test_single_sm_kernels_match_oracle():
+def _run_variant(env_var):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from causal_gqa_attention_attn_gb300 import build
     build.build()
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, GQA_TC_CTA_GROUP="1")
+    env = dict(os.environ, **{env_var: "1"})
     p = subprocess.run([sys.executable, "-c", _SCRIPT.format(root=root)], env=env,
                        capture_output=True, text=True, timeout=600)
     assert p.returncode == 0 and "ok" in p.stdout, p.stdout + p.stderr
+
+
+def test_single_sm_kernels_match_oracle():
+    _run_variant("GQA_TC_CTA_GROUP")
+
+
+def test_two_pass_query_major_matches_oracle():
+    _run_variant("GQA_QM_TWO_PASS")

@@ -2,7 +2,8 @@
 operand layouts (no GPU).
 
 Both backward kernels, at d = 128 on SM pairs, cycle four 32-column TMEM
-slots by halves of a block (key-major) or chunk (query-major). The slot
+slots by halves of a block (key-major) or chunk (query-major, in both its
+two-pass and single-pass forms). The slot
 functions below restate KmCfg::w_s_slot / w_dp_slot / w_first and
 QmCfg::c_s_slot / c_dp_slot / c_first of csrc/tc_bwd.cu; the tests replay the
 MMA issue order of each kernel (the tensor core runs MMAs in issue order)
@@ -149,6 +150,88 @@ def run_query_major(n_chunks):
         dq(j, hl)
         if more:
             s_half(j + 1, hf)
+
+
+def run_query_major_single_pass(n_chunks):
+    """Query-major single pass (QmCfg::SP): the softmax writes P over S and
+    P dP over dP; after the first half's hand-back W_f(j) (reads the S slot),
+    U_f(j) (reads the dP slot), dP(j+1); after the second's U_l(j), the next
+    chunk's first S half, W_l(j), the next chunk's second S half."""
+    t = Tmem()
+
+    def dp_pair(j):
+        p = j & 1
+        t.write(dp_slot(p, 0), ("dP", j, 0))
+        t.write(dp_slot(p, 1), ("dP", j, 1))
+
+    def s_half(j, h):
+        t.write(s_slot(j & 1, h), ("S", j, h))
+
+    def softmax(j, h):
+        p = j & 1
+        t.expect(s_slot(p, h), ("S", j, h))
+        t.expect(dp_slot(p, h), ("dP", j, h))
+        t.write(s_slot(p, h), ("P", j, h))
+        t.write(dp_slot(p, h), ("PdP", j, h))
+
+    def w(j, h):
+        t.expect(s_slot(j & 1, h), ("P", j, h))
+
+    def u(j, h):
+        t.expect(dp_slot(j & 1, h), ("PdP", j, h))
+
+    dp_pair(0)
+    s_half(0, first(0))
+    s_half(0, first(0) ^ 1)
+    for j in range(n_chunks):
+        more = j + 1 < n_chunks
+        hf = first(j & 1)
+        hl = hf ^ 1
+        softmax(j, hf)
+        burst_f = {s_slot(j & 1, hf), dp_slot(j & 1, hf)}
+        if more:
+            assert {dp_slot((j + 1) & 1, 0), dp_slot((j + 1) & 1, 1)} == burst_f
+        assert not burst_f & {s_slot(j & 1, hl), dp_slot(j & 1, hl)}
+        w(j, hf)
+        u(j, hf)
+        if more:
+            dp_pair(j + 1)
+        softmax(j, hl)
+        u(j, hl)
+        if more:
+            s_half(j + 1, hl)
+            nxt = {s_slot((j + 1) & 1, hl), dp_slot((j + 1) & 1, hl)}
+            assert not nxt & {s_slot(j & 1, hl), s_slot((j + 1) & 1, hf)}
+        w(j, hl)
+        if more:
+            s_half(j + 1, hf)
+
+
+@pytest.mark.parametrize("n", range(1, 9))
+def test_query_major_single_pass_schedule(n):
+    run_query_major_single_pass(n)
+
+
+def sw128_offset(row, col, rows):
+    return (col // 32) * rows * 128 + row * 128 + ((((col % 32) // 4) ^ (row % 8)) * 16) + (col % 4) * 4
+
+
+def test_single_pass_do_tile_layout():
+    """The compute warps store the slab's dO rows (128 rows x 128 floats) as
+    four 16 KB panels of 128-byte rows with the 16-byte chunks of row r XORed
+    by r % 8: every float lands once inside the 64 KB tile, and the K step ks
+    descriptor offset (panel ks / 4, 32 bytes per step inside the row) finds
+    column 8 ks of row 0."""
+    offs = {sw128_offset(r, c, 128) for r in range(128) for c in range(128)}
+    assert len(offs) == 128 * 128 and min(offs) == 0 and max(offs) == 65536 - 4
+    assert all(o % 4 == 0 for o in offs)
+    for ks in range(16):
+        assert sw128_offset(0, 8 * ks, 128) == (ks // 4) * 16384 + (ks % 4) * 32
+    # a quarter warp (8 consecutive rows) storing the same 16-byte chunk hits
+    # eight distinct 16-byte bank groups
+    for c in range(0, 32, 4):
+        for r0 in range(0, 128, 8):
+            assert len({sw128_offset(r, c, 128) % 128 for r in range(r0, r0 + 8)}) == 8
 
 
 @pytest.mark.parametrize("n", range(1, 9))
