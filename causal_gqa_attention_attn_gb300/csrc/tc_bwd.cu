@@ -185,6 +185,19 @@ __device__ __forceinline__ void arrive_issuer(uint64_t* bar) {
 // next kernel of the stream start once every CTA of this one runs, and wait
 // until the previous kernel has completed with its writes visible. Both are
 // no-ops for a kernel not launched as a dependent.
+// Make this thread's ordinary shared-memory writes visible to the async
+// proxy (the tensor core's operand reads), before the barrier arrive that
+// hands them over.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Release at cluster scope ahead of a relaxed remote arrive: the writes this
+// thread has made or observed become visible to the CTA that acquires the
+// barrier.
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
 __device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait_prev() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
@@ -805,8 +818,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float pj = ex2(fmaf(sv[jj], sl2, -lse2));
               const float x = pj * dp[jj];
               Dpart += x;
-              sv[jj] = to_tf32(pj);
-              dp[jj] = to_tf32(x);
+              sv[jj] = pj;
+              dp[jj] = x;
             }
           } else {
 #pragma unroll
@@ -816,8 +829,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float pj = vis ? ex2(fmaf(sv[jj], sl2, -lse2)) : 0.f;
               const float x = pj * dp[jj];
               Dpart += x;
-              sv[jj] = to_tf32(pj);
-              dp[jj] = to_tf32(x);
+              sv[jj] = pj;
+              dp[jj] = x;
             }
           }
           tmem_st16(ts, sv);
@@ -862,14 +875,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (full) {
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj)
-              sv[jj] = to_tf32(sh.scale * ex2(fmaf(sv[jj], sl2, -lse2)) * (dp[jj] - Drow));
+              sv[jj] = sh.scale * ex2(fmaf(sv[jj], sl2, -lse2)) * (dp[jj] - Drow);
           } else {
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
               const int key = k0 + jj;
               const bool vis = valid && key >= segq && key <= q;
               const float pj = vis ? ex2(fmaf(sv[jj], sl2, -lse2)) : 0.f;
-              sv[jj] = to_tf32(sh.scale * pj * (dp[jj] - Drow));
+              sv[jj] = sh.scale * pj * (dp[jj] - Drow);
             }
           }
           tmem_st16(ts, sv);
@@ -915,14 +928,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (full) {
 #pragma unroll
         for (int j = 0; j < H2; ++j)
-          sv[j] = to_tf32(sh.scale * ex2(fmaf(sv[j], sl2, -lse2)) * (dp[j] - Drow));
+          sv[j] = sh.scale * ex2(fmaf(sv[j], sl2, -lse2)) * (dp[j] - Drow);
       } else {
 #pragma unroll
         for (int j = 0; j < H2; ++j) {
           const int key = kc + Cfg::key_of(hh, n0 + j);
           const bool vis = valid && key >= segq && key <= q;
           const float pj = vis ? ex2(fmaf(sv[j], sl2, -lse2)) : 0.f;
-          sv[j] = to_tf32(sh.scale * pj * (dp[j] - Drow));
+          sv[j] = sh.scale * pj * (dp[j] - Drow);
         }
       }
       if constexpr (H2 == 16) tmem_st16(ts, sv);
@@ -1155,7 +1168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int smem_shift = (int)(smem - smem_raw);   // 0 .. 1023
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int G = sh.G, QB = NQ / G;        // queries per block
-  const int S = sh.S, H = sh.H;
+  const int S = sh.S;
   const uint32_t rank = (C > 1) ? cluster_ctarank() : 0u;
   const bool issuer = rank == 0;          // issues the group's MMAs
   // Dispatch order: grid (C * band, Hk / band * n_tg), CTAs start x-fastest:
@@ -1225,7 +1238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // C = 2 this CTA loads its half of each block.
     const int pw = warp;
     // debug build: the group's heads and rows exist (recorded only, as above)
-    (void)GQA_DCHECK(status, g < sh.Hk && (g + 1) * G <= H && kg0 < S, kChkTcKmLoad);
+    (void)GQA_DCHECK(status, g < sh.Hk && (g + 1) * G <= sh.H && kg0 < S, kChkTcKmLoad);
     if (elect_one()) {
       if (pw == 0) {
         tma_prefetch_desc(&mapQ);
@@ -1499,7 +1512,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = 32 * (warp & 3) + lane;
     const int key = k0 + r;
     const uint32_t tl = lane_base(tmem, warp);
-    const int wt = threadIdx.x - 32 * kFirstCompute - 128 * wg;   // 0..127 within the warpgroup
     // (debug build: this kv head's K / dK / dV columns exist)
     const bool g_ok = GQA_DCHECK(status, g < sh.Hk, kChkTcKmLoad);
     {
@@ -1569,9 +1581,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every (key, column) of the block visible: key <= first query and >= every seg
       const int q_first = qb * QB;
       const bool full = key <= q_first && key >= (int)maxseg && q_first + QB - 1 < S;
-      // P^T = 2^(s log2e scale - lse log2e) and dS^T = P (scale dP - scale D),
-      // both rounded to TF32, over NC columns: S^T at TMEM column ts, dP^T at
-      // tdp, the columns' records at mt
+      // P^T = 2^(s log2e scale - lse log2e) and dS^T = P (scale dP - scale D)
+      // over NC columns: S^T at TMEM column ts, dP^T at tdp, the columns'
+      // records at mt. Both go to the tensor core unrounded (it keeps the top
+      // 19 bits of each): a rounding here would add two ALU operations per
+      // element to the softmax, which the next MMAs wait for.
       auto softmax_cols = [&](auto nc, uint32_t ts, uint32_t tdp, const float4* mt) {
         constexpr int NC = decltype(nc)::value;
         float sv[NC], dp[NC];
@@ -1588,8 +1602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < NC; ++j) {
             const float4 m = mt[j];
             const float pj = ex2(fmaf(sv[j], sl2, -m.x));
-            sv[j] = to_tf32(pj);
-            dp[j] = to_tf32(pj * fmaf(dp[j], sh.scale, -m.y));
+            sv[j] = pj;
+            dp[j] = pj * fmaf(dp[j], sh.scale, -m.y);
           }
         } else {
 #pragma unroll
@@ -1598,8 +1612,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int q = __float_as_int(m.z), sq = __float_as_int(m.w);
             const bool vis = key <= q && key >= sq;        // q = -1 for padding columns
             const float pj = vis ? ex2(fmaf(sv[j], sl2, -m.x)) : 0.f;
-            sv[j] = to_tf32(pj);
-            dp[j] = to_tf32(pj * fmaf(dp[j], sh.scale, -m.y));
+            sv[j] = pj;
+            dp[j] = pj * fmaf(dp[j], sh.scale, -m.y);
           }
         }
         if constexpr (NC == 16) {

@@ -37,18 +37,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-// Make this thread's ordinary shared-memory writes visible to the async
-// proxy (the tensor core's operand reads), before the barrier arrive that
-// hands them over.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-// Release at cluster scope ahead of a relaxed remote arrive: the writes
-// this thread has made or observed become visible to the CTA that acquires
-// the barrier.
-__device__ __forceinline__ void fence_acq_rel_cluster() {
-  asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
@@ -401,7 +389,10 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool a_mn_major,
 
 // Round to TF32 (10 mantissa bits; the low 13 bits of the fp32 pattern
 // cleared), to nearest with ties away from zero, for operands this code
-// writes itself (P, dS, the TMEM copies of Q, dO and K). On the sign-magnitude
+// writes once per tile (the TMEM copies of Q, dO and K) and the forward's P.
+// (The tensor core itself keeps the top 19 bits of an fp32 operand, that is
+// truncates; the backward's per-element softmax outputs go to it unrounded,
+// as the TMA-loaded operands do.) On the sign-magnitude
 // bit pattern, adding half a TF32 unit in the last place (bit 12) and then
 // truncating rounds the magnitude to nearest, ties up; a mantissa carry moves
 // into the exponent, which is the correctly rounded next binade. Two integer
