@@ -389,10 +389,10 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool a_mn_major,
 
 // Round to TF32 (10 mantissa bits; the low 13 bits of the fp32 pattern
 // cleared), to nearest with ties away from zero, for operands this code
-// writes once per tile (the TMEM copies of Q, dO and K) and the forward's P.
-// (The tensor core itself keeps the top 19 bits of an fp32 operand, that is
-// truncates; the backward's per-element softmax outputs go to it unrounded,
-// as the TMA-loaded operands do.) On the sign-magnitude
+// writes once per tile (the TMEM copies of Q, dO and K). (The tensor core
+// itself keeps the top 19 bits of an fp32 operand, that is truncates; the
+// per-element softmax outputs P and dS go to it unrounded, as the TMA-loaded
+// operands do.) On the sign-magnitude
 // bit pattern, adding half a TF32 unit in the last place (bit 12) and then
 // truncating rounds the magnitude to nearest, ties up; a mantissa carry moves
 // into the exponent, which is the correctly rounded next binade. Two integer

@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int j = 0; j < BK; ++j) {
         const float pj = (sv[j] > -1e29f) ? ex2(sv[j] - m) : 0.f;
         sum += pj;
-        sv[j] = to_tf32(pj);
+        sv[j] = pj;
       }
       l += sum;
       tmem_st32(ts, sv);
