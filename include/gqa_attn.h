@@ -68,8 +68,8 @@ gqa_status attn_fwd_lse(const float* Q, const float* K, const float* V, const ui
  * and LSE overwritten, same definitions and arguments), on tensor cores for
  * head_dim 32, 64, 128 (tcgen05 kind::tf32: S = scale Q.K^T with TF32
  * operands, fp32 accumulation; one pass over the visible keys with an online
- * softmax: a running row max m and sum l, P = exp(s - m) rounded to TF32 and
- * O += P V, the accumulator rescaled when m rises; at the end O = O / l and
+ * softmax: a running row max m and sum l, P = exp(s - m) (a TF32 operand of
+ * O += P V), the accumulator rescaled when m rises; at the end O = O / l and
  * LSE = m + ln l), else on CUDA cores.
  * workspace: >= attn_fwd_workspace_bytes(...) device bytes, caller-owned (a
  * status header and a transposed copy of V). Bounded device waits report
@@ -137,7 +137,10 @@ size_t attn_bwd_workspace_bytes(int seq_len, int n_heads, int n_kv_heads, int he
  * off; otherwise head_dim 32, 64 or 128 runs the tensor-core path where it is
  * built, and other multiples of 4 up to 128 the CUDA-core path
  * (attn_bwd_simt). The result stays within fp32/TF32 rounding of the exact
- * value; which path ran decides the rounding.
+ * value; which path ran decides the rounding. (At head_dim 128 the
+ * tensor-core path forms dQ in one pass over the keys as
+ * scale * (sum_j P_ij dP_ij k_j - D_i sum_j P_ij k_j), equal to sum_j dS_ij k_j
+ * in exact arithmetic.)
  */
 gqa_status attn_bwd(const float* Q, const float* K, const float* V, const float* dO,
                     const float* LSE, const uint32_t* seg, float* dQ, float* dK, float* dV,
