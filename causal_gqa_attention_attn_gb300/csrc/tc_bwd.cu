@@ -201,18 +201,12 @@ __device__ __forceinline__ void fence_acq_rel_cluster() {
   asm volatile("fence.acq_rel.cluster;" ::: "memory");
 }
 
-// Gradient tiles leave through the TMA unit: dst += the box at src (shared
+// The dQ tile leaves through the TMA unit: dst += the box at src (shared
 // memory, in the tensor map's box layout), one add per element, as a
-// read-modify-write would make, without the reads. Coordinates are never
-// negative here; rows past the tensor's end are not written.
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x, int y,
-                                                  int z) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          map),
-      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
+// read-modify-write would make, without the reads (dQ may be formed by a
+// reduction; dK and dV keep their owned read-modify-writes, no global
+// atomics). Coordinates are never negative here; rows past the tensor's end
+// are not written.
 __device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* map, const void* src, int x, int y,
                                                   int z, int w) {
   asm volatile(
@@ -239,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap mapKt, const __grid_constant__ CUtensorMap mapDQ,
                    const float* __restrict__ Q, const float* __restrict__ dO,
                    const float* __restrict__ LSE, const uint32_t* __restrict__ seg,
-                   float* __restrict__ dQ, float* __restrict__ Dws, float* __restrict__ Qt,
+                   float* __restrict__ Dws, float* __restrict__ Qt,
                    float* __restrict__ dOt, long long ld_qt, float4* __restrict__ kmeta,
                    long long ld_meta, uint32_t* __restrict__ status, Shape sh,
                    const RopeParams rope, int slab_major) {
@@ -1135,10 +1129,6 @@ struct KmCfg {
   static constexpr int QSUB_PANEL_BYTES = BLK_PANEL_BYTES / 2;
   static_assert(!W_ || (NS == 1 && NQ == 64 && C == 2 && QSUB_PANEL_BYTES % 1024 == 0),
                 "slot cycling: one stage of 64-column blocks on SM pairs");
-  // the epilogue's dK box over V (the same 128 x d tile) and dV box over the
-  // Q / dO stages
-  static_assert(V_BYTES == 128 * D * 4 && NSQ * 2 * BLK_BYTES >= V_BYTES && OFF_QDO % 1024 == 0,
-                "gradient boxes in idle shared memory");
 };
 
 struct KmBarriers {
@@ -1188,8 +1178,7 @@ template <int D, int C, bool W>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_key_major(const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapQ,
                  const __grid_constant__ CUtensorMap mapDO, const __grid_constant__ CUtensorMap mapQt,
-                 const __grid_constant__ CUtensorMap mapDOt, const __grid_constant__ CUtensorMap mapDK,
-                 const __grid_constant__ CUtensorMap mapDV, const float* __restrict__ K,
+                 const __grid_constant__ CUtensorMap mapDOt, const float* __restrict__ K,
                  const float4* __restrict__ kmeta, long long ld_meta,
                  const uint32_t* __restrict__ blk_minseg, const uint4* __restrict__ blk_maxseg,
                  float* __restrict__ dK,
@@ -1703,19 +1692,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // epilogue: warpgroup 0 adds dK (rotated by the RoPE backward of the key's
-    // position when rope.on), warpgroup 1 adds dV (owned rows, NaN-guarded):
-    // each writes its 128 x d tile to shared memory (dK over the V tile, dV
-    // over the Q / dO stages, both idle once the last MMA has completed) in
-    // the layout of the tensor map's box, and one thread of the warpgroup
-    // adds the box to dK / dV with a TMA reduce (rows past the sequence are
-    // not written). With n_split > 1 each part stores its partial sums
-    // instead (zeros when it saw no block); km_split_reduce adds them up.
-    const bool own = n_split == 1;
-    unsigned char* tile = smem_raw + smem_shift + (wg == 0 ? Cfg::OFF_V : Cfg::OFF_QDO);
-    const bool ep = ok && mbar_wait<kCl>(&bars.acc_done, 0, abort, status, kSiteKmCompute);
-    if (ep) {
+    // position when rope.on), warpgroup 1 adds dV (owned rows, NaN-guarded).
+    // With n_split > 1 each part stores its partial sums instead (zeros when
+    // it saw no block); km_split_reduce adds them up.
+    if (ok && mbar_wait<kCl>(&bars.acc_done, 0, abort, status, kSiteKmCompute)) {
       tc_fence_after();
       const long long row = (long long)key * sh.Hk * D + (long long)g * D;
+      float* dst_row = (wg == 0 ? dK : dV) + row;
       const uint32_t src = tl + (wg == 0 ? Cfg::T_DK : Cfg::T_DV);
       float* part_row = parts + ((size_t)(wg * n_split + part) * S) * ((size_t)sh.Hk * D) + row;
       for (int cc = 0; cc < D; cc += 32) {
@@ -1734,36 +1717,26 @@ __global__ void __launch_bounds__(kThreads, 1)
               pp[i] = n > 0 ? make_float4(a[4 * i], a[4 * i + 1], a[4 * i + 2], a[4 * i + 3])
                             : make_float4(0.f, 0.f, 0.f, 0.f);
           }
-        } else {
-          if (key < S && n > 0 && g_ok) {
+        } else if (key < S && n > 0 && g_ok &&
+                   GQA_DCHECK(status, row + D <= (long long)S * sh.Hk * D, kChkTcKmStore)) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = (a[i] == a[i]) ? a[i] : 0.f;
-            if (wg == 0 && rope.on) {
-              const long long tpos = (long long)key + rope.pos_offset;
+          for (int i = 0; i < 32; ++i) a[i] = (a[i] == a[i]) ? a[i] : 0.f;
+          if (wg == 0 && rope.on) {
+            const long long tpos = (long long)key + rope.pos_offset;
 #pragma unroll
-              for (int j = 0; j < 16; ++j) rope_rotate(a[2 * j], a[2 * j + 1], tpos, cc / 2 + j, rope);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = 0.f;
+            for (int j = 0; j < 16; ++j) rope_rotate(a[2 * j], a[2 * j + 1], tpos, cc / 2 + j, rope);
           }
+          float4* pk = reinterpret_cast<float4*>(dst_row + cc);
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(tile + sw128_offset(r, cc + i, 128)) =
-                make_float4(a[i], a[i + 1], a[i + 2], a[i + 3]);
+          for (int i = 0; i < 8; ++i) {
+            float4 o = pk[i];
+            o.x += a[4 * i];
+            o.y += a[4 * i + 1];
+            o.z += a[4 * i + 2];
+            o.w += a[4 * i + 3];
+            pk[i] = o;
+          }
         }
-      }
-      if (own) fence_proxy_async_smem();   // the box, read by the TMA unit
-    }
-    if (own) {
-      // the warpgroup's 128 threads (a failed wait skips only work); no box
-      // is added after a failed wait or by a tile pair that saw no block
-      if (wg == 0) asm volatile("bar.sync 3, 128;" ::: "memory");
-      else asm volatile("bar.sync 4, 128;" ::: "memory");
-      if (warp == kFirstCompute + 4 * wg && lane == 0 && *abort == 0 && n > 0 && g_ok &&
-          GQA_DCHECK(status, k0 < S, kChkTcKmStore)) {
-        tma_reduce_add_3d(wg == 0 ? &mapDK : &mapDV, tile, 0, k0, g * (D / 32));
-        bulk_commit_wait_read();
       }
     }
   }
@@ -2051,7 +2024,7 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
                        cudaStream_t st, const RopeParams& rope, int n_split, float* parts) {
   using Cfg = KmCfg<D, C, W>;
   const int QB = Cfg::NQ / sh.G;
-  CUtensorMap mv, mq, mdo, mqt, mdot, mdk, mdv;
+  CUtensorMap mv, mq, mdo, mqt, mdot;
   gqa_status r;
   const long long kv_panels = (long long)sh.Hk * D / 32;
   if ((r = map_panels(&mv, V, (long long)sh.Hk * D, sh.S, kv_panels, 128, D / 32)) != GQA_OK) return r;
@@ -2061,9 +2034,6 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
   if ((r = map_heads(&mdo, dO, D, sh.H, sh.S, sh.G, QB / C)) != GQA_OK) return r;
   if ((r = map_panels(&mqt, Qt, ld_qt, (long long)sh.Hk * D, ld_qt / 32, Cfg::DH, Cfg::T_PANELS)) != GQA_OK) return r;
   if ((r = map_panels(&mdot, dOt, ld_qt, (long long)sh.Hk * D, ld_qt / 32, Cfg::DH, Cfg::T_PANELS)) != GQA_OK) return r;
-  // the epilogue's reduces into dK / dV: one 128-key tile per box, like V's
-  if ((r = map_panels(&mdk, dK, (long long)sh.Hk * D, sh.S, kv_panels, 128, D / 32)) != GQA_OK) return r;
-  if ((r = map_panels(&mdv, dV, (long long)sh.Hk * D, sh.S, kv_panels, 128, D / 32)) != GQA_OK) return r;
   if (cudaFuncSetAttribute(tc_key_major<D, C, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess)
     return check_launch("key-major smem attribute");
@@ -2075,7 +2045,7 @@ gqa_status km_launch_c(const float* Q, const float* K, const float* V, const flo
   const int band = few_waves ? sh.Hk : (sh.Hk % 2 == 0 ? 2 : 1);
   const dim3 grid(C * band, (sh.Hk / band) * n_tg * n_split);
   r = launch_clustered(tc_key_major<D, C, W>, grid, C, Cfg::SMEM_BYTES, st,
-                                  "tensor-core key-major", mv, mq, mdo, mqt, mdot, mdk, mdv, K, kmeta, ld_meta,
+                                  "tensor-core key-major", mv, mq, mdo, mqt, mdot, K, kmeta, ld_meta,
                                   blk_minseg, blk_maxseg, dK, dV, status, sh, rope, band, n_split,
                                   parts);
   if (r != GQA_OK || n_split == 1) return r;
@@ -2234,7 +2204,7 @@ gqa_status qm_launch_c(const float* Q, const float* K, const float* V, const flo
   const int slab_major = (long long)n_sg * C * sh.Hk < 4LL * sm_count() ? 1 : 0;
   const dim3 grid = slab_major ? dim3(C * sh.Hk, n_sg) : dim3(n_sg * C, sh.Hk);
   return launch_clustered(tc_query_major<D, C, GD, SP>, grid, C, Cfg::SMEM_BYTES, st,
-                          "tensor-core query-major", mk, mv, mkt, mdq, Q, dO, LSE, seg, dQ, Dws, Qt, dOt,
+                          "tensor-core query-major", mk, mv, mkt, mdq, Q, dO, LSE, seg, Dws, Qt, dOt,
                           ld_qt, kmeta, ld_meta, status, sh, rope, slab_major);
 }
 
