@@ -234,6 +234,24 @@ def test_single_pass_do_tile_layout():
             assert len({sw128_offset(r, c, 128) % 128 for r in range(r0, r0 + 8)}) == 8
 
 
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16, 32])
+def test_dq_box_rows_match_tmem_rows(G):
+    """The query-major epilogue writes TMEM lane r (query r // G of the slab,
+    head r % G of the kv group) at sw128_offset(r, col, 128) and adds the
+    tile to dQ as one TMA box over dQ's (32 floats, heads, queries, d/32
+    panels) view, box (32, G, 128 / G, d/32). TMA lays a box out innermost
+    coordinate first in 128-byte rows, swizzled by the row's index modulo 8,
+    so element (x, head, query, panel) must be where lane r put it."""
+    QR, d = 128 // G, 128
+    for r in range(128):
+        qi, h = r // G, r % G
+        for col in range(0, d, 7):
+            panel, x = col // 32, col % 32
+            box_row = (panel * QR + qi) * G + h        # 128-byte row of the box
+            expect = box_row * 128 + (((x // 4) ^ (box_row % 8)) * 16) + (x % 4) * 4
+            assert sw128_offset(r, col, 128) == expect
+
+
 @pytest.mark.parametrize("n", range(1, 9))
 def test_key_major_slot_schedule(n):
     run_key_major(n)
