@@ -1,9 +1,10 @@
 """Benchmark: causal GQA attention backward from a saved LSE on GB300.
 
 One step = the whole hot path over one batch of synthetic input: zero the
-gradient buffers, attention backward (D pre-pass, key-tile and query-tile
-work), then the interleaved RoPE backward on dQ and dK (the 16k-token
-workload's recipe). Metric: attention-backward TFLOP/s counted over unmasked
+gradient buffers, attention backward (query-tile work: D and dQ, in one pass
+over the keys at head_dim 128 on SM pairs; key-tile work: dK and dV), then
+the interleaved RoPE backward on dQ and dK, fused into the final writes (the
+16k-token workload's recipe). Metric: attention-backward TFLOP/s counted over unmasked
 (query, key) pairs, 10 * head_dim * n_heads * N_pairs per step (five d-deep
 contractions per pair and head), and the fraction of the dense TF32 tensor
 peak.
