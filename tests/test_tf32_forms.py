@@ -97,7 +97,8 @@ def test_one_pass_identity_is_exact():
     assert np.max(np.abs(bad - ref)) > 1e-2 * np.max(np.abs(ref))
 
 
-@pytest.mark.parametrize("name,gain", [("docs2k", 1.0), ("docs2k", 2.0), ("causal512", 1.0)])
+@pytest.mark.parametrize("name,gain", [("docs2k", 1.0), ("docs2k", 2.0), ("causal512", 1.0),
+                                       ("docs4k", 1.0), ("docs4k", 2.0)])
 def test_one_pass_tf32_error_matches_two_pass(name, gain):
     x, lse, rows, ref = _case(name, gain)
     m = np.max(np.abs(ref))
